@@ -1,0 +1,64 @@
+/*
+ * dsa_oracle.h — CPU oracle of the DSA indexer path (TEST INFRASTRUCTURE ONLY).
+ *
+ * Only the test suite, the smoke check and the benchmark's CPU-baseline leg
+ * load this library. The CUDA product library never includes, links or calls
+ * it, and it shares no code with that library.
+ *
+ * Everything here is plain, slow and written to be checked by eye against
+ * the definitions it follows. Floating point work is fp64 on dequantised
+ * values, except where a quantised code is decided: that decision is taken
+ * in fp32, the precision the quantiser works in.
+ */
+#ifndef DSA_ORACLE_H
+#define DSA_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ORA_HEADS 64
+#define ORA_DIM 128
+#define ORA_BLOCK 64
+#define ORA_SLOT_BYTES 132                       /* 128 B FP8 K + 4 B fp32 scale */
+#define ORA_PAGE_BYTES (ORA_BLOCK * ORA_SLOT_BYTES) /* 8448 */
+
+/* E4M3 (OCP FP8) */
+double ora_e4m3_value(uint8_t code);
+uint8_t ora_e4m3_encode(float v);
+
+/* ue8m0 group scale and one group's quantisation */
+float ora_ue8m0_scale(float amax);
+void ora_quant_group(const float *x, int n, uint8_t *codes, float *scale);
+
+/* paged cache */
+void ora_slot_offsets(int64_t slot, int64_t *k_byte, int64_t *scale_byte);
+int64_t ora_k_quant_write(const uint16_t *k_bf16, int64_t n, const int64_t *slot_mapping,
+                          uint8_t *cache, int64_t num_blocks);
+void ora_q_quant(const uint16_t *q_bf16, int64_t rows, uint8_t *q_codes, float *q_scale);
+
+/* indexer scores and selection */
+void ora_logits_row(const uint8_t *q_codes, const float *q_scale, const float *w,
+                    const uint8_t *cache, const int32_t *bt_row, int64_t n_keys,
+                    double *out);
+void ora_topk_row(const double *scores, int64_t n, int k, int32_t *out);
+int64_t ora_indexer(const uint16_t *q_bf16, const float *w, const uint8_t *cache,
+                    const int32_t *block_table, int64_t bt_stride,
+                    const int32_t *req_id_per_token, const int64_t *positions,
+                    const int64_t *rows, int64_t n_rows, int topk,
+                    int32_t *topk_out, double *scores_out, int64_t scores_ld);
+
+/* logical -> physical ids, IndexCache schedule */
+void ora_convert(const int32_t *logical, int64_t n_tokens, int topk,
+                 const int32_t *req_id_per_token, const int32_t *block_table,
+                 int64_t bt_stride, int block_size, int block_stride_rows,
+                 int32_t *physical, int32_t *valid_counts);
+int ora_schedule(int n_layers, int use_index_cache, int freq, int offset,
+                 const char *pattern, char *fs_out, int32_t *producer_out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

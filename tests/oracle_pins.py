@@ -1,0 +1,420 @@
+"""Pins of the CPU oracle against facts fixed outside the oracle itself.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError
+if the oracle disagrees with a hand-worked value, a closed form, a library
+routine or a brute-force enumeration. ``test_oracle_pins.py`` runs them on
+the real oracle; ``test_oracle_mutants.py`` runs them on deliberately broken
+builds and requires that each break is caught.
+
+Sources: the web pages "IndexCache：DeepSeek 稀疏注意力中的跨层索引复用"
+(atomage.cn; its `Indexer`, FP8 indexer-cache, `SparseAttnIndexer` and layer
+schedule snippets), "PR #37735 完整报告" (prhub.com.cn; 关键源码片段 and
+风险与影响), the vLLM API page "vllm.v1.attention.backends.mla.index_group"
+(`_convert_once`), and the OCP 8-bit floating point specification.
+"""
+from __future__ import annotations
+
+import itertools
+import math
+import os
+
+import numpy as np
+import torch
+
+from dsa_sparse_attention_quant_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+SOFTMAX_SCALE = 128 ** -0.5
+HEAD_NORM = 64 ** -0.5
+
+
+def read_golden(name: str):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                rows.append(line.split())
+    return rows
+
+
+def torch_e4m3(values: np.ndarray) -> np.ndarray:
+    """Library E4M3 conversion (round to nearest even) with saturation to +-448."""
+    t = torch.from_numpy(np.ascontiguousarray(values, np.float32))
+    return t.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def torch_e4m3_value(codes: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(codes, np.uint8)).view(torch.float8_e4m3fn)
+    return t.to(torch.float64).numpy()
+
+
+def bf16(x) -> np.ndarray:
+    return synth.bf16_bits(np.asarray(x, np.float64))
+
+
+# ----------------------------------------------------------------- E4M3
+
+def pin_e4m3_golden(ora):
+    for value, code, *_ in read_golden("e4m3_codes.txt"):
+        got = ora.e4m3_encode(float(value))
+        assert got == int(code, 16), f"e4m3({value}) = {got:#04x}, expected {code}"
+
+
+def pin_e4m3_values_vs_library(ora):
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    lib = torch_e4m3_value(codes)
+    mine = np.array([ora.e4m3_value(int(c)) for c in codes])
+    assert np.array_equal(np.signbit(mine), np.signbit(lib))
+    assert np.array_equal(mine, lib)
+    assert math.isnan(ora.e4m3_value(0x7F)) and math.isnan(ora.e4m3_value(0xFF))
+    # round trip of every finite code
+    for c in codes:
+        assert ora.e4m3_encode(ora.e4m3_value(int(c))) == int(c)
+
+
+def pin_e4m3_all_bf16_vs_library(ora):
+    """Every finite bf16 value (the quantiser only ever sees bf16 / 2^k) vs torch."""
+    bits = np.arange(0, 1 << 16, dtype=np.uint32)
+    vals = (bits << np.uint32(16)).view(np.float32)
+    vals = vals[np.isfinite(vals)]
+    assert np.array_equal(ora.e4m3_encode_array(vals), torch_e4m3(vals))
+
+
+def pin_e4m3_random_fp32_brute_force(ora, n: int = 4000):
+    """Nearest finite E4M3 by linear scan, ties to the even code, on random fp32."""
+    table = [(c, ora_free_value(c)) for c in range(0x7F)]  # non-negative finite codes
+    u = synth.uniform01(99, 7, 2 * n)
+    mags = np.exp2(u[:n] * 22.0 - 12.0) * (1.0 + u[n:])
+    vals = np.where(np.arange(n) % 2 == 0, mags, -mags).astype(np.float32)
+    for v in vals:
+        a = abs(float(v))
+        best = None
+        for c, cv in table:
+            d = abs(cv - a)
+            if best is None or d < best[0] or (d == best[0] and c % 2 == 0):
+                best = (d, c)
+        want = (best[1] if a < 448.0 else 0x7E) | (0x80 if v < 0 else 0)
+        assert ora.e4m3_encode(float(v)) == want, (float(v), want)
+
+
+def ora_free_value(c: int) -> float:
+    """E4M3 value of a non-negative finite code by the OCP formula (test's own)."""
+    e, m = c >> 3, c & 7
+    return (m / 8.0) * 2.0 ** -6 if e == 0 else (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+# ----------------------------------------------------------------- scales
+
+def pin_ue8m0_worked(ora):
+    cases = [
+        (1.0, 2.0 ** -8),       # 1/448 lies in (2^-9, 2^-8]
+        (2.0, 2.0 ** -7),
+        (448.0, 1.0),           # exactly a power of two: kept
+        (1.75, 2.0 ** -8),      # 1.75/448 = 2^-8 exactly
+        (1.7578125, 2.0 ** -7), # next bf16 above 1.75: rounds up
+        (0.0, 2.0 ** -42),      # amax floored at 1e-10: 1e-10/448 in (2^-43, 2^-42]
+        (3.0e38, 2.0 ** 120),   # 3e38/448 = 6.7e35 in (2^119, 2^120]
+    ]
+    for amax, want in cases:
+        assert ora.ue8m0_scale(amax) == want, (amax, ora.ue8m0_scale(amax), want)
+
+
+def pin_ue8m0_invariants(ora, n: int = 3000):
+    u = synth.uniform01(5, 1, n)
+    amaxs = np.exp2(u * 60.0 - 30.0).astype(np.float32)
+    for a in amaxs:
+        s = ora.ue8m0_scale(float(a))
+        m, e = math.frexp(s)
+        assert m == 0.5, "scale must be a power of two"
+        assert float(a) / s <= 448.0
+        assert float(a) / s > 224.0, "scale must be the smallest power of two that fits"
+
+
+def pin_quant_group_worked(ora):
+    x = np.zeros(128, np.float32)
+    x[0] = 1.0
+    codes, s = ora.quant_group(x)
+    assert codes[0] == 0x78 and not codes[1:].any()
+    assert np.float32(s).view(np.uint32) == 0x3B800000
+    x[0] = 2.0
+    codes, s = ora.quant_group(x)
+    assert codes[0] == 0x78 and np.float32(s).view(np.uint32) == 0x3C000000
+    x[:] = 0
+    x[7] = 448.0
+    x[8] = -1.0
+    codes, s = ora.quant_group(x)
+    assert s == 1.0 and codes[7] == 0x7E and codes[8] == 0xB8
+    # mixed signs: amax 1 -> scale 2^-8; -1 -> -256 (0xF8); 0.5 -> 128 (0x70); 0.75 -> 192 (0x74)
+    x[:] = 0
+    x[0], x[1], x[2] = -1.0, 0.5, 0.75
+    codes, s = ora.quant_group(x)
+    assert s == 2.0 ** -8 and list(codes[:3]) == [0xF8, 0x70, 0x74]
+
+
+def pin_quant_group_vs_library(ora, n_groups: int = 64):
+    """Groups of N(0,1) bf16 values: codes = torch E4M3 of x / (power-of-two scale)."""
+    x = synth.bf16_to_f32(bf16(synth.normal(11, 1, n_groups * 128))).reshape(n_groups, 128)
+    x[3] *= 1e-20
+    x[4] *= 1e20
+    x[5] = 0.0
+    for g in range(n_groups):
+        codes, s = ora.quant_group(x[g])
+        amax = float(np.abs(x[g]).max())
+        assert s >= max(amax, 1e-10) / 448.0 * (1 - 1e-7)
+        assert np.array_equal(codes, torch_e4m3(x[g] / np.float32(s)))
+        # dequantised error bound: half an E4M3 step (relative 2^-4) of each value
+        deq = torch_e4m3_value(codes) * s
+        assert np.all(np.abs(deq - x[g]) <= np.abs(x[g]) * 2.0 ** -4 + s * 2.0 ** -10)
+
+
+# ----------------------------------------------------------------- cache layout
+
+def pin_slot_layout(ora):
+    # 132 bytes per slot (128 K bytes + one fp32 scale), 64 slots per page = 8448 bytes;
+    # inside a page the 64 K rows come first, then the 64 scales.
+    assert ora.slot_offsets(0) == (0, 8192)
+    assert ora.slot_offsets(1) == (128, 8196)
+    assert ora.slot_offsets(63) == (63 * 128, 8192 + 63 * 4)
+    assert ora.slot_offsets(64) == (8448, 8448 + 8192)
+    assert ora.slot_offsets(65) == (8576, 16644)
+
+
+def pin_k_quant_write_worked(ora):
+    cache = ora.new_cache(2)
+    k = np.zeros((4, 128), np.float64)
+    k[0, 0] = 1.0          # -> code 0x78 at byte 0, scale 2^-8
+    k[1, 5] = -2.0         # padding token: must not be written
+    k[2, 127] = 448.0      # -> code 0x7E, scale 1.0
+    k[3, 0] = 1.0          # slot past the cache: skipped and counted
+    slots = np.array([5, -1, 70, 128], np.int64)
+    bad = ora.k_quant_write(bf16(k), slots, cache)
+    assert bad == 1
+    flat = cache.reshape(-1)
+    want = np.zeros_like(flat)
+    want[5 * 128 + 0] = 0x78
+    want[8192 + 5 * 4: 8192 + 5 * 4 + 4] = np.frombuffer(np.float32(2.0 ** -8).tobytes(), np.uint8)
+    want[8448 + 6 * 128 + 127] = 0x7E
+    want[8448 + 8192 + 6 * 4: 8448 + 8192 + 6 * 4 + 4] = np.frombuffer(np.float32(1.0).tobytes(), np.uint8)
+    assert np.array_equal(flat, want)
+
+
+# ----------------------------------------------------------------- scores
+
+def _cache_with_keys(ora, keys_f64, block_table_row, num_blocks):
+    """Write keys at logical positions 0..n-1 through one request's block table."""
+    n = keys_f64.shape[0]
+    pos = np.arange(n)
+    slots = block_table_row[pos // 64].astype(np.int64) * 64 + pos % 64
+    cache = ora.new_cache(num_blocks)
+    assert ora.k_quant_write(bf16(keys_f64), slots, cache) == 0
+    return cache
+
+
+def pin_logits_hand_case(ora):
+    # q head 0 = (2, 0, ...), every other head 0; k = (1, 0, ...); w_0 = 1:
+    # I = 1 * ReLU(2 * 1) * 128^-1/2 * 64^-1/2 = 0.0220971 (to 7 digits).
+    q = np.zeros((64, 128))
+    q[0, 0] = 2.0
+    k = np.zeros((1, 128))
+    k[0, 0] = 1.0
+    w = np.zeros(64, np.float32)
+    w[0] = 1.0
+    bt = np.array([0], np.int32)
+    cache = _cache_with_keys(ora, k, bt, 1)
+    qc, qs = ora.q_quant(bf16(q))
+    got = ora.logits_row(qc, qs, w, cache, bt, 1)
+    assert abs(got[0] - 0.0220971) < 5e-8
+    # ReLU: a negative dot product contributes nothing
+    q[0, 0] = -2.0
+    qc, qs = ora.q_quant(bf16(q))
+    assert ora.logits_row(qc, qs, w, cache, bt, 1)[0] == 0.0
+    # a negative head weight flips the sign of a positive contribution
+    q[0, 0] = 2.0
+    w[0] = -1.0
+    qc, qs = ora.q_quant(bf16(q))
+    assert abs(ora.logits_row(qc, qs, w, cache, bt, 1)[0] + 0.0220971) < 5e-8
+    # two heads: 3*ReLU(2*1) + 0.5*ReLU(-4*1) + 2*ReLU(1.5*1) = 9 -> 9 / (sqrt(128)*8)
+    q[:] = 0
+    q[0, 0], q[1, 0], q[2, 0] = 2.0, -4.0, 1.5
+    w[:] = 0
+    w[0], w[1], w[2] = 3.0, 0.5, 2.0
+    qc, qs = ora.q_quant(bf16(q))
+    assert abs(ora.logits_row(qc, qs, w, cache, bt, 1)[0] - 9.0 * SOFTMAX_SCALE * HEAD_NORM) < 1e-12
+
+
+def pin_logits_matmul_special_case(ora):
+    """All inputs positive and exactly representable after quantisation, so the
+    ReLU is the identity: I = c * (w^T Q) K^T, a plain float64 matmul."""
+    n_keys = 150
+    grid = np.arange(8) * 0.25  # {0, .25, ..., 1.75}: x * 256 is an exact E4M3 value
+    u = synth.uniform01(3, 1, 64 * 128 + n_keys * 128)
+    Q = grid[(u[: 64 * 128] * 8).astype(int) % 8].reshape(64, 128)
+    K = grid[(u[64 * 128:] * 8).astype(int) % 8].reshape(n_keys, 128)
+    Q[:, 0] = 1.75  # amax 1.75 per row -> scale 2^-8, lossless
+    K[:, 0] = 1.75
+    w = (0.5 + synth.uniform01(3, 2, 64)).astype(np.float32)
+    bt = np.array([2, 0, 1], np.int32)  # a permuted block table
+    cache = _cache_with_keys(ora, K, bt, 3)
+    qc, qs = ora.q_quant(bf16(Q))
+    got = ora.logits_row(qc, qs, w, cache, bt, n_keys)
+    want = SOFTMAX_SCALE * HEAD_NORM * ((w.astype(np.float64) @ Q) @ K.T)
+    np.testing.assert_allclose(got, want, rtol=1e-13, atol=0)
+
+
+def pin_logits_scale_folding(ora):
+    """The pages fold q_scale, softmax_scale and n_head^-0.5 into the weights
+    before the op: I = k_scale * sum_h w'_h ReLU(codes_q . codes_k) with
+    w' = w * q_scale * softmax_scale * n_head^-0.5. Codes are decoded with the
+    library's E4M3 type, not the oracle's decoder."""
+    n_keys = 200
+    Q = synth.normal(21, 1, 64 * 128).reshape(64, 128)
+    Q[7] *= 1e-3   # spread the per-head scales
+    Q[9] *= 40.0
+    K = synth.normal(21, 2, n_keys * 128).reshape(n_keys, 128)
+    K[::3] *= 9.0
+    w = synth.normal(21, 3, 64).astype(np.float32)
+    bt = np.array([3, 1, 0, 2], np.int32)
+    cache = _cache_with_keys(ora, K, bt, 4)
+    qc, qs = ora.q_quant(bf16(Q))
+    got = ora.logits_row(qc, qs, w, cache, bt, n_keys)
+    wf = w.astype(np.float64) * qs.astype(np.float64) * SOFTMAX_SCALE * HEAD_NORM
+    cq = torch_e4m3_value(qc)
+    pos = np.arange(n_keys)
+    slots = bt[pos // 64].astype(np.int64) * 64 + pos % 64
+    flat = cache.reshape(-1)
+    kcodes = np.stack([flat[(s // 64) * 8448 + (s % 64) * 128:][:128] for s in slots])
+    kscale = np.array([np.frombuffer(flat[(s // 64) * 8448 + 8192 + (s % 64) * 4:][:4].tobytes(), np.float32)[0]
+                       for s in slots], np.float64)
+    ck = torch_e4m3_value(kcodes)
+    want = kscale * (np.maximum(cq @ ck.T, 0.0).T @ wf)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-300)
+
+
+def pin_indexer_causal_rows(ora):
+    """A prefill of 70 tokens: row t sees exactly keys 0..t (its own included)."""
+    b = synth.make_batch(41, [], [(70, 70)], 8, identity_table=False)
+    cache = ora.fill_cache(b)
+    topk, scores = ora.indexer(b, cache, with_scores=True)
+    for t in range(70):
+        n = t + 1
+        assert np.all(scores[t, n:] == 0.0)
+        want = ora.topk_row(scores[t, :n], 8)
+        assert np.array_equal(topk[t], want)
+        assert set(topk[t][topk[t] >= 0].tolist()) <= set(range(n))
+        assert int((topk[t] >= 0).sum()) == min(8, n)
+    assert list(topk[0]) == [0] + [-1] * 7
+    # the row's own key is visible: a key that dominates every head lands in the top-1
+    q = synth.bf16_to_f32(b.q[69]).astype(np.float64)
+    kbig = np.maximum(q.mean(axis=0), 0) * 50 + 1e-3
+    b.k_new[69] = bf16(kbig)
+    b.w[69] = np.abs(b.w[69])
+    cache = ora.fill_cache(b)
+    t69 = ora.indexer(b, cache, rows=np.array([69]))
+    assert t69[0][0] == 69
+
+
+def pin_indexer_block_table_invariance(ora):
+    """The same request under two different block tables scores identically."""
+    b1 = synth.make_batch(52, [300], [], 16, identity_table=True)
+    b2 = synth.make_batch(52, [300], [], 16, identity_table=False, spare_blocks=3)
+    assert not np.array_equal(b1.block_table[0], b2.block_table[0, :5])
+    s1 = ora.indexer(b1, ora.fill_cache(b1), with_scores=True)[1]
+    s2 = ora.indexer(b2, ora.fill_cache(b2), with_scores=True)[1]
+    assert np.array_equal(s1, s2)
+
+
+# ----------------------------------------------------------------- top-k
+
+def pin_topk_brute_force(ora, trials: int = 60):
+    u = synth.uniform01(77, 1, trials * 16)
+    for t in range(trials):
+        n = 1 + t % 16
+        k = 1 + (t * 7) % 9
+        # coarse values so that ties happen often
+        sc = np.floor(u[t * 16: t * 16 + n] * 5.0) - 2.0
+        got = ora.topk_row(sc, k)
+        m = min(k, n)
+        assert list(got[m:]) == [-1] * (k - m)
+        best = None
+        for sub in itertools.combinations(range(n), m):
+            inside = sc[list(sub)]
+            outside = np.delete(sc, list(sub))
+            if outside.size and inside.min() < outside.max():
+                continue
+            key = sum(sub)
+            if best is None or key < best[0]:
+                best = (key, set(sub))
+        assert set(got[:m].tolist()) == best[1], (sc, k, got)
+        # reported in score order, lower index first among equal scores
+        for a, b_ in zip(got[: m - 1], got[1:m]):
+            assert sc[a] > sc[b_] or (sc[a] == sc[b_] and a < b_)
+
+
+def pin_topk_vs_argsort(ora):
+    sc = synth.normal(78, 1, 5000)
+    sc[::7] = np.round(sc[::7], 1)  # many exact ties
+    for k in (1, 64, 2048, 5000, 6000):
+        got = ora.topk_row(sc, k)
+        want = np.argsort(-sc, kind="stable")[: min(k, 5000)]
+        assert np.array_equal(got[: min(k, 5000)], want)
+        assert np.all(got[min(k, 5000):] == -1)
+
+
+# ----------------------------------------------------------------- conversion
+
+def pin_convert_worked(ora):
+    bt = np.array([[3, 0, -1], [1, 2, 4]], np.int32)
+    logical = np.array([[0, 63, 64, 100, -1],
+                        [5, 64, -1, -1, 130]], np.int32)
+    req = np.array([0, 1], np.int32)
+    phys, valid = ora.convert(logical, req, bt)
+    assert phys.tolist() == [[192, 255, 0, 36, -1], [69, 128, -1, -1, 258]]
+    assert valid.tolist() == [4, 3]
+    # a physical block holding twice the rows (block_stride_rows = 128)
+    phys, _ = ora.convert(logical, req, bt, block_stride_rows=128)
+    assert phys.tolist() == [[384, 447, 0, 36, -1], [133, 256, -1, -1, 514]]
+    # identity block table: physical == logical
+    ident = np.arange(8, dtype=np.int32)[None, :]
+    lg = np.array([[0, 1, 500, 63, 64, -1]], np.int32)
+    phys, valid = ora.convert(lg, np.array([0], np.int32), ident)
+    assert phys.tolist() == lg.tolist() and valid.tolist() == [5]
+
+
+# ----------------------------------------------------------------- schedule
+
+def pin_schedule(ora):
+    # 61 layers, freq 4, default offset 2: skip iff max(l-1, 0) % 4 != 0
+    fs, prod = ora.schedule(61, True, 4)
+    full = [0, 1, 5, 9, 13, 17, 21, 25, 29, 33, 37, 41, 45, 49, 53, 57]
+    assert [i for i, c in enumerate(fs) if c == "F"] == full
+    assert fs.count("F") == 16 and fs.count("S") == 45
+    for l in range(61):
+        assert prod[l] == max(f for f in full if f <= l)
+    fs, _ = ora.schedule(10, True, 2)
+    assert fs == "FFSFSFSFSF"
+    fs, _ = ora.schedule(9, True, 3)
+    assert fs == "FFSSFSSFS"
+    fs, _ = ora.schedule(8, True, 1)
+    assert fs == "F" * 8
+    fs, _ = ora.schedule(12, False, 4)
+    assert fs == "F" * 12
+    fs, _ = ora.schedule(9, True, 4, offset=1)  # skip iff l % 4 != 0
+    assert fs == "FSSSFSSSF"
+    fs, prod = ora.schedule(6, True, 4, pattern="FSSFFS")
+    assert fs == "FSSFFS" and prod.tolist() == [0, 0, 0, 3, 4, 4]
+    fs, prod = ora.schedule(3, False, 4, pattern="FSS")  # IndexCache off: pattern ignored
+    assert fs == "FFF"
+    for bad in [dict(n_layers=4, pattern="FSXF"), dict(n_layers=4, pattern="FSS"),
+                dict(n_layers=4, pattern="SFFF"), dict(n_layers=4, freq=0),
+                dict(n_layers=4, freq=2, offset=0)]:
+        kw = dict(use_index_cache=True, freq=4)
+        kw.update(bad)
+        try:
+            ora.schedule(**kw)
+        except ValueError:
+            continue
+        raise AssertionError(f"schedule accepted {bad}")
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

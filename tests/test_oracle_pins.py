@@ -1,0 +1,11 @@
+"""The CPU oracle against its pins (hand-worked cases, library routines,
+closed forms, brute force). No GPU needed."""
+import pytest
+
+import oracle
+from tests import oracle_pins
+
+
+@pytest.mark.parametrize("pin", oracle_pins.ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(pin):
+    pin(oracle.get())
