@@ -1,0 +1,460 @@
+#!/usr/bin/env python
+"""Benchmark of one DSA indexer step on GB300.
+
+A step is one pass of the whole indexer path over one batch: K quantisation
+and paged-cache write of the step's tokens, q quantisation with the weight
+fold, the work plan, the FP8 tensor-core scores, per-row top-k, the IndexCache
+schedule for the layer, and the logical->physical id conversion.
+
+Default workload: 32 decode requests with contexts uniform on [4096, 8192]
+(seeded), 64 FP8 heads of dim 128, 132-byte paged K slots under a permuted
+block table, top-2048, one indexer layer. Inputs are synthetic (seeded
+normals), resident in HBM; steps rotate over input replicas whose total
+footprint exceeds twice the 129 MB L2, so every step reads its K cache from
+HBM.
+
+Prints one JSON line (rank 0). ``--impl reference`` times the CPU oracle on
+the host cores instead (a bounded sample of the same workload per step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from dsa_sparse_attention_quant_gb300 import synth  # noqa: E402
+
+METRIC = "indexer score-pairs/s (q·k ×64 heads) + top-k rows/s; % of HBM/FP8 roofline"
+L2_BYTES = 129 * 1024 * 1024
+HBM_FALLBACK_GBS = 6800.0
+
+
+def workload(name: str):
+    if name == "decode32":
+        return synth.decode32(), ("decode32: 32 decode requests x 1 query token, context uniform on [4096, 8192] "
+                                  "(seed 1), 64 FP8 heads x 128, 132 B/slot paged K cache (64-slot pages, "
+                                  "permuted block table), top-2048, 1 indexer layer")
+    if name == "decode8x128k":
+        return synth.decode8x128k(), ("decode8x128k: 8 decode requests at 131072 context, random block table, "
+                                      "top-2048, logical->physical conversion included")
+    if name == "prefill4x8k":
+        return synth.prefill4x8k(), ("prefill4x8k: 4 causal prefills of 8192 tokens (32768 query tokens), "
+                                     "shuffled pages, K quant + cache write fused with logits/top-k, top-2048")
+    if name == "prefill512":
+        return synth.prefill512(), "prefill512: 1 request, causal prefill of 512 tokens, RoPE inputs, top-128"
+    raise SystemExit(f"unknown workload {name}")
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p.get("bf16_tflops", 0.0)), "measured"
+    except (OSError, KeyError, ValueError):
+        return HBM_FALLBACK_GBS, 1900.0, "fallback"
+
+
+# --------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self, t0=None, t1=None):
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            if t0 is not None and not (t0 <= ts <= t1):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+# --------------------------------------------------------------------- our arm
+
+class Replica:
+    """One independent copy of a step's device inputs (K cache, q, w, new K)."""
+
+    def __init__(self, hb, dsa, torch, dev, ctx_k, ctx_slots):
+        self.k_cache = torch.zeros((hb.num_blocks, 8448), dtype=torch.uint8, device=dev)
+        dsa.indexer_k_quant_write(ctx_k, ctx_slots, self.k_cache)
+        self.q = torch.from_numpy(hb.q.view(np.int16)).view(torch.bfloat16).to(dev)
+        self.w = torch.from_numpy(hb.w).to(dev)
+        self.k_new = torch.from_numpy(hb.k_new.view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import dsa_sparse_attention_quant_gb300 as dsa
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    gpu_index = torch.cuda.current_device()
+
+    hb, desc = workload(args.workload)
+    T, k = hb.num_tokens, hb.topk
+    pairs = hb.num_pairs()
+    batch = dsa.Batch.from_host(hb, dev)
+    slots = torch.from_numpy(hb.slot_mapping).to(dev)
+    fs, _ = dsa.schedule_build(1, True, 4)
+
+    cache_bytes = hb.num_blocks * 8448
+    per_replica = cache_bytes + hb.q.nbytes + hb.w.nbytes + hb.k_new.nbytes
+    n_rep = args.replicas or max(1, min(16, math.ceil(2 * L2_BYTES / per_replica)))
+    ctx_k = torch.from_numpy(hb.ctx_k.view(np.int16)).view(torch.bfloat16).to(dev)
+    ctx_slots = torch.from_numpy(hb.ctx_slots).to(dev)
+    reps = [Replica(hb, dsa, torch, dev, ctx_k, ctx_slots) for _ in range(n_rep)]
+    del ctx_k, ctx_slots
+
+    ws = torch.empty(dsa.indexer_workspace_size(batch, k), dtype=torch.uint8, device=dev)
+    ld = (batch.max_seq_len + 3) // 4 * 4
+    logits = torch.empty((T, ld), dtype=torch.float32, device=dev)
+    q8 = torch.empty((T, 64, 128), dtype=torch.uint8, device=dev)
+    wf = torch.empty((T, 64), dtype=torch.float32, device=dev)
+    topk = torch.empty((T, k), dtype=torch.int32, device=dev)
+    phys = torch.empty((T, k), dtype=torch.int32, device=dev)
+    valid = torch.empty(T, dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    launches_per_step = 5 + (1 if hb.num_decodes > 0 else 0) + (1 if hb.num_reqs > hb.num_decodes else 0)
+
+    def step(i, ev=None):
+        r = reps[i % n_rep]
+        # S4: the layer's schedule entry (one layer: 'F')
+        assert fs[0] == "F"
+        dsa.indexer_k_quant_write(r.k_new, slots, r.k_cache, err)                      # S1
+        dsa.indexer_q_quant_fold(r.q, r.w, q_fp8=q8, w_folded=wf)                      # S2a
+        dsa.indexer_plan(batch, ws, err)
+        if ev is not None:
+            ev[0].record(stream)
+        dsa.indexer_logits(batch, q8, wf, r.k_cache, logits=logits, ws=ws, dev_err=err)  # S2b
+        if ev is not None:
+            ev[1].record(stream)
+        dsa.indexer_topk(batch, logits, k, topk_out=topk)                               # S3
+        dsa.topk_logical_to_physical(topk, batch.req_id_per_token, batch.block_table,   # S5
+                                     physical=phys, valid_counts=valid, dev_err=err)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if dsa.check_device_error(err):
+        raise SystemExit(f"device error word set: {int(err.item()):#x}")
+
+    # device-timed region: K steps between two events, logits kernel bracketed per step
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_index) as clocks:
+        # keep the GPU busy for a short clock window before the timed steps
+        t_warm = time.perf_counter()
+        i = 0
+        while time.perf_counter() - t_warm < args.clock_window:
+            step(i)
+            i += 1
+            if i % 64 == 0:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        wall0 = time.perf_counter()
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(i, kev[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        wall1 = time.perf_counter()
+        if world > 1:
+            dist.barrier()
+        elapsed_ms = t_start.elapsed_time(t_end)
+        kernel_ms = [a.elapsed_time(b) for a, b in kev]
+        if world > 1:
+            t = torch.tensor([elapsed_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            elapsed_ms = float(t.item())
+
+        # end to end through the same calls from pinned host memory: H2D of the
+        # step's inputs and metadata, the step, D2H of the physical ids
+        host = {
+            "q": torch.from_numpy(hb.q.view(np.int16)).pin_memory(),
+            "w": torch.from_numpy(hb.w).pin_memory(),
+            "k_new": torch.from_numpy(hb.k_new.view(np.int16)).pin_memory(),
+            "slots": torch.from_numpy(hb.slot_mapping).pin_memory(),
+            "qsl": torch.from_numpy(hb.query_start_loc.astype(np.int32)).pin_memory(),
+            "seq": torch.from_numpy(hb.seq_lens.astype(np.int32)).pin_memory(),
+            "bt": torch.from_numpy(hb.block_table.astype(np.int32)).pin_memory(),
+            "req": torch.from_numpy(hb.req_id_per_token.astype(np.int32)).pin_memory(),
+        }
+        out_phys = torch.empty((T, k), dtype=torch.int32).pin_memory()
+        out_valid = torch.empty(T, dtype=torch.int32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_phys.numel() * 4 + out_valid.numel() * 4
+
+        def e2e_step(i):
+            r = reps[i % n_rep]
+            r.q.view(torch.int16).copy_(host["q"], non_blocking=True)
+            r.w.copy_(host["w"], non_blocking=True)
+            r.k_new.view(torch.int16).copy_(host["k_new"], non_blocking=True)
+            slots.copy_(host["slots"], non_blocking=True)
+            batch.query_start_loc.copy_(host["qsl"], non_blocking=True)
+            batch.seq_lens.copy_(host["seq"], non_blocking=True)
+            batch.block_table.copy_(host["bt"], non_blocking=True)
+            batch.req_id_per_token.copy_(host["req"], non_blocking=True)
+            step(i)
+            out_phys.copy_(phys, non_blocking=True)
+            out_valid.copy_(valid, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        for i in range(args.warmup):
+            e2e_step(i)
+        if world > 1:
+            dist.barrier()
+        e0 = time.perf_counter()
+        for i in range(args.steps):
+            e2e_step(i)
+        e1 = time.perf_counter()
+        e2e_s = e1 - e0
+        if world > 1:
+            t = torch.tensor([e2e_s], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+    torch.cuda.synchronize()
+    if dsa.check_device_error(err):
+        raise SystemExit(f"device error word set: {int(err.item()):#x}")
+
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+    ms_per_step = elapsed_ms / args.steps
+    value = pairs * world / (ms_per_step / 1e3)
+    rows_per_s = T * world / (ms_per_step / 1e3)
+    hbm_peak, _, peak_src = read_peaks()
+    kernel_avg_ms = float(np.mean(kernel_ms))
+    algo_bytes = pairs * (132 + 4) + T * (64 * 128 + 64 * 4)
+    achieved = algo_bytes / (kernel_avg_ms / 1e3) / 1e9
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", f"traffic_{args.workload}.json")
+    if os.path.exists(prof):
+        with open(prof) as f:
+            traffic = json.load(f).get("dram_bytes_per_launch")
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "pairs/s",
+        "topk_rows_per_s": rows_per_s,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp8_e4m3 x fp8_e4m3 -> fp32",
+        "data": "synthetic (seeded normals, bf16-rounded)",
+        "config": {
+            "workload": desc,
+            "query_tokens": T,
+            "pairs_per_step": pairs,
+            "topk": k,
+            "l2": f"inputs larger than L2: {n_rep} rotating input replicas, "
+                  f"{n_rep * per_replica / 1e6:.0f} MB > 2x 129 MB",
+            "parallelism": f"replica per GPU x{world}" if world > 1 else "1 GPU",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "dsa::logits_kernel<1> (decode: tcgen05 FP8 scores)" if hb.num_decodes == hb.num_reqs
+            else "dsa::logits_kernel (scores)",
+            "achieved": achieved,
+            "peak": hbm_peak,
+            "unit": "GB/s",
+            "frac": achieved / hbm_peak,
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": algo_bytes,
+            "avg_launch_ms": kernel_avg_ms,
+            "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
+        },
+        "e2e": {
+            "value": pairs * world / (e2e_s / args.steps),
+            "unit": "pairs/s",
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "ms_per_step": e2e_s / args.steps * 1e3,
+        },
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+        "wall_s_timed_region": wall1 - wall0,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(hb, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------- oracle
+
+def oracle_state(hb):
+    import oracle
+
+    cache = oracle.new_cache(hb.num_blocks)
+    oracle.k_quant_write(hb.ctx_k, hb.ctx_slots, cache)  # the cache state before the step
+    return oracle, cache
+
+
+def oracle_step(ora, hb, cache, rows):
+    """The whole path on the oracle for the given query rows."""
+    ora.k_quant_write(hb.k_new, hb.slot_mapping, cache)
+    ora.schedule(1, True, 4)
+    topk = ora.indexer(hb, cache, rows=rows)
+    ora.convert(topk, hb.req_id_per_token[rows], hb.block_table)
+    return int((hb.positions[rows] + 1).sum())
+
+
+def cpu_baseline(hb, budget_s: float):
+    ora, cache = oracle_state(hb)
+    T = hb.num_tokens
+    t0 = time.perf_counter()
+    oracle_step(ora, hb, cache, np.arange(min(T, 1), dtype=np.int64))
+    t_one = max(time.perf_counter() - t0, 1e-4)
+    n_rows = int(max(1, min(T, budget_s / t_one)))
+    rows = np.arange(n_rows, dtype=np.int64)
+    t0 = time.perf_counter()
+    p = oracle_step(ora, hb, cache, rows)
+    dt = time.perf_counter() - t0
+    return {"value": p / dt, "unit": "pairs/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n_rows} of {T} query rows of the same step ({p} pairs; K write of all {T} new tokens, "
+                      f"fp64 scores, full-sort top-k, conversion), {dt:.1f} s, OpenMP over rows"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    hb, desc = workload(args.workload)
+    ora, cache = oracle_state(hb)
+    T = hb.num_tokens
+    t0 = time.perf_counter()
+    oracle_step(ora, hb, cache, np.arange(1, dtype=np.int64))
+    t_one = max(time.perf_counter() - t0, 1e-4)
+    per_step = 120.0 / max(1, args.steps + args.warmup)
+    n_rows = int(max(1, min(T, per_step / t_one)))
+    rows = np.arange(n_rows, dtype=np.int64)
+    for _ in range(args.warmup):
+        oracle_step(ora, hb, cache, rows)
+    t0 = time.perf_counter()
+    p = 0
+    for _ in range(args.steps):
+        p += oracle_step(ora, hb, cache, rows)
+    dt = time.perf_counter() - t0
+    value = p / dt
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "pairs/s",
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded normals, bf16-rounded)",
+        "config": {"workload": desc, "query_tokens": T, "pairs_per_step": hb.num_pairs(), "topk": hb.topk},
+        "cpu_baseline": {"value": value, "unit": "pairs/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"{n_rows} of {T} query rows per step"},
+        "e2e": {"value": value, "unit": "pairs/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode32")
+    ap.add_argument("--replicas", type=int, default=0)
+    ap.add_argument("--clock-window", type=float, default=1.0, help="seconds of untimed steps while sampling clocks")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,347 @@
+"""ctypes binding of ``libdsaidx.so`` (the C ABI of ``include/dsaidx.h``).
+
+Argument marshalling only: every step of the indexer runs in the library's
+CUDA kernels. Torch supplies device memory (outputs and workspaces are
+allocated with torch when the caller does not pass them) and the current
+CUDA stream. If the library is missing or no sm_103 GPU is present the calls
+raise; there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+DSA_OK, DSA_EINVAL, DSA_ECUDA, DSA_EDEVICE, DSA_ENOSPACE, DSA_ENODEV = range(6)
+DEVERR = {
+    1: "slot out of range",
+    2: "block id out of range",
+    4: "top-k id out of range",
+    8: "pipeline wait timed out",
+    16: "seq_len inconsistent",
+}
+HEADS, HEAD_DIM, BLOCK_SIZE, PAGE_BYTES = 64, 128, 64, 8448
+
+SYMBOLS = [
+    "dsa_status_string", "dsa_version", "dsa_check_device_error",
+    "dsa_indexer_k_quant_write", "dsa_indexer_q_quant_fold",
+    "dsa_indexer_workspace_size", "dsa_indexer_logits_topk",
+    "dsa_indexer_plan", "dsa_indexer_logits", "dsa_indexer_topk",
+    "dsa_topk_logical_to_physical", "dsa_schedule_build",
+    "dsa_layer_stack_workspace_size", "dsa_layer_stack_run",
+]
+
+
+class DsaError(RuntimeError):
+    pass
+
+
+class DsaBatchC(ctypes.Structure):
+    _fields_ = [
+        ("num_reqs", ctypes.c_int32),
+        ("num_decodes", ctypes.c_int32),
+        ("num_tokens", ctypes.c_int32),
+        ("max_seq_len", ctypes.c_int32),
+        ("bt_stride", ctypes.c_int64),
+        ("num_blocks", ctypes.c_int64),
+        ("query_start_loc", ctypes.c_void_p),
+        ("seq_lens", ctypes.c_void_p),
+        ("block_table", ctypes.c_void_p),
+        ("req_id_per_token", ctypes.c_void_p),
+    ]
+
+
+class DsaLayerInputsC(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p),
+        ("w", ctypes.c_void_p),
+        ("k_new", ctypes.c_void_p),
+        ("k_cache", ctypes.c_void_p),
+    ]
+
+
+CONSUMER_FN = ctypes.CFUNCTYPE(None, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                               ctypes.c_void_p)
+
+
+class DsaStackPlanC(ctypes.Structure):
+    _fields_ = [
+        ("n_layers", ctypes.c_int32),
+        ("fs", ctypes.c_char_p),
+        ("layers", ctypes.POINTER(DsaLayerInputsC)),
+        ("topk", ctypes.c_int32),
+        ("softmax_scale", ctypes.c_float),
+        ("block_stride_rows", ctypes.c_int32),
+    ]
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libdsaidx.so (building it with nvcc first if it is missing)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise DsaError(f"{path} is not built")
+            _build.build()
+        lib = ctypes.CDLL(path)
+        P = ctypes.c_void_p
+        I32, I64, F32, SZ = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+        BP = ctypes.POINTER(DsaBatchC)
+        sig = {
+            "dsa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+            "dsa_version": (ctypes.c_int, []),
+            "dsa_check_device_error": (ctypes.c_int, [P, P, P]),
+            "dsa_indexer_k_quant_write": (ctypes.c_int, [P, I64, I64, P, P, I64, P, P]),
+            "dsa_indexer_q_quant_fold": (ctypes.c_int, [P, P, I64, F32, P, P, P, P]),
+            "dsa_indexer_workspace_size": (SZ, [BP, I32]),
+            "dsa_indexer_logits_topk": (ctypes.c_int, [BP, P, P, P, I32, P, P, SZ, P, P, P, P]),
+            "dsa_indexer_plan": (ctypes.c_int, [BP, P, SZ, P, P]),
+            "dsa_indexer_logits": (ctypes.c_int, [BP, P, P, P, P, I64, P, SZ, P, P]),
+            "dsa_indexer_topk": (ctypes.c_int, [BP, P, I64, I32, P, P, SZ, P]),
+            "dsa_topk_logical_to_physical": (ctypes.c_int, [P, I64, I32, P, P, I64, I32, P, P, P, P]),
+            "dsa_schedule_build": (ctypes.c_int, [I32, I32, I32, I32, ctypes.c_char_p, P, P]),
+            "dsa_layer_stack_workspace_size": (SZ, [BP, I32]),
+            "dsa_layer_stack_run": (ctypes.c_int, [ctypes.POINTER(DsaStackPlanC), BP, P, P, P, P, CONSUMER_FN, P, P,
+                                                   SZ, P, P]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != DSA_OK:
+        msg = load().dsa_status_string(status).decode()
+        raise DsaError(f"{what}: {msg} (status {status})")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, dtype, what):
+    if not t.is_cuda:
+        raise DsaError(f"{what} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise DsaError(f"{what} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise DsaError(f"{what} must be contiguous")
+
+
+# ---------------------------------------------------------------- batches
+
+class Batch:
+    """Device-side step metadata (the C ``DsaBatch``) plus the tensors it points to."""
+
+    def __init__(self, query_start_loc, seq_lens, block_table, req_id_per_token, num_decodes: int,
+                 num_blocks: int, max_seq_len: int | None = None):
+        for t, n in ((query_start_loc, "query_start_loc"), (seq_lens, "seq_lens"), (block_table, "block_table"),
+                     (req_id_per_token, "req_id_per_token")):
+            _need(t, torch.int32, n)
+        self.query_start_loc = query_start_loc
+        self.seq_lens = seq_lens
+        self.block_table = block_table
+        self.req_id_per_token = req_id_per_token
+        self.num_reqs = int(seq_lens.shape[0])
+        self.num_tokens = int(req_id_per_token.shape[0])
+        self.num_decodes = int(num_decodes)
+        self.num_blocks = int(num_blocks)
+        if max_seq_len is None:
+            max_seq_len = int(seq_lens.max().item()) if self.num_reqs else 1
+        self.max_seq_len = int(max_seq_len)
+        self.c = DsaBatchC(self.num_reqs, self.num_decodes, self.num_tokens, self.max_seq_len,
+                           int(block_table.shape[1]) if block_table.dim() == 2 else 1, self.num_blocks,
+                           query_start_loc.data_ptr(), seq_lens.data_ptr(), block_table.data_ptr(),
+                           req_id_per_token.data_ptr())
+
+    @classmethod
+    def from_host(cls, hb, device="cuda"):
+        """From a ``synth.Batch`` (numpy metadata) to device tensors."""
+        def d(a):
+            return torch.from_numpy(a.astype("int32")).to(device)
+        return cls(d(hb.query_start_loc), d(hb.seq_lens), d(hb.block_table), d(hb.req_id_per_token),
+                   hb.num_decodes, hb.num_blocks, int(hb.seq_lens.max()) if hb.num_reqs else 1)
+
+
+# ---------------------------------------------------------------- entry points
+
+def indexer_k_quant_write(k, slot_mapping, k_cache, dev_err=None, stream=None):
+    _need(slot_mapping, torch.int64, "slot_mapping")
+    _need(k_cache, torch.uint8, "k_cache")
+    if k.dtype != torch.bfloat16 or not k.is_cuda or k.stride(-1) != 1:
+        raise DsaError("k must be a CUDA bf16 tensor with unit inner stride")
+    n = int(slot_mapping.shape[0])
+    row_stride = int(k.stride(0)) if k.dim() == 2 else HEAD_DIM
+    st = load().dsa_indexer_k_quant_write(_ptr(k), n, row_stride, _ptr(slot_mapping), _ptr(k_cache),
+                                          int(k_cache.shape[0]), _ptr(dev_err), _stream(stream))
+    _check(st, "dsa_indexer_k_quant_write")
+
+
+def indexer_q_quant_fold(q, w, softmax_scale: float = 0.0, q_fp8=None, q_scale=None, w_folded=None, stream=None):
+    _need(q, torch.bfloat16, "q")
+    _need(w, torch.float32, "w")
+    T = int(q.shape[0])
+    if q_fp8 is None:
+        q_fp8 = torch.empty((T, HEADS, HEAD_DIM), dtype=torch.uint8, device=q.device)
+    if w_folded is None:
+        w_folded = torch.empty((T, HEADS), dtype=torch.float32, device=q.device)
+    st = load().dsa_indexer_q_quant_fold(_ptr(q), _ptr(w), T, float(softmax_scale), _ptr(q_fp8), _ptr(q_scale),
+                                         _ptr(w_folded), _stream(stream))
+    _check(st, "dsa_indexer_q_quant_fold")
+    return q_fp8, q_scale, w_folded
+
+
+def indexer_workspace_size(batch: Batch, topk: int) -> int:
+    return int(load().dsa_indexer_workspace_size(ctypes.byref(batch.c), int(topk)))
+
+
+def _workspace(nbytes: int, device, ws=None):
+    if ws is None:
+        ws = torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+    return ws
+
+
+def indexer_logits_topk(batch: Batch, q_fp8, w_folded, k_cache, topk: int, topk_out=None, ws=None, k_new=None,
+                        slot_mapping=None, dev_err=None, stream=None):
+    dev = q_fp8.device
+    if topk_out is None:
+        topk_out = torch.empty((batch.num_tokens, int(topk)), dtype=torch.int32, device=dev)
+    nbytes = indexer_workspace_size(batch, topk)
+    ws = _workspace(nbytes, dev, ws)
+    st = load().dsa_indexer_logits_topk(ctypes.byref(batch.c), _ptr(q_fp8), _ptr(w_folded), _ptr(k_cache),
+                                        int(topk), _ptr(topk_out), _ptr(ws), ws.numel(), _ptr(k_new),
+                                        _ptr(slot_mapping), _ptr(dev_err), _stream(stream))
+    _check(st, "dsa_indexer_logits_topk")
+    return topk_out
+
+
+def indexer_plan(batch: Batch, ws=None, dev_err=None, stream=None):
+    """Plan the batch into ``ws`` (allocated if None) and return ``ws``."""
+    dev = batch.seq_lens.device
+    ws = _workspace(indexer_workspace_size(batch, 4), dev, ws)
+    st = load().dsa_indexer_plan(ctypes.byref(batch.c), _ptr(ws), ws.numel(), _ptr(dev_err), _stream(stream))
+    _check(st, "dsa_indexer_plan")
+    return ws
+
+
+def indexer_logits(batch: Batch, q_fp8, w_folded, k_cache, logits=None, ws=None, dev_err=None, stream=None):
+    """Scores of every causal (token, key) pair; plans into ``ws`` first when ``ws`` is None."""
+    dev = q_fp8.device
+    ld = (batch.max_seq_len + 3) // 4 * 4
+    if logits is None:
+        logits = torch.full((batch.num_tokens, ld), float("nan"), dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = indexer_plan(batch, dev_err=dev_err, stream=stream)
+    st = load().dsa_indexer_logits(ctypes.byref(batch.c), _ptr(q_fp8), _ptr(w_folded), _ptr(k_cache),
+                                   _ptr(logits), int(logits.stride(0)), _ptr(ws), ws.numel(), _ptr(dev_err),
+                                   _stream(stream))
+    _check(st, "dsa_indexer_logits")
+    return logits
+
+
+def indexer_topk(batch: Batch, logits, topk: int, topk_out=None, stream=None):
+    if topk_out is None:
+        topk_out = torch.empty((batch.num_tokens, int(topk)), dtype=torch.int32, device=logits.device)
+    st = load().dsa_indexer_topk(ctypes.byref(batch.c), _ptr(logits), int(logits.stride(0)), int(topk),
+                                 _ptr(topk_out), None, 0, _stream(stream))
+    _check(st, "dsa_indexer_topk")
+    return topk_out
+
+
+def topk_logical_to_physical(logical, req_id_per_token, block_table, block_stride_rows: int = 0, physical=None,
+                             valid_counts=None, with_valid_counts: bool = True, dev_err=None, stream=None):
+    _need(logical, torch.int32, "logical")
+    T, k = logical.shape
+    if physical is None:
+        physical = torch.empty_like(logical)
+    if valid_counts is None and with_valid_counts:
+        valid_counts = torch.empty(T, dtype=torch.int32, device=logical.device)
+    st = load().dsa_topk_logical_to_physical(_ptr(logical), int(T), int(k), _ptr(req_id_per_token),
+                                             _ptr(block_table), int(block_table.shape[1]), int(block_stride_rows),
+                                             _ptr(physical), _ptr(valid_counts), _ptr(dev_err), _stream(stream))
+    _check(st, "dsa_topk_logical_to_physical")
+    return physical, valid_counts
+
+
+def schedule_build(n_layers: int, use_index_cache: bool = True, freq: int = 1, offset: int = 2,
+                   pattern: str | None = None):
+    """Host-side IndexCache schedule: (fs string, producer list)."""
+    fs = ctypes.create_string_buffer(max(int(n_layers), 1))
+    prod = (ctypes.c_int32 * max(int(n_layers), 1))()
+    st = load().dsa_schedule_build(int(n_layers), int(bool(use_index_cache)), int(freq), int(offset),
+                                   None if pattern is None else pattern.encode(), fs, prod)
+    _check(st, "dsa_schedule_build")
+    return fs.raw[:n_layers].decode(), list(prod[:n_layers])
+
+
+def check_device_error(dev_err, stream=None) -> int:
+    out = ctypes.c_uint32(0)
+    st = load().dsa_check_device_error(_ptr(dev_err), ctypes.byref(out), _stream(stream))
+    if st not in (DSA_OK, DSA_EDEVICE):
+        _check(st, "dsa_check_device_error")
+    return int(out.value)
+
+
+def layer_stack_workspace_size(batch: Batch, topk: int) -> int:
+    return int(load().dsa_layer_stack_workspace_size(ctypes.byref(batch.c), int(topk)))
+
+
+def layer_stack_run(batch: Batch, fs: str, layers, topk: int, slot_mapping=None, topk_buf=None, phys_buf=None,
+                    valid_buf=None, consumer=None, ws=None, softmax_scale: float = 0.0, block_stride_rows: int = 0,
+                    dev_err=None, stream=None):
+    """Run a stack of layers. ``layers[l]`` is None for 'S' layers, else a dict
+    with tensors ``q``, ``w``, ``k_cache`` and optionally ``k_new``.
+    ``consumer(layer, producer, phys_ptr, valid_ptr)`` is called per layer."""
+    n = len(fs)
+    arr = (DsaLayerInputsC * max(n, 1))()
+    keep = []
+    for l, L in enumerate(layers):
+        if L is None:
+            continue
+        keep.append(L)
+        arr[l] = DsaLayerInputsC(L["q"].data_ptr(), L["w"].data_ptr(),
+                                 L["k_new"].data_ptr() if L.get("k_new") is not None else None,
+                                 L["k_cache"].data_ptr())
+    plan = DsaStackPlanC(n, fs.encode(), arr, int(topk), float(softmax_scale), int(block_stride_rows))
+    dev = torch.device("cuda", torch.cuda.current_device())
+    T = batch.num_tokens
+    if topk_buf is None:
+        topk_buf = torch.empty((T, int(topk)), dtype=torch.int32, device=dev)
+    if phys_buf is None:
+        phys_buf = torch.empty((T, int(topk)), dtype=torch.int32, device=dev)
+    if valid_buf is None:
+        valid_buf = torch.empty(T, dtype=torch.int32, device=dev)
+    ws = _workspace(layer_stack_workspace_size(batch, topk), dev, ws)
+    if consumer is not None:
+        cb = CONSUMER_FN(lambda l, p, ph, va, u: consumer(int(l), int(p), ph, va))
+    else:
+        cb = CONSUMER_FN()
+    st = load().dsa_layer_stack_run(ctypes.byref(plan), ctypes.byref(batch.c), _ptr(slot_mapping), _ptr(topk_buf),
+                                    _ptr(phys_buf), _ptr(valid_buf), cb, None, _ptr(ws), ws.numel(),
+                                    _ptr(dev_err), _stream(stream))
+    _check(st, "dsa_layer_stack_run")
+    return topk_buf, phys_buf, valid_buf

@@ -1,0 +1,419 @@
+// api.cu — the C ABI declared in include/dsaidx.h: argument checks, workspace
+// carving, TMA descriptors and kernel launches. Host code only.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/dsaidx.h"
+#include "kernels.h"
+
+using namespace dsa;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int g_num_sms[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::mutex g_mutex;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return DSA_OK;
+  if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver)
+    return DSA_ENODEV;
+  return DSA_ECUDA;
+}
+
+// SM count of the current device; DSA_ENODEV unless it is an sm_103 part.
+int device_sms(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DSA_ENODEV;
+  if (dev < 0 || dev >= kMaxDevices) return DSA_ENODEV;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_num_sms[dev] == 0) {
+    int major = 0, minor = 0, n = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return DSA_ENODEV;
+    if (major != 10 || minor != 3) return DSA_ENODEV;
+    g_num_sms[dev] = n;
+  }
+  *sms = g_num_sms[dev];
+  return DSA_OK;
+}
+
+int tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return DSA_ENODEV;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  *out = g_encode;
+  return DSA_OK;
+}
+
+// K cache as a 3-D byte tensor {128 K bytes, 64 slots, num_blocks pages}: one
+// box is the 64 K rows of one page, landed with the 128-byte swizzle.
+int make_kcache_map(CUtensorMap* m, const uint8_t* cache, int64_t num_blocks) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  int st = tensor_map_encoder(&enc);
+  if (st != DSA_OK) return st;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(kBlock),
+                        static_cast<cuuint64_t>(num_blocks)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(kPageBytes)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kDim), static_cast<cuuint32_t>(kBlock), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(cache), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DSA_OK : DSA_ECUDA;
+}
+
+// q codes as a 2-D byte tensor {128, T*64}: one box is `rows` head rows.
+int make_q_map(CUtensorMap* m, const uint8_t* q, int64_t n_tokens, int rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  int st = tensor_map_encoder(&enc);
+  if (st != DSA_OK) return st;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(n_tokens * kHeads)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDim)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kDim), static_cast<cuuint32_t>(rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(q), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DSA_OK : DSA_ECUDA;
+}
+
+int check_batch(const DsaBatch* b) {
+  if (b == nullptr) return DSA_EINVAL;
+  if (b->num_reqs < 0 || b->num_decodes < 0 || b->num_decodes > b->num_reqs || b->num_tokens < 0)
+    return DSA_EINVAL;
+  if (b->num_tokens > 0 && (b->num_reqs == 0 || b->max_seq_len < 1)) return DSA_EINVAL;
+  if (b->num_reqs > 0 &&
+      (b->query_start_loc == nullptr || b->seq_lens == nullptr || b->block_table == nullptr ||
+       b->bt_stride < 1 || b->num_blocks < 1 || b->num_blocks > (int64_t{1} << 31) - 1))
+    return DSA_EINVAL;
+  if (b->num_tokens > 0 && b->req_id_per_token == nullptr) return DSA_EINVAL;
+  if (static_cast<int64_t>(b->num_tokens) * kHeads > (int64_t{1} << 31) - 1) return DSA_EINVAL;
+  return DSA_OK;
+}
+
+int64_t logits_ld(const DsaBatch* b) { return static_cast<int64_t>(align_up(b->max_seq_len > 0 ? b->max_seq_len : 1, 4)); }
+
+// Workspace carving of the indexer: both segment plans, then the score matrix.
+struct IndexerWs {
+  SegmentPlan dec, pre;
+  float* logits;
+  size_t bytes;
+};
+
+IndexerWs carve(const DsaBatch* b, void* base) {
+  IndexerWs w{};
+  uint8_t* p = static_cast<uint8_t*>(base);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    void* r = p ? p + off : nullptr;
+    off = align_up(off + bytes, 256);
+    return r;
+  };
+  const size_t T = static_cast<size_t>(b->num_tokens);
+  const size_t B = static_cast<size_t>(b->num_reqs);
+  const size_t max_dec = T + 1;
+  const size_t max_pre = T / 4 + B + 1;
+  w.dec.qb = static_cast<QBlock*>(take(max_dec * sizeof(QBlock)));
+  w.dec.tile_start = static_cast<int32_t*>(take((max_dec + 1) * 4));
+  w.dec.nqb = static_cast<int32_t*>(take(4));
+  w.dec.req_base = static_cast<int32_t*>(take((B + 1) * 4));
+  w.pre.qb = static_cast<QBlock*>(take(max_pre * sizeof(QBlock)));
+  w.pre.tile_start = static_cast<int32_t*>(take((max_pre + 1) * 4));
+  w.pre.nqb = static_cast<int32_t*>(take(4));
+  w.pre.req_base = static_cast<int32_t*>(take((B + 1) * 4));
+  w.logits = static_cast<float*>(take(T * static_cast<size_t>(logits_ld(b)) * 4));
+  w.bytes = off;
+  return w;
+}
+
+// Plan + logits for both segments (no top-k).
+int run_logits(const DsaBatch* b, const uint8_t* q_fp8, const float* w_folded, const uint8_t* k_cache,
+               float* logits, int64_t ld, const IndexerWs& ws, int32_t* dev_err, cudaStream_t stream,
+               bool run_plan) {
+  if (b->num_tokens == 0) return DSA_OK;
+  int sms = 0;
+  int st = device_sms(&sms);
+  if (st != DSA_OK) return st;
+  if (run_plan) {
+    st = from_cuda(launch_plan(b->query_start_loc, b->seq_lens, b->num_reqs, b->num_decodes, b->num_tokens, b->bt_stride, ws.dec,
+                               ws.pre, dev_err, stream));
+    if (st != DSA_OK) return st;
+  }
+  CUtensorMap mk, mq1, mq4;
+  if ((st = make_kcache_map(&mk, k_cache, b->num_blocks)) != DSA_OK) return st;
+  LogitsArgs a{w_folded, k_cache, b->block_table, b->bt_stride, b->num_blocks, logits, ld, dev_err};
+  if (b->num_decodes > 0) {
+    if ((st = make_q_map(&mq1, q_fp8, b->num_tokens, kHeads)) != DSA_OK) return st;
+    if ((st = from_cuda(launch_logits(1, &mk, &mq1, ws.dec, a, sms, stream))) != DSA_OK) return st;
+  }
+  if (b->num_reqs > b->num_decodes) {
+    if ((st = make_q_map(&mq4, q_fp8, b->num_tokens, 4 * kHeads)) != DSA_OK) return st;
+    if ((st = from_cuda(launch_logits(4, &mk, &mq4, ws.pre, a, sms, stream))) != DSA_OK) return st;
+  }
+  return DSA_OK;
+}
+
+bool topk_ok(int32_t topk) { return topk >= 4 && topk <= 4096 && topk % 4 == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* dsa_status_string(int status) {
+  switch (status) {
+    case DSA_OK: return "ok";
+    case DSA_EINVAL: return "invalid argument";
+    case DSA_ECUDA: return "CUDA call failed";
+    case DSA_EDEVICE: return "device reported inconsistent data (see the device error word)";
+    case DSA_ENOSPACE: return "workspace too small";
+    case DSA_ENODEV: return "no sm_103 device or kernel image";
+    default: return "unknown status";
+  }
+}
+
+int dsa_version(void) { return 100; }
+
+int dsa_check_device_error(const int32_t* dev_err, uint32_t* out, dsa_stream_t stream) {
+  if (dev_err == nullptr) return DSA_EINVAL;
+  uint32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, dev_err, 4, cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return from_cuda(e);
+  if (out) *out = v;
+  return v ? DSA_EDEVICE : DSA_OK;
+}
+
+int dsa_indexer_k_quant_write(const void* k, int64_t n_tokens, int64_t k_row_stride, const int64_t* slot_mapping,
+                              uint8_t* k_cache, int64_t num_blocks, int32_t* dev_err, dsa_stream_t stream) {
+  if (n_tokens < 0 || num_blocks < 1 || k_row_stride < kDim || k_row_stride % 8 != 0) return DSA_EINVAL;
+  if (n_tokens == 0) return DSA_OK;
+  if (!k || !slot_mapping || !k_cache || !aligned16(k) || !aligned16(k_cache)) return DSA_EINVAL;
+  int sms;
+  int st = device_sms(&sms);
+  if (st != DSA_OK) return st;
+  return from_cuda(launch_k_quant_write(k, n_tokens, k_row_stride, slot_mapping, k_cache, num_blocks, dev_err,
+                                        stream));
+}
+
+int dsa_indexer_q_quant_fold(const void* q, const float* w, int64_t n_tokens, float softmax_scale, uint8_t* q_fp8,
+                             float* q_scale, float* w_folded, dsa_stream_t stream) {
+  if (n_tokens < 0) return DSA_EINVAL;
+  if (n_tokens == 0) return DSA_OK;
+  if (!q || !w || !q_fp8 || !w_folded || !aligned16(q) || !aligned16(q_fp8)) return DSA_EINVAL;
+  int sms;
+  int st = device_sms(&sms);
+  if (st != DSA_OK) return st;
+  if (!(softmax_scale > 0.0f)) softmax_scale = 0.08838834764831845f;  // 128^-1/2
+  return from_cuda(launch_q_quant_fold(q, w, n_tokens, softmax_scale, q_fp8, q_scale, w_folded, stream));
+}
+
+size_t dsa_indexer_workspace_size(const DsaBatch* batch, int32_t topk) {
+  (void)topk;
+  if (check_batch(batch) != DSA_OK) return 0;
+  return carve(batch, nullptr).bytes;
+}
+
+int dsa_indexer_plan(const DsaBatch* batch, void* ws, size_t ws_bytes, int32_t* dev_err, dsa_stream_t stream) {
+  int st = check_batch(batch);
+  if (st != DSA_OK) return st;
+  if (batch->num_tokens == 0) return DSA_OK;
+  if (!ws || !aligned16(ws)) return DSA_EINVAL;
+  IndexerWs w = carve(batch, ws);
+  if (ws_bytes < w.bytes) return DSA_ENOSPACE;
+  int sms;
+  if ((st = device_sms(&sms)) != DSA_OK) return st;
+  return from_cuda(launch_plan(batch->query_start_loc, batch->seq_lens, batch->num_reqs, batch->num_decodes,
+                               batch->num_tokens, batch->bt_stride, w.dec, w.pre, dev_err, stream));
+}
+
+int dsa_indexer_logits(const DsaBatch* batch, const uint8_t* q_fp8, const float* w_folded, const uint8_t* k_cache,
+                       float* logits, int64_t logits_ld, void* ws, size_t ws_bytes, int32_t* dev_err,
+                       dsa_stream_t stream) {
+  int st = check_batch(batch);
+  if (st != DSA_OK) return st;
+  if (batch->num_tokens == 0) return DSA_OK;
+  if (!q_fp8 || !w_folded || !k_cache || !logits || !ws || logits_ld < batch->max_seq_len) return DSA_EINVAL;
+  if (!aligned16(q_fp8) || !aligned16(w_folded) || !aligned16(k_cache) || !aligned16(ws)) return DSA_EINVAL;
+  IndexerWs w = carve(batch, ws);
+  if (ws_bytes < w.bytes) return DSA_ENOSPACE;
+  return run_logits(batch, q_fp8, w_folded, k_cache, logits, logits_ld, w, dev_err, stream, false);
+}
+
+int dsa_indexer_topk(const DsaBatch* batch, const float* logits, int64_t logits_ld, int32_t topk, int32_t* topk_out,
+                     void* ws, size_t ws_bytes, dsa_stream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  int st = check_batch(batch);
+  if (st != DSA_OK) return st;
+  if (!topk_ok(topk)) return DSA_EINVAL;
+  if (batch->num_tokens == 0) return DSA_OK;
+  if (!logits || !topk_out || logits_ld < 1) return DSA_EINVAL;
+  int sms;
+  if ((st = device_sms(&sms)) != DSA_OK) return st;
+  return from_cuda(launch_topk(logits, logits_ld, batch->query_start_loc, batch->seq_lens,
+                               batch->req_id_per_token, batch->num_reqs, batch->num_tokens, topk, topk_out, stream));
+}
+
+int dsa_indexer_logits_topk(const DsaBatch* batch, const uint8_t* q_fp8, const float* w_folded, uint8_t* k_cache,
+                            int32_t topk, int32_t* topk_out, void* ws, size_t ws_bytes, const void* k_new,
+                            const int64_t* slot_mapping, int32_t* dev_err, dsa_stream_t stream) {
+  int st = check_batch(batch);
+  if (st != DSA_OK) return st;
+  if (!topk_ok(topk)) return DSA_EINVAL;
+  if ((k_new == nullptr) != (slot_mapping == nullptr)) return DSA_EINVAL;
+  if (batch->num_tokens == 0) return DSA_OK;
+  if (!q_fp8 || !w_folded || !k_cache || !topk_out || !ws) return DSA_EINVAL;
+  if (!aligned16(q_fp8) || !aligned16(w_folded) || !aligned16(k_cache) || !aligned16(ws) || !aligned16(topk_out))
+    return DSA_EINVAL;
+  IndexerWs w = carve(batch, ws);
+  if (ws_bytes < w.bytes) return DSA_ENOSPACE;
+  if (k_new != nullptr) {
+    if (!aligned16(k_new)) return DSA_EINVAL;
+    st = dsa_indexer_k_quant_write(k_new, batch->num_tokens, kDim, slot_mapping, k_cache, batch->num_blocks,
+                                   dev_err, stream);
+    if (st != DSA_OK) return st;
+  }
+  const int64_t ld = logits_ld(batch);
+  st = run_logits(batch, q_fp8, w_folded, k_cache, w.logits, ld, w, dev_err, stream, true);
+  if (st != DSA_OK) return st;
+  return from_cuda(launch_topk(w.logits, ld, batch->query_start_loc, batch->seq_lens, batch->req_id_per_token,
+                               batch->num_reqs, batch->num_tokens, topk, topk_out, stream));
+}
+
+int dsa_topk_logical_to_physical(const int32_t* logical, int64_t n_tokens, int32_t topk,
+                                 const int32_t* req_id_per_token, const int32_t* block_table, int64_t bt_stride,
+                                 int32_t block_stride_rows, int32_t* physical, int32_t* valid_counts,
+                                 int32_t* dev_err, dsa_stream_t stream) {
+  if (n_tokens < 0 || !topk_ok(topk) || bt_stride < 1) return DSA_EINVAL;
+  if (n_tokens == 0) return DSA_OK;
+  if (!logical || !req_id_per_token || !block_table || !physical || !aligned16(logical) || !aligned16(physical))
+    return DSA_EINVAL;
+  if (n_tokens > 0x7FFFFFFF) return DSA_EINVAL;
+  int sms;
+  int st = device_sms(&sms);
+  if (st != DSA_OK) return st;
+  if (block_stride_rows <= 0) block_stride_rows = kBlock;
+  return from_cuda(launch_convert(logical, n_tokens, topk, req_id_per_token, block_table, bt_stride,
+                                  block_stride_rows, physical, valid_counts, dev_err, stream));
+}
+
+int dsa_schedule_build(int32_t n_layers, int32_t use_index_cache, int32_t freq, int32_t offset, const char* pattern,
+                       char* fs_out, int32_t* producer_out) {
+  if (n_layers < 0 || (n_layers > 0 && (fs_out == nullptr || producer_out == nullptr))) return DSA_EINVAL;
+  if (use_index_cache) {
+    if (pattern != nullptr) {
+      if (static_cast<int64_t>(std::strlen(pattern)) != n_layers) return DSA_EINVAL;
+      for (int32_t l = 0; l < n_layers; ++l)
+        if (pattern[l] != 'F' && pattern[l] != 'S') return DSA_EINVAL;
+      if (n_layers > 0 && pattern[0] != 'F') return DSA_EINVAL;
+    } else {
+      if (freq < 1) return DSA_EINVAL;
+      const int32_t first = 1 - offset > 0 ? 1 - offset : 0;
+      if (n_layers > 0 && first % freq != 0) return DSA_EINVAL;
+    }
+  }
+  int32_t producer = 0;
+  for (int32_t l = 0; l < n_layers; ++l) {
+    bool full = true;
+    if (use_index_cache) {
+      if (pattern != nullptr) {
+        full = pattern[l] == 'F';
+      } else {
+        const int64_t v = static_cast<int64_t>(l) - offset + 1;
+        full = (v > 0 ? v : 0) % freq == 0;
+      }
+    }
+    if (full) producer = l;
+    fs_out[l] = full ? 'F' : 'S';
+    producer_out[l] = producer;
+  }
+  return DSA_OK;
+}
+
+size_t dsa_layer_stack_workspace_size(const DsaBatch* batch, int32_t topk) {
+  if (check_batch(batch) != DSA_OK) return 0;
+  const size_t T = static_cast<size_t>(batch->num_tokens);
+  size_t bytes = align_up(T * kHeads * kDim, 256) + align_up(T * kHeads * 4, 256);
+  return bytes + dsa_indexer_workspace_size(batch, topk);
+}
+
+int dsa_layer_stack_run(const DsaStackPlan* plan, const DsaBatch* batch, const int64_t* slot_mapping,
+                        int32_t* topk_buf, int32_t* phys_buf, int32_t* valid_buf, dsa_layer_consumer_fn consumer,
+                        void* user, void* ws, size_t ws_bytes, int32_t* dev_err, dsa_stream_t stream) {
+  int st = check_batch(batch);
+  if (st != DSA_OK) return st;
+  if (plan == nullptr || plan->n_layers < 0 || (plan->n_layers > 0 && (plan->fs == nullptr || plan->layers == nullptr)))
+    return DSA_EINVAL;
+  if (!topk_ok(plan->topk)) return DSA_EINVAL;
+  if (plan->n_layers > 0 && plan->fs[0] != 'F') return DSA_EINVAL;
+  for (int32_t l = 0; l < plan->n_layers; ++l) {
+    const char c = plan->fs[l];
+    if (c != 'F' && c != 'S') return DSA_EINVAL;
+    if (c == 'F' && batch->num_tokens > 0) {
+      const DsaLayerInputs& L = plan->layers[l];
+      if (!L.q || !L.w || !L.k_cache || !aligned16(L.q) || !aligned16(L.k_cache)) return DSA_EINVAL;
+      if (L.k_new != nullptr && (slot_mapping == nullptr || !aligned16(L.k_new))) return DSA_EINVAL;
+    }
+  }
+  if (batch->num_tokens > 0 && (!topk_buf || !phys_buf || !ws || !aligned16(ws))) return DSA_EINVAL;
+  if (ws_bytes < dsa_layer_stack_workspace_size(batch, plan->topk)) return DSA_ENOSPACE;
+  const size_t T = static_cast<size_t>(batch->num_tokens);
+  uint8_t* q8 = static_cast<uint8_t*>(ws);
+  float* wf = reinterpret_cast<float*>(q8 + align_up(T * kHeads * kDim, 256));
+  void* iws = reinterpret_cast<uint8_t*>(wf) + align_up(T * kHeads * 4, 256);
+  IndexerWs w = carve(batch, iws);
+  const int64_t ld = logits_ld(batch);
+  bool planned = false;
+  int32_t producer = 0;
+  for (int32_t l = 0; l < plan->n_layers; ++l) {
+    if (plan->fs[l] == 'F') {
+      producer = l;
+      if (batch->num_tokens > 0) {
+        const DsaLayerInputs& L = plan->layers[l];
+        if (L.k_new != nullptr) {
+          st = dsa_indexer_k_quant_write(L.k_new, batch->num_tokens, kDim, slot_mapping, L.k_cache,
+                                         batch->num_blocks, dev_err, stream);
+          if (st != DSA_OK) return st;
+        }
+        st = dsa_indexer_q_quant_fold(L.q, L.w, batch->num_tokens, plan->softmax_scale, q8, nullptr, wf, stream);
+        if (st != DSA_OK) return st;
+        // the batch layout is the same for every layer of the step: plan once
+        st = run_logits(batch, q8, wf, L.k_cache, w.logits, ld, w, dev_err, stream, !planned);
+        if (st != DSA_OK) return st;
+        planned = true;
+        st = from_cuda(launch_topk(w.logits, ld, batch->query_start_loc, batch->seq_lens, batch->req_id_per_token,
+                                   batch->num_reqs, batch->num_tokens, plan->topk, topk_buf, stream));
+        if (st != DSA_OK) return st;
+        st = dsa_topk_logical_to_physical(topk_buf, batch->num_tokens, plan->topk, batch->req_id_per_token,
+                                          batch->block_table, batch->bt_stride, plan->block_stride_rows, phys_buf,
+                                          valid_buf, dev_err, stream);
+        if (st != DSA_OK) return st;
+      }
+    }
+    if (consumer != nullptr) consumer(l, producer, phys_buf, valid_buf, user);
+  }
+  return DSA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,63 @@
+// kernels.h — host-side launchers of the sm_103a kernels (internal to the library).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dsaidx.h"
+
+namespace dsa {
+
+constexpr int kHeads = DSA_HEADS;
+constexpr int kDim = DSA_HEAD_DIM;
+constexpr int kBlock = DSA_BLOCK_SIZE;
+constexpr int kPageBytes = DSA_PAGE_BYTES;
+constexpr int kScaleOffset = kBlock * kDim;  // 8192: the 64 fp32 scales follow the 64 K rows
+
+// One query block: NTOK consecutive query tokens of one request.
+struct QBlock {
+  int32_t req;  // request
+  int32_t t0;   // first token (row of q / logits)
+  int32_t ntok; // tokens in the block (1..NTOK)
+  int32_t p0;   // position of the first token; token i sees keys [0, p0 + i]
+};
+
+// Work plan of one kernel segment, in device memory.
+struct SegmentPlan {
+  QBlock* qb;           // [max_qb]
+  int32_t* tile_start;  // [max_qb + 1]: exclusive prefix of 128-key tiles; tile_start[nqb] = total
+  int32_t* nqb;         // [1]
+  int32_t* req_base;    // [B + 1] scratch
+};
+
+cudaError_t launch_k_quant_write(const void* k, int64_t n, int64_t row_stride, const int64_t* slot_mapping,
+                                 uint8_t* cache, int64_t num_blocks, int32_t* err, cudaStream_t stream);
+cudaError_t launch_q_quant_fold(const void* q, const float* w, int64_t n_tokens, float softmax_scale,
+                                uint8_t* q_fp8, float* q_scale, float* w_folded, cudaStream_t stream);
+cudaError_t launch_convert(const int32_t* logical, int64_t n_tokens, int topk, const int32_t* req_id,
+                           const int32_t* block_table, int64_t bt_stride, int stride_rows, int32_t* physical,
+                           int32_t* valid_counts, int32_t* err, cudaStream_t stream);
+
+cudaError_t launch_plan(const int32_t* qsl, const int32_t* seq_lens, int num_reqs, int num_decodes, int num_tokens,
+                        int64_t bt_stride, SegmentPlan dec, SegmentPlan pre, int32_t* err, cudaStream_t stream);
+
+struct LogitsArgs {
+  const float* w_folded;
+  const uint8_t* k_cache;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  int64_t num_blocks;
+  float* logits;
+  int64_t ld;
+  int32_t* err;
+};
+
+// ntok_per_block = 1 (decode segment) or 4 (prefill segment).
+cudaError_t launch_logits(int ntok_per_block, const CUtensorMap* tmap_k, const CUtensorMap* tmap_q,
+                          SegmentPlan plan, const LogitsArgs& a, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_topk(const float* logits, int64_t ld, const int32_t* qsl, const int32_t* seq_lens,
+                        const int32_t* req_id, int num_reqs, int n_tokens, int topk, int32_t* out, cudaStream_t stream);
+
+}  // namespace dsa

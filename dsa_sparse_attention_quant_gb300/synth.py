@@ -300,21 +300,21 @@ def decode32(scale: float = 1.0, n_reqs: int = 32) -> Batch:
     """32 decode requests, context uniform on [4096, 8192], permuted table, top-2048."""
     lo, hi = int(4096 * scale), int(8192 * scale)
     lens = uniform_int(1, STREAM_LEN, max(2, lo), max(2, hi), n_reqs)
-    topk = 2048 if scale >= 1.0 else max(16, int(2048 * scale))
+    topk = 2048 if scale >= 1.0 else max(16, int(2048 * scale) // 4 * 4)
     return make_batch(1, lens, [], topk, name="decode32")
 
 
 def prefill4x8k(scale: float = 1.0, n_reqs: int = 4) -> Batch:
     """4 causal prefills of 8192 tokens (fresh requests), shuffled pages, top-2048."""
     L = max(8, int(8192 * scale))
-    topk = 2048 if scale >= 1.0 else max(16, int(2048 * scale))
+    topk = 2048 if scale >= 1.0 else max(16, int(2048 * scale) // 4 * 4)
     return make_batch(2, [], [(L, L)] * n_reqs, topk, name="prefill4x8k")
 
 
 def decode8x128k(scale: float = 1.0, n_reqs: int = 8) -> Batch:
     """8 decode requests at 131072 context, random table, top-2048."""
     L = max(2, int(131072 * scale))
-    topk = 2048 if scale >= 1.0 else max(16, int(2048 * scale))
+    topk = 2048 if scale >= 1.0 else max(16, int(2048 * scale) // 4 * 4)
     return make_batch(3, [L] * n_reqs, [], topk, name="decode8x128k")
 
 
@@ -329,7 +329,7 @@ def stack_layer(layer: int, scale: float = 1.0, n_decode: int = 64) -> Batch:
     """
     L = max(2, int(32768 * scale))
     P = max(8, int(4096 * scale))
-    topk = 2048 if scale >= 1.0 else max(16, int(2048 * scale))
+    topk = 2048 if scale >= 1.0 else max(16, int(2048 * scale) // 4 * 4)
     return make_batch(1000 * 5 + layer, [L] * n_decode, [(P, P)], topk, name=f"stack61.l{layer}")
 
 

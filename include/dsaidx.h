@@ -1,0 +1,254 @@
+/*
+ * dsaidx.h — C ABI of the GB300 (sm_103a) DSA sparse-attention indexer with
+ * IndexCache cross-layer reuse.
+ *
+ * The operation is DeepSeek-V3.2's "lightning indexer" as vLLM runs it,
+ * described by three web pages, cited by short name:
+ *   [IC] "IndexCache：DeepSeek 稀疏注意力中的跨层索引复用" (atomage.cn) —
+ *        snippets of `Indexer.forward`, the FP8 indexer K cache
+ *        (`DeepseekV32IndexerCache`, `DeepseekV32IndexerBackend`),
+ *        `SparseAttnIndexer`, `DeepseekV32IndexerMetadata`, the IndexCache
+ *        layer schedule and the shared `topk_indices_buffer`;
+ *   [PR] "PR #37735 完整报告" (prhub.com.cn), vLLM "[Feature]: IndexCache
+ *        support for DSA models" — sections 实现拆解, 关键源码片段, 风险与影响;
+ *   [IG] "vllm.v1.attention.backends.mla.index_group" (docs.vllm.ai) —
+ *        `SparseMLAIndexGroup._convert_once`, `SparseMLAIndexGroupBuilder`.
+ *
+ * Shapes are fixed by the model: H = 64 indexer heads of dim D = 128 sharing
+ * one K row per token (MQA), pages of 64 slots.
+ *
+ * Conventions for every entry point:
+ *  - Ownership: the caller owns every buffer. Pointers marked "device" are
+ *    device memory of the current CUDA device; "host" pointers are read
+ *    during the call only. The library never allocates device memory: the
+ *    scratch an entry point needs is a caller buffer of the size that the
+ *    matching *_workspace_size() returns.
+ *  - Launches are asynchronous on `stream` (NULL = legacy default stream);
+ *    a call returns once its kernels are queued.
+ *  - Status: every entry point returns DSA_OK (0) or an error code below;
+ *    dsa_status_string() names it. Argument errors are found on the host
+ *    before anything is launched (nothing is written then).
+ *  - Device error word: entry points that take `dev_err` (a device int32,
+ *    zeroed by the caller) OR a DSA_DEVERR_* bit into it when the data is
+ *    inconsistent — a slot or block id outside the cache, a token id beyond
+ *    its block-table row, a wait that ran out of time. The kernel then skips
+ *    the offending access (no trap, no fault) and keeps going; results that
+ *    depend on the skipped data are unspecified. dev_err may be NULL.
+ *  - Alignment: all device pointers 16-byte aligned; the K cache is
+ *    num_blocks pages of 8448 bytes.
+ */
+#ifndef DSAIDX_H
+#define DSAIDX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *dsa_stream_t; /* same type as cudaStream_t */
+
+#if defined(__GNUC__)
+#define DSA_API __attribute__((visibility("default")))
+#else
+#define DSA_API
+#endif
+
+/* ---------------------------------------------------------------- status */
+#define DSA_OK 0
+#define DSA_EINVAL 1   /* bad argument: shape, pointer, pattern, frequency, size */
+#define DSA_ECUDA 2    /* a CUDA runtime/driver call failed */
+#define DSA_EDEVICE 3  /* the device error word is nonzero (dsa_check_device_error) */
+#define DSA_ENOSPACE 4 /* workspace smaller than *_workspace_size() */
+#define DSA_ENODEV 5   /* no sm_103a device / kernel image for this device */
+
+#define DSA_DEVERR_SLOT_RANGE 1u  /* slot_mapping entry >= num_blocks*64 */
+#define DSA_DEVERR_BLOCK_RANGE 2u /* block-table entry outside [0, num_blocks) for a visible key */
+#define DSA_DEVERR_ID_RANGE 4u    /* top-k id past its request's block-table row */
+#define DSA_DEVERR_TIMEOUT 8u     /* a pipeline wait gave up (about 1 s); kernel returned early */
+#define DSA_DEVERR_SEQ_RANGE 16u  /* seq_len < q_len, or seq_len beyond the block-table row */
+
+#define DSA_HEADS 64
+#define DSA_HEAD_DIM 128
+#define DSA_BLOCK_SIZE 64
+#define DSA_SLOT_BYTES 132                        /* 128 B FP8 K + 4 B fp32 scale */
+#define DSA_PAGE_BYTES (DSA_BLOCK_SIZE * DSA_SLOT_BYTES) /* 8448 */
+
+DSA_API const char *dsa_status_string(int status);
+DSA_API int dsa_version(void); /* major*10000 + minor*100 + patch */
+
+/* Copy the device error word to *out (synchronising `stream`) and return
+ * DSA_EDEVICE if it is nonzero, DSA_OK otherwise. */
+DSA_API int dsa_check_device_error(const int32_t *dev_err, uint32_t *out, dsa_stream_t stream);
+
+/* ------------------------------------------------------------ the batch */
+/* One step's attention metadata, after [IC] `DeepseekV32IndexerMetadata`
+ * (seq_lens, slot_mapping, num_decodes, ...) and the decode-first ordering of
+ * [IG] `HiSparseMLAIndexGroup` (decode requests occupy rows [0, num_decodes)).
+ * Request r has q_len[r] = query_start_loc[r+1] - query_start_loc[r] query
+ * tokens and seq_lens[r] keys in total, this step's tokens included; query
+ * token i of request r sits at position seq_lens[r] - q_len[r] + i and sees
+ * keys [0, position] (causal, itself included). Key s of request r lives in
+ * slot block_table[r*bt_stride + s/64]*64 + s%64 of the paged cache. */
+typedef struct DsaBatch {
+  int32_t num_reqs;        /* B >= 0 */
+  int32_t num_decodes;     /* requests [0, num_decodes) are run by the decode kernel */
+  int32_t num_tokens;      /* T = query_start_loc[B] (host copy) */
+  int32_t max_seq_len;     /* host upper bound of seq_lens[*]; sizes the score rows */
+  int64_t bt_stride;       /* row stride of block_table, int32 elements */
+  int64_t num_blocks;      /* pages in the K cache */
+  const int32_t *query_start_loc;  /* device [B+1] */
+  const int32_t *seq_lens;         /* device [B] */
+  const int32_t *block_table;      /* device [B, bt_stride] */
+  const int32_t *req_id_per_token; /* device [T] */
+} DsaBatch;
+
+/* ------------------------------------------------- S1: K quant + cache */
+/* [IC] `SparseAttnIndexer` body, `indexer_k_quant_and_cache(k, kv_cache,
+ * slot_mapping, quant_block_size, scale_fmt)`: each token's 128-dim K row is
+ * quantised to FP8 E4M3 with one power-of-two (ue8m0) fp32 scale,
+ * scale = 2^ceil(log2(max(amax, 1e-10)/448)), codes = RNE_satfinite(k/scale),
+ * and stored at its slot: K bytes at page*8448 + (slot%64)*128, the scale at
+ * page*8448 + 8192 + (slot%64)*4 (page = slot/64) — 132 bytes per slot as in
+ * the [IC] FP8 cache snippet ("128 bytes K + 4 bytes FP32 scale").
+ *   k            device bf16 [n_tokens, k_row_stride] (first 128 used)
+ *   slot_mapping device int64 [n_tokens]; -1 = padding token, skipped
+ *   k_cache      device uint8 [num_blocks, 8448], written in place
+ * Slots >= num_blocks*64 are skipped and flag DSA_DEVERR_SLOT_RANGE. */
+DSA_API int dsa_indexer_k_quant_write(const void *k, int64_t n_tokens, int64_t k_row_stride,
+                              const int64_t *slot_mapping, uint8_t *k_cache,
+                              int64_t num_blocks, int32_t *dev_err, dsa_stream_t stream);
+
+/* --------------------------------------- S2a: q quant + weight folding */
+/* [IC] `Indexer.forward`: q viewed as rows of 128 is quantised per row with a
+ * ue8m0 scale exactly like K above, and the head weights absorb the scales,
+ * w'[t,h] = w[t,h] * q_scale[t,h] * softmax_scale * 64^-0.5 (fp32, in that
+ * order).
+ *   q        device bf16 [n_tokens, 64, 128] contiguous
+ *   w        device fp32 [n_tokens, 64]
+ *   q_fp8    device uint8 [n_tokens, 64, 128] (E4M3 codes), written
+ *   q_scale  device fp32 [n_tokens, 64] or NULL, written
+ *   w_folded device fp32 [n_tokens, 64], written
+ *   softmax_scale <= 0 selects 128^-0.5. */
+DSA_API int dsa_indexer_q_quant_fold(const void *q, const float *w, int64_t n_tokens,
+                             float softmax_scale, uint8_t *q_fp8, float *q_scale,
+                             float *w_folded, dsa_stream_t stream);
+
+/* ---------------------------------------- S2b + S3: logits and top-k */
+/* Indexer scores over the causal keys of every query token,
+ *   I[t,s] = k_scale[s] * sum_h w'[t,h] * ReLU(sum_d q8[t,h,d] * k8[s,d]),
+ * FP8 x FP8 products accumulated in fp32 on the tensor cores, then the rows'
+ * top-k ([IC]: the op fills `topk_indices_buffer`, whose rows start as -1).
+ * topk_out[t, :] receives the request-local key ids of the `topk` largest
+ * scores of row t, in no particular order, followed by -1 when the row has
+ * fewer than `topk` keys. Every row [0, T) is written.
+ *   q_fp8, w_folded  from dsa_indexer_q_quant_fold
+ *   k_cache          device uint8 [num_blocks, 8448]; must hold every key the
+ *                    rows see (write this step's K first, or pass k_new)
+ *   topk             1..4096, multiple of 4
+ *   topk_out         device int32 [T, topk]
+ *   ws, ws_bytes     device scratch of dsa_indexer_workspace_size() bytes
+ *   k_new, slot_mapping  optional (both NULL = [IC]'s skip_k_cache_insert):
+ *                    this step's bf16 K rows [T,128] and their slots; they are
+ *                    quantised into k_cache before any score is computed. */
+DSA_API size_t dsa_indexer_workspace_size(const DsaBatch *batch, int32_t topk);
+DSA_API int dsa_indexer_logits_topk(const DsaBatch *batch, const uint8_t *q_fp8,
+                            const float *w_folded, uint8_t *k_cache, int32_t topk,
+                            int32_t *topk_out, void *ws, size_t ws_bytes,
+                            const void *k_new, const int64_t *slot_mapping,
+                            int32_t *dev_err, dsa_stream_t stream);
+
+/* The steps of the call above, one by one.
+ * dsa_indexer_plan splits the batch into work items (query blocks x 128-key
+ * tiles) and stores the plan in ws; it depends only on the batch metadata,
+ * so one plan serves every layer of a step.
+ * dsa_indexer_logits needs a plan in ws (same batch) and writes I[t, s] for
+ * s in [0, position_t] to logits[t*logits_ld + s] (fp32; other entries
+ * untouched); logits_ld >= max_seq_len.
+ * dsa_indexer_topk selects from such a score matrix (ws unused, may be NULL). */
+DSA_API int dsa_indexer_plan(const DsaBatch *batch, void *ws, size_t ws_bytes, int32_t *dev_err,
+                     dsa_stream_t stream);
+DSA_API int dsa_indexer_logits(const DsaBatch *batch, const uint8_t *q_fp8, const float *w_folded,
+                       const uint8_t *k_cache, float *logits, int64_t logits_ld,
+                       void *ws, size_t ws_bytes, int32_t *dev_err, dsa_stream_t stream);
+DSA_API int dsa_indexer_topk(const DsaBatch *batch, const float *logits, int64_t logits_ld,
+                     int32_t topk, int32_t *topk_out, void *ws, size_t ws_bytes,
+                     dsa_stream_t stream);
+
+/* ------------------------------------------ S5: logical -> physical ids */
+/* [IG] `SparseMLAIndexGroup._convert_once` (the conversion kernel it calls):
+ * physical = block_table[req][id/64] * block_stride_rows + id%64, -1 stays -1;
+ * valid_counts[t] = number of ids >= 0 in row t.
+ *   logical          device int32 [n_tokens, topk]
+ *   req_id_per_token device int32 [n_tokens]
+ *   block_table      device int32 [*, bt_stride]
+ *   block_stride_rows  rows per physical block; <= 0 selects 64
+ *   physical         device int32 [n_tokens, topk], written
+ *   valid_counts     device int32 [n_tokens] or NULL, written
+ * An id whose page lies past bt_stride, or a negative block entry, gives -1
+ * and flags DSA_DEVERR_ID_RANGE. */
+DSA_API int dsa_topk_logical_to_physical(const int32_t *logical, int64_t n_tokens, int32_t topk,
+                                 const int32_t *req_id_per_token, const int32_t *block_table,
+                                 int64_t bt_stride, int32_t block_stride_rows,
+                                 int32_t *physical, int32_t *valid_counts,
+                                 int32_t *dev_err, dsa_stream_t stream);
+
+/* ------------------------------------------------ S4: IndexCache schedule */
+/* [IC] layer-construction snippet and [PR] 关键源码片段: with IndexCache on,
+ * layer l is 'S' (reuses the previous top-k) iff max(l - offset + 1, 0) % freq
+ * != 0 (offset 2 by default, i.e. max(l-1,0) % freq), unless an explicit
+ * pattern is given ('F' = compute, 'S' = reuse); with it off every layer is
+ * 'F'. producer_out[l] = the 'F' layer whose top-k layer l consumes.
+ * Host-only, synchronous. Stricter than the page ([PR] 风险与影响): the
+ * pattern must be exactly n_layers characters of 'F'/'S' starting with 'F';
+ * freq >= 1; layer 0 must be 'F'. Otherwise DSA_EINVAL and nothing written.
+ *   fs_out       host char [n_layers] ('F'/'S', not NUL-terminated)
+ *   producer_out host int32 [n_layers] */
+DSA_API int dsa_schedule_build(int32_t n_layers, int32_t use_index_cache, int32_t freq,
+                       int32_t offset, const char *pattern, char *fs_out,
+                       int32_t *producer_out);
+
+/* ------------------------------------------- the layer-schedule runner */
+/* One decoding step over a stack of DSA layers with IndexCache: [IC] F/S
+ * layer forward and [IG] `SparseMLAIndexGroup` (one group = an F layer and
+ * the S layers after it; the leader converts the group's indices once).
+ * For every 'F' layer l (per the schedule): quantise this step's K of layer l
+ * into its cache, quantise q and fold w, run logits + top-k into topk_buf,
+ * convert to physical ids in phys_buf/valid_buf (once for the group). Then
+ * for every layer (F or S) the optional consumer is called on the host with
+ * the group's buffers, in layer order, after that layer's device work is
+ * queued on `stream`; it may enqueue its own work on the stream (the sparse
+ * attention that reads the indices). 'S' layers own no indexer inputs: their
+ * entries of `layers` are ignored and may be zero. */
+typedef struct DsaLayerInputs {
+  const void *q;        /* device bf16 [T, 64, 128] */
+  const float *w;       /* device fp32 [T, 64] */
+  const void *k_new;    /* device bf16 [T, 128] or NULL (skip the cache insert) */
+  uint8_t *k_cache;     /* device uint8 [num_blocks, 8448] */
+} DsaLayerInputs;
+
+typedef void (*dsa_layer_consumer_fn)(int32_t layer, int32_t producer,
+                                      const int32_t *physical, const int32_t *valid_counts,
+                                      void *user);
+
+typedef struct DsaStackPlan {
+  int32_t n_layers;
+  const char *fs;                 /* host [n_layers] from dsa_schedule_build */
+  const DsaLayerInputs *layers;   /* host [n_layers] */
+  int32_t topk;
+  float softmax_scale;            /* <= 0 selects 128^-0.5 */
+  int32_t block_stride_rows;      /* for the conversion; <= 0 selects 64 */
+} DsaStackPlan;
+
+DSA_API size_t dsa_layer_stack_workspace_size(const DsaBatch *batch, int32_t topk);
+DSA_API int dsa_layer_stack_run(const DsaStackPlan *plan, const DsaBatch *batch,
+                        const int64_t *slot_mapping, int32_t *topk_buf,
+                        int32_t *phys_buf, int32_t *valid_buf,
+                        dsa_layer_consumer_fn consumer, void *user, void *ws,
+                        size_t ws_bytes, int32_t *dev_err, dsa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSAIDX_H */

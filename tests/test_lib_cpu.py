@@ -1,0 +1,85 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every symbol
+that include/dsaidx.h declares, runs its host-only schedule builder exactly
+like the oracle, and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import oracle
+from dsa_sparse_attention_quant_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "dsaidx.h")).read()
+    return sorted(set(re.findall(r"DSA_API\s+[\w\s\*]*?\b(dsa_\w+)\s*\(", text)))
+
+
+def test_header_declares_binding_symbols():
+    assert declared_symbols() == sorted(binding.SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = binding.load()
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert lib.dsa_version() == 100
+    assert lib.dsa_status_string(0) == b"ok"
+    assert b"invalid" in lib.dsa_status_string(1)
+
+
+@pytest.mark.parametrize("n_layers", [0, 1, 2, 5, 13, 61, 96])
+@pytest.mark.parametrize("freq", [1, 2, 3, 4, 7])
+@pytest.mark.parametrize("offset", [1, 2, 3])
+def test_schedule_matches_oracle(n_layers, freq, offset):
+    for use in (False, True):
+        want = oracle.schedule(n_layers, use, freq, offset)
+        got = binding.schedule_build(n_layers, use, freq, offset)
+        assert got[0] == want[0]
+        assert got[1] == want[1].tolist()
+
+
+def test_schedule_patterns_and_rejections():
+    for pat in ["F", "FS", "FFSSF", "F" + "S" * 60, "FSFSFSFS"]:
+        want = oracle.schedule(len(pat), True, 4, 2, pat)
+        got = binding.schedule_build(len(pat), True, 4, 2, pat)
+        assert got[0] == want[0] and got[1] == want[1].tolist()
+    for kw in [dict(n_layers=3, pattern="FSX"), dict(n_layers=3, pattern="FS"), dict(n_layers=2, pattern="SF"),
+               dict(n_layers=4, freq=0), dict(n_layers=4, freq=3, offset=0), dict(n_layers=-1)]:
+        args = dict(use_index_cache=True, freq=4, offset=2, pattern=None)
+        args.update(kw)
+        with pytest.raises(binding.DsaError):
+            binding.schedule_build(**args)
+        with pytest.raises(ValueError):
+            oracle.schedule(**args)
+
+
+def test_host_validation_without_gpu():
+    lib = binding.load()
+    P = ctypes.c_void_p
+    # negative token count, bad row stride, bad top-k: rejected on the host
+    assert lib.dsa_indexer_k_quant_write(P(16), -1, 128, P(16), P(16), 1, None, None) == binding.DSA_EINVAL
+    assert lib.dsa_indexer_k_quant_write(P(16), 4, 100, P(16), P(16), 1, None, None) == binding.DSA_EINVAL
+    assert lib.dsa_topk_logical_to_physical(P(16), 4, 6, P(16), P(16), 1, 0, P(16), None, None,
+                                            None) == binding.DSA_EINVAL
+    assert lib.dsa_topk_logical_to_physical(P(16), 4, 8192, P(16), P(16), 1, 0, P(16), None, None,
+                                            None) == binding.DSA_EINVAL
+    b = binding.DsaBatchC(1, 2, 1, 10, 1, 1, 16, 16, 16, 16)  # num_decodes > num_reqs
+    assert lib.dsa_indexer_workspace_size(ctypes.byref(b), 64) == 0
+    # empty batches are no-ops that succeed without a device
+    assert lib.dsa_indexer_k_quant_write(None, 0, 128, None, P(16), 1, None, None) == binding.DSA_OK
+    empty = binding.DsaBatchC(0, 0, 0, 0, 1, 1, None, None, None, None)
+    assert lib.dsa_indexer_logits_topk(ctypes.byref(empty), None, None, None, 64, None, None, 0, None, None,
+                                       None, None) == binding.DSA_OK
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")
+def test_valid_call_without_gpu_reports_no_device():
+    lib = binding.load()
+    P = ctypes.c_void_p
+    st = lib.dsa_indexer_k_quant_write(P(256), 4, 128, P(256), P(256), 1, None, None)
+    assert st == binding.DSA_ENODEV
