@@ -272,7 +272,8 @@ int dsa_indexer_topk(const DsaBatch* batch, const float* logits, int64_t logits_
   int sms;
   if ((st = device_sms(&sms)) != DSA_OK) return st;
   return from_cuda(launch_topk(logits, logits_ld, batch->query_start_loc, batch->seq_lens,
-                               batch->req_id_per_token, batch->num_reqs, batch->num_tokens, topk, topk_out, stream));
+                               batch->req_id_per_token, batch->num_reqs, batch->num_tokens, topk, topk_out, nullptr,
+                               stream));
 }
 
 int dsa_indexer_logits_topk(const DsaBatch* batch, const uint8_t* q_fp8, const float* w_folded, uint8_t* k_cache,
@@ -298,7 +299,7 @@ int dsa_indexer_logits_topk(const DsaBatch* batch, const uint8_t* q_fp8, const f
   st = run_logits(batch, q_fp8, w_folded, k_cache, w.logits, ld, w, dev_err, stream, true);
   if (st != DSA_OK) return st;
   return from_cuda(launch_topk(w.logits, ld, batch->query_start_loc, batch->seq_lens, batch->req_id_per_token,
-                               batch->num_reqs, batch->num_tokens, topk, topk_out, stream));
+                               batch->num_reqs, batch->num_tokens, topk, topk_out, nullptr, stream));
 }
 
 int dsa_topk_logical_to_physical(const int32_t* logical, int64_t n_tokens, int32_t topk,
@@ -402,12 +403,11 @@ int dsa_layer_stack_run(const DsaStackPlan* plan, const DsaBatch* batch, const i
         st = run_logits(batch, q8, wf, L.k_cache, w.logits, ld, w, dev_err, stream, !planned);
         if (st != DSA_OK) return st;
         planned = true;
+        // S3 with S5 fused into its output pass: logical ids, physical ids, valid counts
+        TopkPhys tp{batch->block_table, batch->bt_stride,
+                    plan->block_stride_rows > 0 ? plan->block_stride_rows : kBlock, phys_buf, valid_buf, dev_err};
         st = from_cuda(launch_topk(w.logits, ld, batch->query_start_loc, batch->seq_lens, batch->req_id_per_token,
-                                   batch->num_reqs, batch->num_tokens, plan->topk, topk_buf, stream));
-        if (st != DSA_OK) return st;
-        st = dsa_topk_logical_to_physical(topk_buf, batch->num_tokens, plan->topk, batch->req_id_per_token,
-                                          batch->block_table, batch->bt_stride, plan->block_stride_rows, phys_buf,
-                                          valid_buf, dev_err, stream);
+                                   batch->num_reqs, batch->num_tokens, plan->topk, topk_buf, &tp, stream));
         if (st != DSA_OK) return st;
       }
     }

@@ -57,7 +57,18 @@ struct LogitsArgs {
 cudaError_t launch_logits(int ntok_per_block, const CUtensorMap* tmap_k, const CUtensorMap* tmap_q,
                           SegmentPlan plan, const LogitsArgs& a, int num_sms, cudaStream_t stream);
 
+// Optional S5 fused into the top-k output: physical ids and valid counts.
+struct TopkPhys {
+  const int32_t* block_table;
+  int64_t bt_stride;
+  int stride_rows;
+  int32_t* physical;
+  int32_t* valid_counts;  // may be nullptr
+  int32_t* err;
+};
+
 cudaError_t launch_topk(const float* logits, int64_t ld, const int32_t* qsl, const int32_t* seq_lens,
-                        const int32_t* req_id, int num_reqs, int n_tokens, int topk, int32_t* out, cudaStream_t stream);
+                        const int32_t* req_id, int num_reqs, int n_tokens, int topk, int32_t* out,
+                        const TopkPhys* phys, cudaStream_t stream);
 
 }  // namespace dsa

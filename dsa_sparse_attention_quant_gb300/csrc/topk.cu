@@ -1,9 +1,13 @@
-// topk.cu — S3: per-row top-k of the indexer scores (sm_103a).
+// topk.cu — S3: per-row top-k of the indexer scores (sm_103a), optionally
+// fused with S5 (logical -> physical ids).
 //
 // "IndexCache：DeepSeek 稀疏注意力中的跨层索引复用" (atomage.cn): the indexer op
 // resets the rows of the shared `topk_indices_buffer` to -1 and fills each
 // row with the ids of the `index_topk` highest-scoring keys. A row with fewer
-// visible keys than k keeps -1 in the tail.
+// visible keys than k keeps -1 in the tail. "vllm.v1.attention.backends.mla.
+// index_group" (`_convert_once`): the consumers want physical slots,
+// block_table[req][id/64] * block_stride_rows + id%64, and the count of valid
+// ids per row; when asked, each selected id is converted as it is written.
 //
 // Exact radix select over order-preserving 32-bit keys of the fp32 scores: up
 // to three histogram rounds (11, 11 and 10 bits) narrow down the k-th largest
@@ -21,8 +25,9 @@ constexpr int kBins = 2048;
 constexpr int kRowCap = 12288;  // scores staged in shared memory: 48 KB
 
 __device__ __forceinline__ int row_length(int t, const int32_t* qsl, const int32_t* seq_lens, const int32_t* req_id,
-                                          int num_reqs, int64_t ld) {
+                                          int num_reqs, int64_t ld, int* req) {
   const int r = req_id[t];
+  *req = r;
   if (r < 0 || r >= num_reqs) return 0;
   const int q0 = qsl[r], ql = qsl[r + 1] - q0;
   int n = seq_lens[r] - ql + (t - q0) + 1;
@@ -74,11 +79,31 @@ __device__ void find_bin(const uint32_t* hist, uint32_t need, int* s_bin, uint32
   __syncthreads();
 }
 
+struct PhysOut {
+  const int32_t* block_table;  // nullptr: logical ids only
+  int64_t bt_stride;
+  int stride_rows;
+  int32_t* physical;
+  int32_t* valid_counts;
+  int32_t* err;
+};
+
+__device__ __forceinline__ void emit(int32_t* orow, int32_t* prow, const int32_t* bt_row, int64_t bt_stride,
+                                     int stride_rows, uint32_t pos, int id, bool* bad) {
+  orow[pos] = id;
+  if (prow != nullptr) {
+    const int64_t page = id / kBlock;
+    const int32_t blk = page < bt_stride ? __ldg(bt_row + page) : -1;
+    if (blk < 0) *bad = true;
+    prow[pos] = blk < 0 ? -1 : blk * stride_rows + id % kBlock;
+  }
+}
+
 template <bool kStaged>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restrict__ logits, int64_t ld,
                                                             const int32_t* qsl, const int32_t* seq_lens,
                                                             const int32_t* req_id, int num_reqs, int topk,
-                                                            int32_t* __restrict__ out) {
+                                                            int32_t* __restrict__ out, PhysOut po) {
   extern __shared__ uint32_t sh[];
   uint32_t* hist = sh;
   uint32_t* keys = sh + kBins;
@@ -88,11 +113,27 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
 
   const int t = blockIdx.x;
   const int tid = threadIdx.x;
-  const int n = row_length(t, qsl, seq_lens, req_id, num_reqs, ld);
+  int r;
+  const int n = row_length(t, qsl, seq_lens, req_id, num_reqs, ld, &r);
   int32_t* orow = out + static_cast<int64_t>(t) * topk;
+  int32_t* prow = po.block_table != nullptr ? po.physical + static_cast<int64_t>(t) * topk : nullptr;
+  const int32_t* bt_row = po.block_table != nullptr && r >= 0 && r < num_reqs
+                              ? po.block_table + static_cast<int64_t>(r) * po.bt_stride
+                              : nullptr;
+  if (bt_row == nullptr) prow = nullptr;
+  bool bad = false;
+  if (prow != nullptr && po.valid_counts != nullptr && tid == 0) po.valid_counts[t] = n < topk ? n : topk;
   const float* lrow = logits + static_cast<int64_t>(t) * ld;
   if (n <= topk) {
-    for (int i = tid; i < topk; i += kTopkThreads) orow[i] = i < n ? i : -1;
+    for (int i = tid; i < topk; i += kTopkThreads) {
+      if (i < n) {
+        emit(orow, prow, bt_row, po.bt_stride, po.stride_rows, i, i, &bad);
+      } else {
+        orow[i] = -1;
+        if (prow != nullptr) prow[i] = -1;
+      }
+    }
+    if (bad) flag_error(po.err, DSA_DEVERR_ID_RANGE);
     return;
   }
   if constexpr (kStaged) {
@@ -140,14 +181,24 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
     } else if (pk == prefix && atomicAdd(&s_eq, 1u) < need) {
       pos = atomicAdd(&s_cnt, 1u);
     }
-    if (pos < static_cast<uint32_t>(topk)) orow[pos] = i;
+    if (pos < static_cast<uint32_t>(topk)) emit(orow, prow, bt_row, po.bt_stride, po.stride_rows, pos, i, &bad);
   }
+  if (bad) flag_error(po.err, DSA_DEVERR_ID_RANGE);
 }
 
 cudaError_t launch_topk(const float* logits, int64_t ld, const int32_t* qsl, const int32_t* seq_lens,
                         const int32_t* req_id, int num_reqs, int n_tokens, int topk, int32_t* out,
-                        cudaStream_t stream) {
+                        const TopkPhys* phys, cudaStream_t stream) {
   if (n_tokens <= 0) return cudaSuccess;
+  PhysOut po{};
+  if (phys != nullptr) {
+    po.block_table = phys->block_table;
+    po.bt_stride = phys->bt_stride;
+    po.stride_rows = phys->stride_rows;
+    po.physical = phys->physical;
+    po.valid_counts = phys->valid_counts;
+    po.err = phys->err;
+  }
   if (ld <= kRowCap) {
     const int smem = (kBins + kRowCap) * 4;
     static bool configured = false;
@@ -156,10 +207,11 @@ cudaError_t launch_topk(const float* logits, int64_t ld, const int32_t* qsl, con
       if (e != cudaSuccess) return e;
       configured = true;
     }
-    topk_kernel<true><<<n_tokens, kTopkThreads, smem, stream>>>(logits, ld, qsl, seq_lens, req_id, num_reqs, topk, out);
+    topk_kernel<true><<<n_tokens, kTopkThreads, smem, stream>>>(logits, ld, qsl, seq_lens, req_id, num_reqs, topk,
+                                                                out, po);
   } else {
-    topk_kernel<false><<<n_tokens, kTopkThreads, kBins * 4, stream>>>(logits, ld, qsl, seq_lens, req_id,
-                                                                       num_reqs, topk, out);
+    topk_kernel<false><<<n_tokens, kTopkThreads, kBins * 4, stream>>>(logits, ld, qsl, seq_lens, req_id, num_reqs,
+                                                                       topk, out, po);
   }
   return cudaGetLastError();
 }

@@ -211,6 +211,7 @@ def make_batch(
     rope: bool = False,
     spare_blocks: int = 0,
     bt_pad: int = 0,
+    table_seed: int | None = None,
 ) -> Batch:
     """Build a seeded batch.
 
@@ -233,7 +234,7 @@ def make_batch(
     if identity_table:
         perm = np.arange(num_blocks, dtype=np.int64)
     else:
-        perm = permutation(seed, STREAM_PERM, num_blocks)
+        perm = permutation(seed if table_seed is None else table_seed, STREAM_PERM, num_blocks)
     bt_stride = max(pages) + bt_pad
     block_table = np.full((B, bt_stride), -1, dtype=np.int32)
     cur = 0
@@ -325,12 +326,13 @@ STACK_FREQ = 4
 def stack_layer(layer: int, scale: float = 1.0, n_decode: int = 64) -> Batch:
     """One F layer's batch of the 61-layer stack: 64 decodes at 32768 + a 4096-token prefill.
 
-    Every F layer has its own seeded q, w, new K and K cache (seed 5000+layer).
+    Every F layer has its own seeded q, w, new K and K cache (seed 5000+layer);
+    all layers share the step's metadata (lengths and block table, seed 5).
     """
     L = max(2, int(32768 * scale))
     P = max(8, int(4096 * scale))
     topk = 2048 if scale >= 1.0 else max(16, int(2048 * scale) // 4 * 4)
-    return make_batch(1000 * 5 + layer, [L] * n_decode, [(P, P)], topk, name=f"stack61.l{layer}")
+    return make_batch(1000 * 5 + layer, [L] * n_decode, [(P, P)], topk, name=f"stack61.l{layer}", table_seed=5)
 
 
 WORKLOADS = {

@@ -1,0 +1,86 @@
+"""The IndexCache layer-stack runner against the oracle.
+
+Every F layer (own q, w, new K and K cache) runs the whole path; every layer,
+F or S, hands the consumer the buffers of its producer — the nearest F layer
+at or before it — and S layers launch nothing.
+"""
+import numpy as np
+import pytest
+import torch
+
+import dsa_sparse_attention_quant_gb300 as dsa
+import oracle
+from dsa_sparse_attention_quant_gb300 import synth
+from oracle import compare
+from tests.gpu_harness import DEV, bf16_tensor
+
+pytestmark = pytest.mark.gpu
+
+
+def run_stack(n_layers, freq, scale, n_decode, pattern=None, check_rows=None):
+    fs, prod = dsa.schedule_build(n_layers, True, freq, 2, pattern)
+    fs_o, prod_o = oracle.schedule(n_layers, True, freq, 2, pattern)
+    assert fs == fs_o and prod == prod_o.tolist()
+    hbs = {l: synth.stack_layer(l, scale, n_decode) for l in range(n_layers) if fs[l] == "F"}
+    meta = hbs[0]
+    for hb in hbs.values():
+        assert np.array_equal(hb.block_table, meta.block_table)
+    batch = dsa.Batch.from_host(meta, DEV)
+    slots = torch.from_numpy(meta.slot_mapping).to(DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    layers = []
+    for l in range(n_layers):
+        if fs[l] != "F":
+            layers.append(None)
+            continue
+        hb = hbs[l]
+        cache = torch.zeros((hb.num_blocks, 8448), dtype=torch.uint8, device=DEV)
+        dsa.indexer_k_quant_write(bf16_tensor(hb.ctx_k), torch.from_numpy(hb.ctx_slots).to(DEV), cache, err)
+        layers.append(dict(q=bf16_tensor(hb.q), w=torch.from_numpy(hb.w).to(DEV), k_new=bf16_tensor(hb.k_new),
+                           k_cache=cache))
+    T, k = meta.num_tokens, meta.topk
+    topk_buf = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    phys_buf = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    valid_buf = torch.empty(T, dtype=torch.int32, device=DEV)
+    seen = []
+
+    def consumer(layer, producer, phys_ptr, valid_ptr):
+        assert phys_ptr == phys_buf.data_ptr() and valid_ptr == valid_buf.data_ptr()
+        seen.append((layer, producer, phys_buf.clone(), valid_buf.clone(), topk_buf.clone()))
+
+    dsa.layer_stack_run(batch, fs, layers, k, slot_mapping=slots, topk_buf=topk_buf, phys_buf=phys_buf,
+                        valid_buf=valid_buf, consumer=consumer, dev_err=err)
+    torch.cuda.synchronize()
+    assert dsa.check_device_error(err) == 0
+    assert [s[0] for s in seen] == list(range(n_layers))
+    assert [s[1] for s in seen] == prod
+    snap = {s[0]: s for s in seen}
+    for l in range(n_layers):
+        p = prod[l]
+        assert torch.equal(snap[l][2], snap[p][2]) and torch.equal(snap[l][3], snap[p][3])
+    rows = np.arange(T) if check_rows is None else check_rows
+    for l, hb in hbs.items():
+        cache = oracle.fill_cache(hb)
+        assert np.array_equal(layers[l]["k_cache"].cpu().numpy(), cache), f"layer {l}: cache bytes"
+        _, scores = oracle.indexer(hb, cache, rows=rows, with_scores=True)
+        lens = hb.positions[rows] + 1
+        topk = snap[l][4].cpu().numpy()[rows]
+        fails = compare.check_topk(topk, scores, lens, k)
+        assert not fails, f"layer {l}: {fails[:2]}"
+        phys = snap[l][2].cpu().numpy()[rows]
+        for i, t in enumerate(rows):
+            n = int(lens[i])
+            table, _ = oracle.convert(np.arange(n, dtype=np.int32)[None, :], hb.req_id_per_token[t:t + 1],
+                                      hb.block_table)
+            want = np.where(topk[i] >= 0, table[0][np.clip(topk[i], 0, None)], -1)
+            assert np.array_equal(phys[i], want)
+    return fs
+
+
+def test_stack_freq4_scaled():
+    fs = run_stack(9, 4, scale=0.05, n_decode=6)
+    assert fs == "FFSSSFSSS"
+
+
+def test_stack_pattern_scaled():
+    run_stack(6, 4, scale=0.03, n_decode=3, pattern="FSFFSS")
