@@ -194,10 +194,10 @@ def run_ours(args):
         dsa.indexer_q_quant_fold(r.q, r.w, q_fp8=q8, w_folded=wf)                      # S2a
         dsa.indexer_plan(batch, ws, err)
         if ev is not None:
-            ev[0].record(stream)
+            ev[0].record(torch.cuda.current_stream())
         dsa.indexer_logits(batch, q8, wf, r.k_cache, logits=logits, ws=ws, dev_err=err)  # S2b
         if ev is not None:
-            ev[1].record(stream)
+            ev[1].record(torch.cuda.current_stream())
         dsa.indexer_topk(batch, logits, k, topk_out=topk)                               # S3
         dsa.topk_logical_to_physical(topk, batch.req_id_per_token, batch.block_table,   # S5
                                      physical=phys, valid_counts=valid, dev_err=err)

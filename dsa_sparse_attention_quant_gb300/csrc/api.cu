@@ -112,7 +112,12 @@ int check_batch(const DsaBatch* b) {
   return DSA_OK;
 }
 
-int64_t logits_ld(const DsaBatch* b) { return static_cast<int64_t>(align_up(b->max_seq_len > 0 ? b->max_seq_len : 1, 4)); }
+int64_t logits_ld(const DsaBatch* b) {
+  return static_cast<int64_t>(align_up(b->max_seq_len > 0 ? b->max_seq_len : 1, 4));
+}
+
+// Persistent logits grid: one CTA per SM. The plan and the launch must agree on it.
+int grid_ctas(int sms) { return sms < kMaxCtas ? sms : kMaxCtas; }
 
 // Workspace carving of the indexer: both segment plans, then the score matrix.
 struct IndexerWs {
@@ -138,10 +143,12 @@ IndexerWs carve(const DsaBatch* b, void* base) {
   w.dec.tile_start = static_cast<int32_t*>(take((max_dec + 1) * 4));
   w.dec.nqb = static_cast<int32_t*>(take(4));
   w.dec.req_base = static_cast<int32_t*>(take((B + 1) * 4));
+  w.dec.cta = static_cast<CtaWork*>(take(kMaxCtas * sizeof(CtaWork)));
   w.pre.qb = static_cast<QBlock*>(take(max_pre * sizeof(QBlock)));
   w.pre.tile_start = static_cast<int32_t*>(take((max_pre + 1) * 4));
   w.pre.nqb = static_cast<int32_t*>(take(4));
   w.pre.req_base = static_cast<int32_t*>(take((B + 1) * 4));
+  w.pre.cta = static_cast<CtaWork*>(take(kMaxCtas * sizeof(CtaWork)));
   w.logits = static_cast<float*>(take(T * static_cast<size_t>(logits_ld(b)) * 4));
   w.bytes = off;
   return w;
@@ -156,8 +163,8 @@ int run_logits(const DsaBatch* b, const uint8_t* q_fp8, const float* w_folded, c
   int st = device_sms(&sms);
   if (st != DSA_OK) return st;
   if (run_plan) {
-    st = from_cuda(launch_plan(b->query_start_loc, b->seq_lens, b->num_reqs, b->num_decodes, b->num_tokens, b->bt_stride, ws.dec,
-                               ws.pre, dev_err, stream));
+    st = from_cuda(launch_plan(b->query_start_loc, b->seq_lens, b->num_reqs, b->num_decodes, b->num_tokens,
+                               b->bt_stride, grid_ctas(sms), ws.dec, ws.pre, dev_err, stream));
     if (st != DSA_OK) return st;
   }
   CUtensorMap mk, mq1, mq4;
@@ -165,11 +172,11 @@ int run_logits(const DsaBatch* b, const uint8_t* q_fp8, const float* w_folded, c
   LogitsArgs a{w_folded, k_cache, b->block_table, b->bt_stride, b->num_blocks, logits, ld, dev_err};
   if (b->num_decodes > 0) {
     if ((st = make_q_map(&mq1, q_fp8, b->num_tokens, kHeads)) != DSA_OK) return st;
-    if ((st = from_cuda(launch_logits(1, &mk, &mq1, ws.dec, a, sms, stream))) != DSA_OK) return st;
+    if ((st = from_cuda(launch_logits(1, &mk, &mq1, ws.dec, a, grid_ctas(sms), stream))) != DSA_OK) return st;
   }
   if (b->num_reqs > b->num_decodes) {
     if ((st = make_q_map(&mq4, q_fp8, b->num_tokens, 4 * kHeads)) != DSA_OK) return st;
-    if ((st = from_cuda(launch_logits(4, &mk, &mq4, ws.pre, a, sms, stream))) != DSA_OK) return st;
+    if ((st = from_cuda(launch_logits(4, &mk, &mq4, ws.pre, a, grid_ctas(sms), stream))) != DSA_OK) return st;
   }
   return DSA_OK;
 }
@@ -244,7 +251,7 @@ int dsa_indexer_plan(const DsaBatch* batch, void* ws, size_t ws_bytes, int32_t* 
   int sms;
   if ((st = device_sms(&sms)) != DSA_OK) return st;
   return from_cuda(launch_plan(batch->query_start_loc, batch->seq_lens, batch->num_reqs, batch->num_decodes,
-                               batch->num_tokens, batch->bt_stride, w.dec, w.pre, dev_err, stream));
+                               batch->num_tokens, batch->bt_stride, grid_ctas(sms), w.dec, w.pre, dev_err, stream));
 }
 
 int dsa_indexer_logits(const DsaBatch* batch, const uint8_t* q_fp8, const float* w_folded, const uint8_t* k_cache,

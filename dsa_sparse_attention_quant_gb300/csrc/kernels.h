@@ -23,12 +23,22 @@ struct QBlock {
   int32_t p0;   // position of the first token; token i sees keys [0, p0 + i]
 };
 
+// Slice of the flat (query block, tile) list that one persistent CTA runs.
+struct CtaWork {
+  int32_t it_begin, it_end;  // items [it_begin, it_end)
+  int32_t qb0;               // query block holding it_begin
+  int32_t kt0;               // tile of it_begin within that block
+};
+
+constexpr int kMaxCtas = 1024;
+
 // Work plan of one kernel segment, in device memory.
 struct SegmentPlan {
   QBlock* qb;           // [max_qb]
   int32_t* tile_start;  // [max_qb + 1]: exclusive prefix of 128-key tiles; tile_start[nqb] = total
   int32_t* nqb;         // [1]
   int32_t* req_base;    // [B + 1] scratch
+  CtaWork* cta;         // [kMaxCtas]: each CTA's slice, so a CTA starts with one load
 };
 
 cudaError_t launch_k_quant_write(const void* k, int64_t n, int64_t row_stride, const int64_t* slot_mapping,
@@ -40,7 +50,7 @@ cudaError_t launch_convert(const int32_t* logical, int64_t n_tokens, int topk, c
                            int32_t* valid_counts, int32_t* err, cudaStream_t stream);
 
 cudaError_t launch_plan(const int32_t* qsl, const int32_t* seq_lens, int num_reqs, int num_decodes, int num_tokens,
-                        int64_t bt_stride, SegmentPlan dec, SegmentPlan pre, int32_t* err, cudaStream_t stream);
+                        int64_t bt_stride, int grid, SegmentPlan dec, SegmentPlan pre, int32_t* err, cudaStream_t stream);
 
 struct LogitsArgs {
   const float* w_folded;

@@ -53,7 +53,7 @@ __device__ int block_scan_incl(int v, int* sm, int* total) {
 // Split requests [r_begin, r_end) into query blocks of up to `ntok` tokens and
 // count the 128-key tiles each block needs (keys visible to its last token).
 __device__ void plan_segment(const int32_t* qsl, const int32_t* seq_lens, int r_begin, int r_end, int ntok,
-                             int num_tokens, int64_t bt_stride, SegmentPlan P, int32_t* err, int* sm) {
+                             int num_tokens, int64_t bt_stride, int grid, SegmentPlan P, int32_t* err, int* sm) {
   const int nreq = r_end - r_begin;
   int carry = 0, tot;
   for (int base = 0; base < nreq; base += blockDim.x) {
@@ -80,7 +80,8 @@ __device__ void plan_segment(const int32_t* qsl, const int32_t* seq_lens, int r_
     *P.nqb = nqb;
   }
   __syncthreads();
-  carry = 0;
+  // pass 1: describe every query block, count the tiles of the segment
+  int total = 0;
   for (int base = 0; base < nqb; base += blockDim.x) {
     const int j = base + threadIdx.x;
     int tiles = 0;
@@ -101,25 +102,53 @@ __device__ void plan_segment(const int32_t* qsl, const int32_t* seq_lens, int r_
       P.qb[j] = b;
       tiles = (b.p0 + b.ntok + 127) / 128;
     }
+    block_scan_incl(tiles, sm, &tot);
+    total += tot;
+  }
+  for (int c = threadIdx.x; c < grid; c += blockDim.x) P.cta[c] = CtaWork{0, 0, 0, 0};
+  __syncthreads();
+  // pass 2: tile prefix, and for every CTA the block holding the start of its slice
+  carry = 0;
+  for (int base = 0; base < nqb; base += blockDim.x) {
+    const int j = base + threadIdx.x;
+    int tiles = 0;
+    if (j < nqb) {
+      const QBlock b = P.qb[j];  // written by this thread in pass 1
+      tiles = (b.p0 + b.ntok + 127) / 128;
+    }
     const int incl = block_scan_incl(tiles, sm, &tot);
-    if (j < nqb) P.tile_start[j] = carry + incl - tiles;
+    if (j < nqb) {
+      const int s = carry + incl - tiles;
+      P.tile_start[j] = s;
+      // CTA c starts at floor(total*c/grid): the c with s <= start < s + tiles
+      const int64_t c_lo = (static_cast<int64_t>(s) * grid + total - 1) / total;
+      const int64_t c_hi = (static_cast<int64_t>(s + tiles) * grid + total - 1) / total - 1;
+      for (int64_t c = c_lo; c <= c_hi && c < grid; ++c) {
+        const int b0 = static_cast<int>(static_cast<int64_t>(total) * c / grid);
+        const int b1 = static_cast<int>(static_cast<int64_t>(total) * (c + 1) / grid);
+        P.cta[c] = CtaWork{b0, b1, j, b0 - s};
+      }
+    }
     carry += tot;
   }
   if (threadIdx.x == 0) P.tile_start[nqb] = carry;
 }
 
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* qsl, const int32_t* seq_lens, int num_reqs,
-                                                    int num_decodes, int num_tokens, int64_t bt_stride,
+                                                    int num_decodes, int num_tokens, int64_t bt_stride, int grid,
                                                     SegmentPlan dec, SegmentPlan pre, int32_t* err) {
   __shared__ int sm[33];
-  plan_segment(qsl, seq_lens, 0, num_decodes, 1, num_tokens, bt_stride, dec, err, sm);
+  plan_segment(qsl, seq_lens, 0, num_decodes, 1, num_tokens, bt_stride, grid, dec, err, sm);
   __syncthreads();
-  plan_segment(qsl, seq_lens, num_decodes, num_reqs, 4, num_tokens, bt_stride, pre, err, sm);
+  plan_segment(qsl, seq_lens, num_decodes, num_reqs, 4, num_tokens, bt_stride, grid, pre, err, sm);
 }
 
 cudaError_t launch_plan(const int32_t* qsl, const int32_t* seq_lens, int num_reqs, int num_decodes, int num_tokens,
-                        int64_t bt_stride, SegmentPlan dec, SegmentPlan pre, int32_t* err, cudaStream_t stream) {
-  plan_kernel<<<1, 1024, 0, stream>>>(qsl, seq_lens, num_reqs, num_decodes, num_tokens, bt_stride, dec, pre, err);
+                        int64_t bt_stride, int grid, SegmentPlan dec, SegmentPlan pre, int32_t* err,
+                        cudaStream_t stream) {
+  if (grid < 1 || grid > kMaxCtas) return cudaErrorInvalidValue;
+  plan_kernel<<<1, 1024, 0, stream>>>(qsl, seq_lens, num_reqs, num_decodes, num_tokens, bt_stride, grid, dec, pre,
+                                      err);
   return cudaGetLastError();
 }
 
@@ -176,10 +205,9 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nqb = *plan.nqb;
-  const int total = plan.tile_start[nqb];
-  const int it_begin = static_cast<int>(static_cast<int64_t>(total) * blockIdx.x / gridDim.x);
-  const int it_end = static_cast<int>(static_cast<int64_t>(total) * (blockIdx.x + 1) / gridDim.x);
+  const CtaWork cw = plan.cta[blockIdx.x];  // this CTA's slice, laid out by the plan kernel
+  const int it_begin = cw.it_begin;
+  const int it_end = cw.it_end;
   if (it_begin >= it_end) return;  // uniform over the CTA
 
   if (threadIdx.x == 0) {
@@ -209,23 +237,14 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  // first query block of this CTA's slice: last j with tile_start[j] <= it_begin
-  int j0;
-  {
-    int lo = 0, hi = nqb - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (plan.tile_start[mid] <= it_begin) lo = mid; else hi = mid - 1;
-    }
-    j0 = lo;
-  }
+  const int j0 = cw.qb0;  // first query block of this CTA's slice
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     int j = j0;
     QBlock qb = plan.qb[j];
     int jt_end = plan.tile_start[j + 1];
-    int kt = it_begin - plan.tile_start[j];
+    int kt = cw.kt0;
     int qcount = 0, n = 0, npages = 0, batch = -1;
     int32_t cur_ids = -1, nxt_ids = -1;
     const int32_t* bt_row = nullptr;
@@ -340,7 +359,7 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
     int j = j0;
     QBlock qb = plan.qb[j];
     int jt_end = plan.tile_start[j + 1];
-    int kt = it_begin - plan.tile_start[j];
+    int kt = cw.kt0;
     int qcount = 0, qs = 0, n = 0;
     bool new_qb = true, aborted = false;
     float wr[NTOK == 1 ? kHeads : 1];

@@ -235,7 +235,7 @@ def make_batch(
         perm = np.arange(num_blocks, dtype=np.int64)
     else:
         perm = permutation(seed if table_seed is None else table_seed, STREAM_PERM, num_blocks)
-    bt_stride = max(pages) + bt_pad
+    bt_stride = max(pages, default=1) + bt_pad
     block_table = np.full((B, bt_stride), -1, dtype=np.int32)
     cur = 0
     for r in range(B):
