@@ -36,7 +36,9 @@ SYMBOLS = [
     "dsa_indexer_plan", "dsa_indexer_logits", "dsa_indexer_topk",
     "dsa_topk_logical_to_physical", "dsa_schedule_build",
     "dsa_layer_stack_workspace_size", "dsa_layer_stack_run",
+    "dsa_indexer_logits_topk_static",
 ]
+STATIC_WORKSPACE_BYTES = 32 << 20
 
 
 class DsaError(RuntimeError):
@@ -117,6 +119,7 @@ def load(build_if_missing: bool = True):
             "dsa_layer_stack_workspace_size": (SZ, [BP, I32]),
             "dsa_layer_stack_run": (ctypes.c_int, [ctypes.POINTER(DsaStackPlanC), BP, P, P, P, P, CONSUMER_FN, P, P,
                                                    SZ, P, P]),
+            "dsa_indexer_logits_topk_static": (ctypes.c_int, [BP, P, P, P, I32, P, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -236,6 +239,19 @@ def indexer_logits_topk(batch: Batch, q_fp8, w_folded, k_cache, topk: int, topk_
                                         int(topk), _ptr(topk_out), _ptr(ws), ws.numel(), _ptr(k_new),
                                         _ptr(slot_mapping), _ptr(dev_err), _stream(stream))
     _check(st, "dsa_indexer_logits_topk")
+    return topk_out
+
+
+def indexer_logits_topk_static(batch: Batch, q_fp8, w_folded, k_cache, topk: int, topk_out, k_new=None,
+                               slot_mapping=None, dev_err=None, stream=None):
+    """``indexer_logits_topk`` without any allocation: for callers that cannot
+    allocate device memory. ``topk_out`` must be passed; the scratch is the
+    library's own static device array (DSA_STATIC_WORKSPACE_BYTES), shared by
+    all calls, so calls must not overlap on the GPU."""
+    st = load().dsa_indexer_logits_topk_static(ctypes.byref(batch.c), _ptr(q_fp8), _ptr(w_folded), _ptr(k_cache),
+                                               int(topk), _ptr(topk_out), _ptr(k_new), _ptr(slot_mapping),
+                                               _ptr(dev_err), _stream(stream))
+    _check(st, "dsa_indexer_logits_topk_static")
     return topk_out
 
 

@@ -176,6 +176,33 @@ DSA_API int dsa_indexer_topk(const DsaBatch *batch, const float *logits, int64_t
                      int32_t topk, int32_t *topk_out, void *ws, size_t ws_bytes,
                      dsa_stream_t stream);
 
+/* dsa_indexer_logits_topk for callers that cannot allocate device memory.
+ * The pages have no counterpart: this is a service of this library. Callers
+ * that cannot call cudaMalloc or supply a scratch buffer — code inside a
+ * CUDA-graph capture that someone else owns, plugins that are handed only an
+ * op's input and output tensors, loops that must not touch an allocator — get
+ * the same computation with the scratch taken from a device array of
+ * DSA_STATIC_WORKSPACE_BYTES inside the library. Every GPU that loads the
+ * library holds that array until the process exits. Arguments are those of
+ * dsa_indexer_logits_topk without ws/ws_bytes; the caller still passes all
+ * inputs and outputs. Nothing is allocated: no cudaMalloc, no cudaFree, no
+ * allocating library call.
+ *  - A batch whose dsa_indexer_workspace_size() exceeds
+ *    DSA_STATIC_WORKSPACE_BYTES is rejected with DSA_ENOSPACE before any
+ *    launch (32 MiB holds, e.g., the score rows of 256 decode tokens at 32K
+ *    context).
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - All calls share the array and it keeps the last call's contents (nothing
+ *    in it needs to start at zero). Calls whose kernels overlap on the GPU —
+ *    on two streams, or from two host threads — race on it: serialise them. */
+#define DSA_STATIC_WORKSPACE_BYTES (32u << 20)
+DSA_API int dsa_indexer_logits_topk_static(const DsaBatch *batch, const uint8_t *q_fp8,
+                                   const float *w_folded, uint8_t *k_cache, int32_t topk,
+                                   int32_t *topk_out, const void *k_new,
+                                   const int64_t *slot_mapping, int32_t *dev_err,
+                                   dsa_stream_t stream);
+
 /* ------------------------------------------ S5: logical -> physical ids */
 /* [IG] `SparseMLAIndexGroup._convert_once` (the conversion kernel it calls):
  * physical = block_table[req][id/64] * block_stride_rows + id%64, -1 stays -1;
