@@ -57,6 +57,37 @@ def workload(name: str):
     raise SystemExit(f"unknown workload {name}")
 
 
+def kernel_source_sha() -> str:
+    import hashlib
+
+    csrc = os.path.join(ROOT, "dsa_sparse_attention_quant_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in ("logits.cu", "common.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(summary: str):
+    """DRAM bytes per launch from an ncu summary in profiles/, or None when the
+    summary is missing or was taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", summary)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        line = line.strip().strip("|").strip()
+        if line.startswith("source_sha:"):
+            fields["sha"] = line.split(":", 1)[1].strip()
+        elif line.startswith("dram_bytes_per_launch"):
+            fields["bytes"] = line.split("|")[-1].strip()
+    if fields.get("sha") != kernel_source_sha() or "bytes" not in fields:
+        return None
+    return int(fields["bytes"])
+
+
 def read_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -314,11 +345,7 @@ def run_ours(args):
     kernel_avg_ms = float(np.mean(kernel_ms))
     algo_bytes = pairs * (132 + 4) + T * (64 * 128 + 64 * 4)
     achieved = algo_bytes / (kernel_avg_ms / 1e3) / 1e9
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", f"traffic_{args.workload}.json")
-    if os.path.exists(prof):
-        with open(prof) as f:
-            traffic = json.load(f).get("dram_bytes_per_launch")
+    traffic = profiled_traffic(f"logits_kernel_{args.workload}.md")
     line = {
         "metric": METRIC,
         "value": value,
