@@ -36,7 +36,7 @@ SYMBOLS = [
     "dsa_indexer_plan", "dsa_indexer_logits", "dsa_indexer_topk",
     "dsa_topk_logical_to_physical", "dsa_schedule_build",
     "dsa_layer_stack_workspace_size", "dsa_layer_stack_run",
-    "dsa_indexer_logits_topk_static",
+    "dsa_indexer_logits_topk_static", "dsa_set_launch_events",
 ]
 STATIC_WORKSPACE_BYTES = 32 << 20
 
@@ -49,6 +49,7 @@ class DsaBatchC(ctypes.Structure):
     _fields_ = [
         ("num_reqs", ctypes.c_int32),
         ("num_decodes", ctypes.c_int32),
+        ("num_decode_tokens", ctypes.c_int32),
         ("num_tokens", ctypes.c_int32),
         ("max_seq_len", ctypes.c_int32),
         ("bt_stride", ctypes.c_int64),
@@ -120,6 +121,7 @@ def load(build_if_missing: bool = True):
             "dsa_layer_stack_run": (ctypes.c_int, [ctypes.POINTER(DsaStackPlanC), BP, P, P, P, P, CONSUMER_FN, P, P,
                                                    SZ, P, P]),
             "dsa_indexer_logits_topk_static": (ctypes.c_int, [BP, P, P, P, I32, P, P, P, P, P]),
+            "dsa_set_launch_events": (ctypes.c_int, [P, I32]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -161,7 +163,7 @@ class Batch:
     """Device-side step metadata (the C ``DsaBatch``) plus the tensors it points to."""
 
     def __init__(self, query_start_loc, seq_lens, block_table, req_id_per_token, num_decodes: int,
-                 num_blocks: int, max_seq_len: int | None = None):
+                 num_blocks: int, max_seq_len: int | None = None, num_decode_tokens: int | None = None):
         for t, n in ((query_start_loc, "query_start_loc"), (seq_lens, "seq_lens"), (block_table, "block_table"),
                      (req_id_per_token, "req_id_per_token")):
             _need(t, torch.int32, n)
@@ -176,7 +178,10 @@ class Batch:
         if max_seq_len is None:
             max_seq_len = int(seq_lens.max().item()) if self.num_reqs else 1
         self.max_seq_len = int(max_seq_len)
-        self.c = DsaBatchC(self.num_reqs, self.num_decodes, self.num_tokens, self.max_seq_len,
+        if num_decode_tokens is None:
+            num_decode_tokens = int(query_start_loc[self.num_decodes].item()) if self.num_reqs else 0
+        self.num_decode_tokens = int(num_decode_tokens)
+        self.c = DsaBatchC(self.num_reqs, self.num_decodes, self.num_decode_tokens, self.num_tokens, self.max_seq_len,
                            int(block_table.shape[1]) if block_table.dim() == 2 else 1, self.num_blocks,
                            query_start_loc.data_ptr(), seq_lens.data_ptr(), block_table.data_ptr(),
                            req_id_per_token.data_ptr())
@@ -187,7 +192,8 @@ class Batch:
         def d(a):
             return torch.from_numpy(a.astype("int32")).to(device)
         return cls(d(hb.query_start_loc), d(hb.seq_lens), d(hb.block_table), d(hb.req_id_per_token),
-                   hb.num_decodes, hb.num_blocks, int(hb.seq_lens.max()) if hb.num_reqs else 1)
+                   hb.num_decodes, hb.num_blocks, int(hb.seq_lens.max()) if hb.num_reqs else 1,
+                   int(hb.query_start_loc[hb.num_decodes]) if hb.num_reqs else 0)
 
 
 # ---------------------------------------------------------------- entry points
@@ -195,9 +201,11 @@ class Batch:
 def indexer_k_quant_write(k, slot_mapping, k_cache, dev_err=None, stream=None):
     _need(slot_mapping, torch.int64, "slot_mapping")
     _need(k_cache, torch.uint8, "k_cache")
+    n = int(slot_mapping.shape[0])
+    if n == 0:
+        return
     if k.dtype != torch.bfloat16 or not k.is_cuda or k.stride(-1) != 1:
         raise DsaError("k must be a CUDA bf16 tensor with unit inner stride")
-    n = int(slot_mapping.shape[0])
     row_stride = int(k.stride(0)) if k.dim() == 2 else HEAD_DIM
     st = load().dsa_indexer_k_quant_write(_ptr(k), n, row_stride, _ptr(slot_mapping), _ptr(k_cache),
                                           int(k_cache.shape[0]), _ptr(dev_err), _stream(stream))
@@ -312,6 +320,15 @@ def schedule_build(n_layers: int, use_index_cache: bool = True, freq: int = 1, o
                                    None if pattern is None else pattern.encode(), fs, prod)
     _check(st, "dsa_schedule_build")
     return fs.raw[:n_layers].decode(), list(prod[:n_layers])
+
+
+def set_launch_events(events=()) -> None:
+    """Launch timeline: the following fused calls on this thread record these
+    torch.cuda.Event objects, one before the first kernel and one after every
+    kernel (an empty sequence switches it off)."""
+    handles = (ctypes.c_void_p * max(len(events), 1))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    st = load().dsa_set_launch_events(handles, len(events))
+    _check(st, "dsa_set_launch_events")
 
 
 def check_device_error(dev_err, stream=None) -> int:

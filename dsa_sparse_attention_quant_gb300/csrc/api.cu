@@ -102,6 +102,7 @@ int check_batch(const DsaBatch* b) {
   if (b == nullptr) return DSA_EINVAL;
   if (b->num_reqs < 0 || b->num_decodes < 0 || b->num_decodes > b->num_reqs || b->num_tokens < 0)
     return DSA_EINVAL;
+  if (b->num_decode_tokens < 0 || b->num_decode_tokens > b->num_tokens) return DSA_EINVAL;
   if (b->num_tokens > 0 && (b->num_reqs == 0 || b->max_seq_len < 1)) return DSA_EINVAL;
   if (b->num_reqs > 0 &&
       (b->query_start_loc == nullptr || b->seq_lens == nullptr || b->block_table == nullptr ||
@@ -119,10 +120,15 @@ int64_t logits_ld(const DsaBatch* b) {
 // Persistent logits grid: one CTA per SM. The plan and the launch must agree on it.
 int grid_ctas(int sms) { return sms < kMaxCtas ? sms : kMaxCtas; }
 
-// Workspace carving of the indexer: both segment plans, then the score matrix.
+// Workspace of the indexer: both segment plans, the score matrix, and for the
+// decode rows the score histograms, top-k counters and boundary candidates.
 struct IndexerWs {
   SegmentPlan dec, pre;
   float* logits;
+  uint32_t* hist;
+  uint32_t* counters;
+  uint2* cand;
+  int hist_rows;
   size_t bytes;
 };
 
@@ -137,7 +143,9 @@ IndexerWs carve(const DsaBatch* b, void* base) {
   };
   const size_t T = static_cast<size_t>(b->num_tokens);
   const size_t B = static_cast<size_t>(b->num_reqs);
-  const size_t max_dec = T + 1;
+  const size_t Td = static_cast<size_t>(b->num_decode_tokens);
+  const size_t ld = static_cast<size_t>(logits_ld(b));
+  const size_t max_dec = Td + 1;
   const size_t max_pre = T / 4 + B + 1;
   w.dec.qb = static_cast<QBlock*>(take(max_dec * sizeof(QBlock)));
   w.dec.tile_start = static_cast<int32_t*>(take((max_dec + 1) * 4));
@@ -149,36 +157,102 @@ IndexerWs carve(const DsaBatch* b, void* base) {
   w.pre.nqb = static_cast<int32_t*>(take(4));
   w.pre.req_base = static_cast<int32_t*>(take((B + 1) * 4));
   w.pre.cta = static_cast<CtaWork*>(take(kMaxCtas * sizeof(CtaWork)));
-  w.logits = static_cast<float*>(take(T * static_cast<size_t>(logits_ld(b)) * 4));
+  w.dec.max_qb = static_cast<int32_t>(max_dec);
+  w.pre.max_qb = static_cast<int32_t>(max_pre);
+  w.logits = static_cast<float*>(take(T * ld * 4));
+  w.hist = static_cast<uint32_t*>(take(Td * kHistBins * 4));
+  w.counters = static_cast<uint32_t*>(take(Td * kRowCounters * 4));
+  w.cand = static_cast<uint2*>(take(Td * ld * sizeof(uint2)));
+  w.hist_rows = static_cast<int>(Td);
   w.bytes = off;
   return w;
 }
 
-// Plan + logits for both segments (no top-k).
+PlanArgs plan_args(const DsaBatch* b, const IndexerWs& ws, int sms, int32_t* dev_err) {
+  return PlanArgs{b->query_start_loc, b->seq_lens,    b->num_reqs, b->num_decodes, b->num_decode_tokens,
+                  b->num_tokens,      b->bt_stride,   grid_ctas(sms), ws.dec,     ws.pre,
+                  dev_err};
+}
+
+// Prologue with no q: (optional) K quant + cache write, plan, and zeroed
+// decode-row histograms and counters.
+PrologueArgs plan_only(const DsaBatch* b, const IndexerWs& ws, int sms, const void* k_new,
+                       const int64_t* slot_mapping, uint8_t* k_cache, int32_t* dev_err) {
+  PrologueArgs pa{};
+  pa.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  pa.slot_mapping = slot_mapping;
+  pa.k_cache = k_cache;
+  pa.num_blocks = b->num_blocks;
+  pa.n_tokens = b->num_tokens;
+  pa.plan = true;
+  pa.p = plan_args(b, ws, sms, dev_err);
+  pa.hist = ws.hist;
+  pa.counters = ws.counters;
+  pa.hist_rows = ws.hist_rows;
+  pa.err = dev_err;
+  return pa;
+}
+
+// Launch timeline set by dsa_set_launch_events for this host thread: one
+// event before the first kernel of each call and one after every kernel.
+constexpr int kMaxTimeline = 32;
+thread_local cudaEvent_t t_events[kMaxTimeline];
+thread_local int t_count = 0;
+thread_local int t_next = 0;
+
+int mark(cudaStream_t stream) {
+  if (t_next >= t_count) return DSA_OK;
+  return from_cuda(cudaEventRecordWithFlags(t_events[t_next++], stream, cudaEventRecordExternal));
+}
+
+// Status of a kernel launch, followed by the timeline mark after it.
+int launched(cudaError_t e, cudaStream_t stream) {
+  const int st = from_cuda(e);
+  return st != DSA_OK ? st : mark(stream);
+}
+
+// Scores for both segments (the plan is already in ws). With `hist`, the
+// decode kernel also accumulates the decode rows' histograms (zeroed before).
 int run_logits(const DsaBatch* b, const uint8_t* q_fp8, const float* w_folded, const uint8_t* k_cache,
-               float* logits, int64_t ld, const IndexerWs& ws, int32_t* dev_err, cudaStream_t stream,
-               bool run_plan) {
+               float* logits, int64_t ld, const IndexerWs& ws, bool hist, int32_t* dev_err, cudaStream_t stream) {
   if (b->num_tokens == 0) return DSA_OK;
   int sms = 0;
   int st = device_sms(&sms);
   if (st != DSA_OK) return st;
-  if (run_plan) {
-    st = from_cuda(launch_plan(b->query_start_loc, b->seq_lens, b->num_reqs, b->num_decodes, b->num_tokens,
-                               b->bt_stride, grid_ctas(sms), ws.dec, ws.pre, dev_err, stream));
-    if (st != DSA_OK) return st;
-  }
   CUtensorMap mk, mq1, mq4;
   if ((st = make_kcache_map(&mk, k_cache, b->num_blocks)) != DSA_OK) return st;
-  LogitsArgs a{w_folded, k_cache, b->block_table, b->bt_stride, b->num_blocks, logits, ld, dev_err};
+  LogitsArgs a{w_folded, k_cache, b->block_table, b->bt_stride, b->num_blocks, logits, ld,
+               hist ? ws.hist : nullptr, hist ? ws.hist_rows : 0, dev_err};
   if (b->num_decodes > 0) {
     if ((st = make_q_map(&mq1, q_fp8, b->num_tokens, kHeads)) != DSA_OK) return st;
-    if ((st = from_cuda(launch_logits(1, &mk, &mq1, ws.dec, a, grid_ctas(sms), stream))) != DSA_OK) return st;
+    if ((st = launched(launch_logits(1, &mk, &mq1, ws.dec, a, grid_ctas(sms), stream), stream)) != DSA_OK) return st;
   }
   if (b->num_reqs > b->num_decodes) {
     if ((st = make_q_map(&mq4, q_fp8, b->num_tokens, 4 * kHeads)) != DSA_OK) return st;
-    if ((st = from_cuda(launch_logits(4, &mk, &mq4, ws.pre, a, grid_ctas(sms), stream))) != DSA_OK) return st;
+    if ((st = launched(launch_logits(4, &mk, &mq4, ws.pre, a, grid_ctas(sms), stream), stream)) != DSA_OK) return st;
   }
   return DSA_OK;
+}
+
+// Top-k of every row from scores built with the decode rows' histograms.
+// Rows that fit in shared memory: one CTA per row, one launch for all rows.
+// Longer rows: the multi-CTA select for the decode rows, one CTA per row for
+// the others.
+int run_topk(const DsaBatch* b, const IndexerWs& ws, int64_t ld, int32_t topk, int32_t* out, const TopkPhys* phys,
+             cudaStream_t stream) {
+  if (ld <= kTopkRowCap)
+    return launched(launch_topk(ws.logits, ld, b->query_start_loc, b->seq_lens, b->req_id_per_token, b->num_reqs, 0,
+                                b->num_tokens, topk, out, phys, ws.hist, ws.hist_rows, stream),
+                    stream);
+  SelectArgs sa{ws.logits, ld, b->query_start_loc, b->seq_lens, b->req_id_per_token, b->num_reqs,
+                ws.hist_rows, topk, out, ws.hist, ws.counters, ws.cand};
+  int st = DSA_OK;
+  if (ws.hist_rows > 0 && (st = launched(launch_select(sa, phys, stream), stream)) != DSA_OK) return st;
+  if (b->num_tokens > ws.hist_rows)
+    st = launched(launch_topk(ws.logits, ld, b->query_start_loc, b->seq_lens, b->req_id_per_token, b->num_reqs,
+                              ws.hist_rows, b->num_tokens, topk, out, phys, nullptr, 0, stream),
+                  stream);
+  return st;
 }
 
 bool topk_ok(int32_t topk) { return topk >= 4 && topk <= 4096 && topk % 4 == 0; }
@@ -250,10 +324,18 @@ int dsa_indexer_plan(const DsaBatch* batch, void* ws, size_t ws_bytes, int32_t* 
   if (ws_bytes < w.bytes) return DSA_ENOSPACE;
   int sms;
   if ((st = device_sms(&sms)) != DSA_OK) return st;
-  return from_cuda(launch_plan(batch->query_start_loc, batch->seq_lens, batch->num_reqs, batch->num_decodes,
-                               batch->num_tokens, batch->bt_stride, grid_ctas(sms), w.dec, w.pre, dev_err, stream));
+  return from_cuda(launch_prologue(plan_only(batch, w, sms, nullptr, nullptr, nullptr, dev_err), stream));
 }
 
+int dsa_set_launch_events(void* const* events, int32_t n_events) {
+  if (n_events < 0 || n_events > kMaxTimeline || (n_events > 0 && events == nullptr)) return DSA_EINVAL;
+  for (int32_t i = 0; i < n_events; ++i)
+    if (events[i] == nullptr) return DSA_EINVAL;
+  for (int32_t i = 0; i < n_events; ++i) t_events[i] = static_cast<cudaEvent_t>(events[i]);
+  t_count = n_events;
+  t_next = 0;
+  return DSA_OK;
+}
 int dsa_indexer_logits(const DsaBatch* batch, const uint8_t* q_fp8, const float* w_folded, const uint8_t* k_cache,
                        float* logits, int64_t logits_ld, void* ws, size_t ws_bytes, int32_t* dev_err,
                        dsa_stream_t stream) {
@@ -264,7 +346,7 @@ int dsa_indexer_logits(const DsaBatch* batch, const uint8_t* q_fp8, const float*
   if (!aligned16(q_fp8) || !aligned16(w_folded) || !aligned16(k_cache) || !aligned16(ws)) return DSA_EINVAL;
   IndexerWs w = carve(batch, ws);
   if (ws_bytes < w.bytes) return DSA_ENOSPACE;
-  return run_logits(batch, q_fp8, w_folded, k_cache, logits, logits_ld, w, dev_err, stream, false);
+  return run_logits(batch, q_fp8, w_folded, k_cache, logits, logits_ld, w, false, dev_err, stream);
 }
 
 int dsa_indexer_topk(const DsaBatch* batch, const float* logits, int64_t logits_ld, int32_t topk, int32_t* topk_out,
@@ -279,8 +361,8 @@ int dsa_indexer_topk(const DsaBatch* batch, const float* logits, int64_t logits_
   int sms;
   if ((st = device_sms(&sms)) != DSA_OK) return st;
   return from_cuda(launch_topk(logits, logits_ld, batch->query_start_loc, batch->seq_lens,
-                               batch->req_id_per_token, batch->num_reqs, batch->num_tokens, topk, topk_out, nullptr,
-                               stream));
+                               batch->req_id_per_token, batch->num_reqs, 0, batch->num_tokens, topk, topk_out,
+                               nullptr, nullptr, 0, stream));
 }
 
 int dsa_indexer_logits_topk(const DsaBatch* batch, const uint8_t* q_fp8, const float* w_folded, uint8_t* k_cache,
@@ -296,17 +378,17 @@ int dsa_indexer_logits_topk(const DsaBatch* batch, const uint8_t* q_fp8, const f
     return DSA_EINVAL;
   IndexerWs w = carve(batch, ws);
   if (ws_bytes < w.bytes) return DSA_ENOSPACE;
-  if (k_new != nullptr) {
-    if (!aligned16(k_new)) return DSA_EINVAL;
-    st = dsa_indexer_k_quant_write(k_new, batch->num_tokens, kDim, slot_mapping, k_cache, batch->num_blocks,
-                                   dev_err, stream);
-    if (st != DSA_OK) return st;
-  }
-  const int64_t ld = logits_ld(batch);
-  st = run_logits(batch, q_fp8, w_folded, k_cache, w.logits, ld, w, dev_err, stream, true);
+  if (k_new != nullptr && !aligned16(k_new)) return DSA_EINVAL;
+  int sms;
+  if ((st = device_sms(&sms)) != DSA_OK) return st;
+  // one launch: this step's K into the cache (if given), the plan, zeroed histograms
+  if ((st = mark(stream)) != DSA_OK) return st;
+  st = launched(launch_prologue(plan_only(batch, w, sms, k_new, slot_mapping, k_cache, dev_err), stream), stream);
   if (st != DSA_OK) return st;
-  return from_cuda(launch_topk(w.logits, ld, batch->query_start_loc, batch->seq_lens, batch->req_id_per_token,
-                               batch->num_reqs, batch->num_tokens, topk, topk_out, nullptr, stream));
+  const int64_t ld = logits_ld(batch);
+  st = run_logits(batch, q_fp8, w_folded, k_cache, w.logits, ld, w, true, dev_err, stream);
+  if (st != DSA_OK) return st;
+  return run_topk(batch, w, ld, topk, topk_out, nullptr, stream);
 }
 
 int dsa_topk_logical_to_physical(const int32_t* logical, int64_t n_tokens, int32_t topk,
@@ -392,6 +474,9 @@ int dsa_layer_stack_run(const DsaStackPlan* plan, const DsaBatch* batch, const i
   void* iws = reinterpret_cast<uint8_t*>(wf) + align_up(T * kHeads * 4, 256);
   IndexerWs w = carve(batch, iws);
   const int64_t ld = logits_ld(batch);
+  int sms = 0;
+  if (batch->num_tokens > 0 && (st = device_sms(&sms)) != DSA_OK) return st;
+  const float softmax_scale = plan->softmax_scale > 0.0f ? plan->softmax_scale : 0.08838834764831845f;
   bool planned = false;
   int32_t producer = 0;
   for (int32_t l = 0; l < plan->n_layers; ++l) {
@@ -399,22 +484,26 @@ int dsa_layer_stack_run(const DsaStackPlan* plan, const DsaBatch* batch, const i
       producer = l;
       if (batch->num_tokens > 0) {
         const DsaLayerInputs& L = plan->layers[l];
-        if (L.k_new != nullptr) {
-          st = dsa_indexer_k_quant_write(L.k_new, batch->num_tokens, kDim, slot_mapping, L.k_cache,
-                                         batch->num_blocks, dev_err, stream);
-          if (st != DSA_OK) return st;
-        }
-        st = dsa_indexer_q_quant_fold(L.q, L.w, batch->num_tokens, plan->softmax_scale, q8, nullptr, wf, stream);
-        if (st != DSA_OK) return st;
-        // the batch layout is the same for every layer of the step: plan once
-        st = run_logits(batch, q8, wf, L.k_cache, w.logits, ld, w, dev_err, stream, !planned);
+        // one launch: this layer's K into its cache, q quant + weight fold, and
+        // (first F layer only: the batch layout is the same for every layer) the plan
+        // (histograms and counters of the decode rows zeroed for this layer's top-k)
+        PrologueArgs pa = plan_only(batch, w, sms, L.k_new, slot_mapping, L.k_cache, dev_err);
+        pa.q = static_cast<const __nv_bfloat16*>(L.q);
+        pa.w = L.w;
+        pa.softmax_scale = softmax_scale;
+        pa.q_fp8 = q8;
+        pa.w_folded = wf;
+        pa.plan = !planned;
+        if ((st = mark(stream)) != DSA_OK) return st;
+        st = launched(launch_prologue(pa, stream), stream);
         if (st != DSA_OK) return st;
         planned = true;
+        st = run_logits(batch, q8, wf, L.k_cache, w.logits, ld, w, true, dev_err, stream);
+        if (st != DSA_OK) return st;
         // S3 with S5 fused into its output pass: logical ids, physical ids, valid counts
         TopkPhys tp{batch->block_table, batch->bt_stride,
                     plan->block_stride_rows > 0 ? plan->block_stride_rows : kBlock, phys_buf, valid_buf, dev_err};
-        st = from_cuda(launch_topk(w.logits, ld, batch->query_start_loc, batch->seq_lens, batch->req_id_per_token,
-                                   batch->num_reqs, batch->num_tokens, plan->topk, topk_buf, &tp, stream));
+        st = run_topk(batch, w, ld, plan->topk, topk_buf, &tp, stream);
         if (st != DSA_OK) return st;
       }
     }

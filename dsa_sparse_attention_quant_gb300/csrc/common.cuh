@@ -18,6 +18,33 @@ namespace dsa {
 // flags DSA_DEVERR_TIMEOUT and unwinds.
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
+// Programmatic dependent launch: wait until the previous kernel of the stream
+// has completed and its memory is visible (a no-op when the launch did not
+// opt in), and let the next kernel of the stream start its own set-up.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch `kernel` so that it may start while the previous kernel of the
+// stream is still running; the kernel calls pdl_wait() before it reads that
+// kernel's results. Stream capture keeps the relation as a programmatic edge.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 __device__ __forceinline__ void flag_error(int32_t* err, uint32_t bit) {
   if (err != nullptr) atomicOr(reinterpret_cast<unsigned int*>(err), bit);
 }

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -39,6 +40,7 @@ struct SegmentPlan {
   int32_t* nqb;         // [1]
   int32_t* req_base;    // [B + 1] scratch
   CtaWork* cta;         // [kMaxCtas]: each CTA's slice, so a CTA starts with one load
+  int32_t max_qb;       // capacity of qb / tile_start
 };
 
 cudaError_t launch_k_quant_write(const void* k, int64_t n, int64_t row_stride, const int64_t* slot_mapping,
@@ -49,8 +51,44 @@ cudaError_t launch_convert(const int32_t* logical, int64_t n_tokens, int topk, c
                            const int32_t* block_table, int64_t bt_stride, int stride_rows, int32_t* physical,
                            int32_t* valid_counts, int32_t* err, cudaStream_t stream);
 
-cudaError_t launch_plan(const int32_t* qsl, const int32_t* seq_lens, int num_reqs, int num_decodes, int num_tokens,
-                        int64_t bt_stride, int grid, SegmentPlan dec, SegmentPlan pre, int32_t* err, cudaStream_t stream);
+struct PlanArgs {
+  const int32_t* qsl;
+  const int32_t* seq_lens;
+  int num_reqs, num_decodes, num_decode_tokens, num_tokens;
+  int64_t bt_stride;
+  int grid;  // CTAs of the score kernels
+  SegmentPlan dec, pre;
+  int32_t* err;
+};
+
+
+// Fused per-layer prologue: K quant + cache write of the step's tokens, q quant
+// with the weight fold, and (when `plan`) the work plan.
+struct PrologueArgs {
+  const __nv_bfloat16* q;   // [T, 64, 128]
+  const float* w;           // [T, 64]
+  float softmax_scale;
+  uint8_t* q_fp8;           // [T, 64, 128]
+  float* w_folded;          // [T, 64]
+  const __nv_bfloat16* k_new;     // [T, 128] or nullptr
+  const int64_t* slot_mapping;    // [T]
+  uint8_t* k_cache;
+  int64_t num_blocks;
+  int n_tokens;
+  bool plan;
+  PlanArgs p;
+  uint32_t* hist;      // zeroed here for the score kernel: [hist_rows][kHistBins]
+  uint32_t* counters;  // [hist_rows][kRowCounters]
+  int hist_rows;
+  int32_t* err;
+};
+
+cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t stream);
+
+// Histogram bins of a decode row's scores: the top 11 bits of the
+// order-preserving 32-bit key (sign, exponent, 2 mantissa bits).
+constexpr int kHistBins = 2048;
+constexpr int kHistShift = 21;
 
 struct LogitsArgs {
   const float* w_folded;
@@ -60,7 +98,27 @@ struct LogitsArgs {
   int64_t num_blocks;
   float* logits;
   int64_t ld;
+  uint32_t* hist;  // [hist_rows][kHistBins] or nullptr: decode rows' score histograms (zeroed before)
+  int hist_rows;
   int32_t* err;
+};
+
+// Per decode row: out count, candidate count, finished chunks, spare.
+constexpr int kRowCounters = 4;
+
+struct SelectArgs {
+  const float* logits;
+  int64_t ld;
+  const int32_t* qsl;
+  const int32_t* seq_lens;
+  const int32_t* req_id;
+  int num_reqs;
+  int n_rows;               // decode rows [0, n_rows)
+  int topk;
+  int32_t* out;             // [T, topk]
+  const uint32_t* hist;     // [n_rows][kHistBins]
+  uint32_t* counters;       // [n_rows][kRowCounters], zeroed before
+  uint2* cand;              // [n_rows][ld]: (key, id) of the boundary bin
 };
 
 // ntok_per_block = 1 (decode segment) or 4 (prefill segment).
@@ -77,8 +135,17 @@ struct TopkPhys {
   int32_t* err;
 };
 
+// Rows up to this many scores are staged in shared memory by the per-row top-k.
+constexpr int kTopkRowCap = 12288;
+
+// Rows [row_begin, n_tokens): one CTA per row. Rows t < hist_rows take their
+// first radix round from hist (the score kernel's histograms; may be nullptr).
 cudaError_t launch_topk(const float* logits, int64_t ld, const int32_t* qsl, const int32_t* seq_lens,
-                        const int32_t* req_id, int num_reqs, int n_tokens, int topk, int32_t* out,
-                        const TopkPhys* phys, cudaStream_t stream);
+                        const int32_t* req_id, int num_reqs, int row_begin, int n_tokens, int topk, int32_t* out,
+                        const TopkPhys* phys, const uint32_t* hist, int hist_rows, cudaStream_t stream);
+
+// Decode rows [0, a.n_rows) whose score histograms the score kernel built:
+// several CTAs per row, the last one of a row resolves the boundary bin.
+cudaError_t launch_select(const SelectArgs& a, const TopkPhys* phys, cudaStream_t stream);
 
 }  // namespace dsa

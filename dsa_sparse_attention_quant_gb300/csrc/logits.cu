@@ -24,141 +24,13 @@
 
 namespace dsa {
 
-// ------------------------------------------------------------------ planning
-__device__ int block_scan_incl(int v, int* sm, int* total) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int n = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += n;
-  }
-  if (lane == 31) sm[wid] = v;
-  __syncthreads();
-  if (wid == 0) {
-    int x = lane < nw ? sm[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int n = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += n;
-    }
-    if (lane < nw) sm[lane] = x;
-  }
-  __syncthreads();
-  const int res = v + (wid > 0 ? sm[wid - 1] : 0);
-  *total = sm[nw - 1];
-  __syncthreads();
-  return res;
-}
-
-// Split requests [r_begin, r_end) into query blocks of up to `ntok` tokens and
-// count the 128-key tiles each block needs (keys visible to its last token).
-__device__ void plan_segment(const int32_t* qsl, const int32_t* seq_lens, int r_begin, int r_end, int ntok,
-                             int num_tokens, int64_t bt_stride, int grid, SegmentPlan P, int32_t* err, int* sm) {
-  const int nreq = r_end - r_begin;
-  int carry = 0, tot;
-  for (int base = 0; base < nreq; base += blockDim.x) {
-    const int r = base + threadIdx.x;
-    int c = 0;
-    if (r < nreq) {
-      const int rr = r_begin + r;
-      const int ql = qsl[rr + 1] - qsl[rr];
-      const int sl = seq_lens[rr];
-      if (ql < 0 || sl < ql || static_cast<int64_t>(sl) > bt_stride * kBlock || qsl[rr] < 0 ||
-          qsl[rr + 1] > num_tokens) {
-        flag_error(err, DSA_DEVERR_SEQ_RANGE);
-      } else {
-        c = (ql + ntok - 1) / ntok;
-      }
-    }
-    const int incl = block_scan_incl(c, sm, &tot);
-    if (r < nreq) P.req_base[r] = carry + incl - c;
-    carry += tot;
-  }
-  const int nqb = carry;
-  if (threadIdx.x == 0) {
-    P.req_base[nreq] = nqb;
-    *P.nqb = nqb;
-  }
-  __syncthreads();
-  // pass 1: describe every query block, count the tiles of the segment
-  int total = 0;
-  for (int base = 0; base < nqb; base += blockDim.x) {
-    const int j = base + threadIdx.x;
-    int tiles = 0;
-    if (j < nqb) {
-      int lo = 0, hi = nreq - 1;  // last r with req_base[r] <= j
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (P.req_base[mid] <= j) lo = mid; else hi = mid - 1;
-      }
-      const int rr = r_begin + lo;
-      const int jj = j - P.req_base[lo];
-      const int q0 = qsl[rr], ql = qsl[rr + 1] - q0, sl = seq_lens[rr];
-      QBlock b;
-      b.req = rr;
-      b.t0 = q0 + jj * ntok;
-      b.ntok = min(ntok, ql - jj * ntok);
-      b.p0 = sl - ql + jj * ntok;
-      P.qb[j] = b;
-      tiles = (b.p0 + b.ntok + 127) / 128;
-    }
-    block_scan_incl(tiles, sm, &tot);
-    total += tot;
-  }
-  for (int c = threadIdx.x; c < grid; c += blockDim.x) P.cta[c] = CtaWork{0, 0, 0, 0};
-  __syncthreads();
-  // pass 2: tile prefix, and for every CTA the block holding the start of its slice
-  carry = 0;
-  for (int base = 0; base < nqb; base += blockDim.x) {
-    const int j = base + threadIdx.x;
-    int tiles = 0;
-    if (j < nqb) {
-      const QBlock b = P.qb[j];  // written by this thread in pass 1
-      tiles = (b.p0 + b.ntok + 127) / 128;
-    }
-    const int incl = block_scan_incl(tiles, sm, &tot);
-    if (j < nqb) {
-      const int s = carry + incl - tiles;
-      P.tile_start[j] = s;
-      // CTA c starts at floor(total*c/grid): the c with s <= start < s + tiles
-      const int64_t c_lo = (static_cast<int64_t>(s) * grid + total - 1) / total;
-      const int64_t c_hi = (static_cast<int64_t>(s + tiles) * grid + total - 1) / total - 1;
-      for (int64_t c = c_lo; c <= c_hi && c < grid; ++c) {
-        const int b0 = static_cast<int>(static_cast<int64_t>(total) * c / grid);
-        const int b1 = static_cast<int>(static_cast<int64_t>(total) * (c + 1) / grid);
-        P.cta[c] = CtaWork{b0, b1, j, b0 - s};
-      }
-    }
-    carry += tot;
-  }
-  if (threadIdx.x == 0) P.tile_start[nqb] = carry;
-}
-
-__global__ void __launch_bounds__(1024) plan_kernel(const int32_t* qsl, const int32_t* seq_lens, int num_reqs,
-                                                    int num_decodes, int num_tokens, int64_t bt_stride, int grid,
-                                                    SegmentPlan dec, SegmentPlan pre, int32_t* err) {
-  __shared__ int sm[33];
-  plan_segment(qsl, seq_lens, 0, num_decodes, 1, num_tokens, bt_stride, grid, dec, err, sm);
-  __syncthreads();
-  plan_segment(qsl, seq_lens, num_decodes, num_reqs, 4, num_tokens, bt_stride, grid, pre, err, sm);
-}
-
-cudaError_t launch_plan(const int32_t* qsl, const int32_t* seq_lens, int num_reqs, int num_decodes, int num_tokens,
-                        int64_t bt_stride, int grid, SegmentPlan dec, SegmentPlan pre, int32_t* err,
-                        cudaStream_t stream) {
-  if (grid < 1 || grid > kMaxCtas) return cudaErrorInvalidValue;
-  plan_kernel<<<1, 1024, 0, stream>>>(qsl, seq_lens, num_reqs, num_decodes, num_tokens, bt_stride, grid, dec, pre,
-                                      err);
-  return cudaGetLastError();
-}
-
 // ------------------------------------------------------------------ logits
 template <int NTOK>
 struct LogitsCfg {
   static constexpr int N = 64 * NTOK;                     // MMA N: heads x tokens
   static constexpr int kStages = NTOK == 1 ? 8 : 6;       // K-tile ring
   static constexpr int kAcc = NTOK == 1 ? 4 : 2;          // TMEM accumulator ring
-  static constexpr int kEpiWG = NTOK == 1 ? 1 : 2;        // epilogue warpgroups (take tiles in turn)
+  static constexpr int kEpiWG = 2;                        // epilogue warpgroups (take tiles in turn)
   static constexpr int kEpiWarps = 4 * kEpiWG;
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr uint32_t kTmemCols = N * kAcc;         // 256 or 512
@@ -171,7 +43,10 @@ struct LogitsCfg {
   static constexpr int kOffBar = kOffW + 2 * kWBytes;
   static constexpr int kNumBars = 2 * kStages + 4 + 2 * kAcc + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
+  // decode: one score histogram per epilogue warp (first radix round of the top-k)
+  static constexpr int kHistBytes = NTOK == 1 ? kEpiWarps * kHistBins * 4 : 0;
+  static constexpr int kOffHist = (kOffMisc + 16 + 127) / 128 * 128;
+  static constexpr int kSmemBytes = kOffHist + kHistBytes + 1024;  // + slack to align the base to 1024
   static constexpr uint32_t kIdesc = f8_idesc(128, N);
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation must be a power of two");
@@ -205,10 +80,6 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const CtaWork cw = plan.cta[blockIdx.x];  // this CTA's slice, laid out by the plan kernel
-  const int it_begin = cw.it_begin;
-  const int it_end = cw.it_end;
-  if (it_begin >= it_end) return;  // uniform over the CTA
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -237,6 +108,13 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  // Everything above may overlap the previous kernel of the stream (programmatic
+  // dependent launch); the plan, q codes, weights and K cache are read below.
+  pdl_wait();
+  pdl_launch_dependents();
+  const CtaWork cw = plan.cta[blockIdx.x];  // this CTA's slice, laid out by the plan kernel
+  const int it_begin = cw.it_begin;         // an empty slice runs no loop iteration below
+  const int it_end = cw.it_end;
   const int j0 = cw.qb0;  // first query block of this CTA's slice
 
   if (warp == 0) {
@@ -363,10 +241,25 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
     int qcount = 0, qs = 0, n = 0;
     bool new_qb = true, aborted = false;
     float wr[NTOK == 1 ? kHeads : 1];
+    // decode rows: this warp's histogram of the keys of its stored scores,
+    // added to the row's global histogram when the warp leaves the row
+    uint32_t* whist = reinterpret_cast<uint32_t*>(smem + C::kOffHist) + (warp - 2) * kHistBins;
+    bool use_hist = false;
+    auto flush_hist = [&](int row_t) {
+      __syncwarp();
+      uint32_t* dst = a.hist + static_cast<int64_t>(row_t) * kHistBins;
+      for (int b = lane; b < kHistBins; b += 32) {
+        const uint32_t v = whist[b];
+        if (v != 0) atomicAdd(dst + b, v);
+      }
+    };
     for (int it = it_begin; it < it_end; ++it, ++n, ++kt) {
       if (it == jt_end) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&qempty[qs]);  // done with this q/w' buffer
+        if constexpr (NTOK == 1) {
+          if (use_hist) flush_hist(qb.t0);
+        }
         ++j;
         qb = plan.qb[j];
         jt_end = plan.tile_start[j + 1];
@@ -390,6 +283,12 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
             wr[4 * h + 1] = v.y;
             wr[4 * h + 2] = v.z;
             wr[4 * h + 3] = v.w;
+          }
+          use_hist = a.hist != nullptr && qb.t0 < a.hist_rows;
+          if (use_hist) {
+            uint4* z = reinterpret_cast<uint4*>(whist);
+            for (int b = lane; b < kHistBins / 4; b += 32) z[b] = make_uint4(0, 0, 0, 0);
+            __syncwarp();
           }
         }
       }
@@ -429,7 +328,13 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
               s1 = fmaf(wt[half * 32 + h + 1], fmaxf(v[h + 1], 0.f), s1);
             }
           }
-          if (key <= qb.p0 + tok && key < a.ld) a.logits[static_cast<int64_t>(qb.t0 + tok) * a.ld + key] = (s0 + s1) * kscale;
+          if (key <= qb.p0 + tok && key < a.ld) {
+            const float score = (s0 + s1) * kscale;
+            a.logits[static_cast<int64_t>(qb.t0 + tok) * a.ld + key] = score;
+            if constexpr (NTOK == 1) {
+              if (use_hist) atomicAdd(&whist[f32_key(score) >> kHistShift], 1u);
+            }
+          }
         }
       }
       tc_fence_before();
@@ -437,7 +342,12 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
       if (lane == 0) mbar_arrive(&tempty[acc]);
     }
     __syncwarp();
-    if (!aborted && lane == 0) mbar_arrive(&qempty[qs]);
+    if (!aborted) {
+      if (lane == 0) mbar_arrive(&qempty[qs]);
+      if constexpr (NTOK == 1) {
+        if (use_hist) flush_hist(qb.t0);
+      }
+    }
   }
 
   tc_fence_before();
@@ -459,8 +369,8 @@ static cudaError_t launch_logits_t(const CUtensorMap* tmap_k, const CUtensorMap*
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  logits_kernel<NTOK><<<num_sms, C::kThreads, C::kSmemBytes, stream>>>(*tmap_k, *tmap_q, plan, a);
-  return cudaGetLastError();
+  return launch_pdl(logits_kernel<NTOK>, dim3(num_sms), dim3(C::kThreads), C::kSmemBytes, stream, *tmap_k, *tmap_q,
+                    plan, a);
 }
 
 cudaError_t launch_logits(int ntok_per_block, const CUtensorMap* tmap_k, const CUtensorMap* tmap_q,

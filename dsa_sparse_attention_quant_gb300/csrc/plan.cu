@@ -1,0 +1,244 @@
+// plan.cu — work planning for the score kernels, and the fused per-layer
+// prologue (K quant + cache write, q quant + weight fold, plan) (sm_103a).
+//
+// The plan splits every request into query blocks (1 token for the decode
+// segment, 4 for the prefill segment), counts the 128-key tiles each block
+// scores (keys visible to its last token: causal, [0, position]), and cuts the
+// flat list of (block, tile) items into one equal slice per persistent CTA of
+// the score kernel, so each CTA starts with a single load. Request metadata
+// is staged in shared memory so the lookups are not chains of global loads.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dsa {
+
+constexpr int kPlanStage = 2048;  // requests per segment staged in shared memory
+
+__device__ int block_scan_incl(int v, int* sm, int* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) sm[wid] = v;
+  __syncthreads();
+  if (wid == 0) {
+    int x = lane < nw ? sm[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int n = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += n;
+    }
+    if (lane < nw) sm[lane] = x;
+  }
+  __syncthreads();
+  const int res = v + (wid > 0 ? sm[wid - 1] : 0);
+  *total = sm[nw - 1];
+  __syncthreads();
+  return res;
+}
+
+struct PlanSmem {
+  int scan[33];
+  int qsl[kPlanStage + 1];
+  int sl[kPlanStage];
+  int base[kPlanStage + 1];
+};
+
+__device__ __forceinline__ QBlock make_qblock(const int* qsl, const int* sl, const int* base, int nreq, int r_begin,
+                                              int ntok, int j) {
+  int lo = 0, hi = nreq - 1;  // last r with base[r] <= j
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (base[mid] <= j) lo = mid; else hi = mid - 1;
+  }
+  const int jj = j - base[lo];
+  const int q0 = qsl[lo], ql = qsl[lo + 1] - q0;
+  QBlock b;
+  b.req = r_begin + lo;
+  b.t0 = q0 + jj * ntok;
+  b.ntok = min(ntok, ql - jj * ntok);
+  b.p0 = sl[lo] - ql + jj * ntok;
+  return b;
+}
+
+// Plan requests [r_begin, r_end) into query blocks of up to `ntok` tokens.
+__device__ void plan_segment(const int32_t* qsl_g, const int32_t* sl_g, int r_begin, int r_end, int ntok,
+                             int num_tokens, int64_t bt_stride, int grid, SegmentPlan P, int32_t* err,
+                             PlanSmem& S) {
+  const int nreq = r_end - r_begin;
+  const bool staged = nreq <= kPlanStage;
+  if (staged) {
+    for (int i = threadIdx.x; i <= nreq; i += blockDim.x) S.qsl[i] = qsl_g[r_begin + i];
+    for (int i = threadIdx.x; i < nreq; i += blockDim.x) S.sl[i] = sl_g[r_begin + i];
+    __syncthreads();
+  }
+  const int* qsl = staged ? S.qsl : qsl_g + r_begin;  // request-relative views
+  const int* sl = staged ? S.sl : sl_g + r_begin;
+  int* base = staged ? S.base : P.req_base;
+  int carry = 0, tot;
+  for (int b0 = 0; b0 < nreq; b0 += blockDim.x) {
+    const int r = b0 + threadIdx.x;
+    int c = 0;
+    if (r < nreq) {
+      const int ql = qsl[r + 1] - qsl[r];
+      const int s = sl[r];
+      if (ql < 0 || s < ql || static_cast<int64_t>(s) > bt_stride * kBlock || qsl[r] < 0 ||
+          qsl[r + 1] > num_tokens) {
+        flag_error(err, DSA_DEVERR_SEQ_RANGE);
+      } else {
+        c = (ql + ntok - 1) / ntok;
+      }
+    }
+    const int incl = block_scan_incl(c, S.scan, &tot);
+    if (r < nreq) base[r] = carry + incl - c;
+    carry += tot;
+  }
+  int nqb = carry;
+  if (nqb > P.max_qb) {  // metadata inconsistent with the host sizes: plan nothing
+    if (threadIdx.x == 0) flag_error(err, DSA_DEVERR_SEQ_RANGE);
+    nqb = 0;
+  }
+  if (threadIdx.x == 0) {
+    base[nreq] = nqb;
+    *P.nqb = nqb;
+  }
+  __syncthreads();
+  // pass 1: count the tiles of the segment
+  int total = 0;
+  for (int b0 = 0; b0 < nqb; b0 += blockDim.x) {
+    const int j = b0 + threadIdx.x;
+    int tiles = 0;
+    if (j < nqb) {
+      const QBlock b = make_qblock(qsl, sl, base, nreq, r_begin, ntok, j);
+      P.qb[j] = b;
+      tiles = (b.p0 + b.ntok + 127) / 128;
+    }
+    block_scan_incl(tiles, S.scan, &tot);
+    total += tot;
+  }
+  for (int c = threadIdx.x; c < grid; c += blockDim.x) P.cta[c] = CtaWork{0, 0, 0, 0};
+  __syncthreads();
+  // pass 2: tile prefix, and for every CTA the block holding the start of its slice
+  carry = 0;
+  for (int b0 = 0; b0 < nqb; b0 += blockDim.x) {
+    const int j = b0 + threadIdx.x;
+    int tiles = 0;
+    if (j < nqb) {
+      const QBlock b = make_qblock(qsl, sl, base, nreq, r_begin, ntok, j);
+      tiles = (b.p0 + b.ntok + 127) / 128;
+    }
+    const int incl = block_scan_incl(tiles, S.scan, &tot);
+    if (j < nqb) {
+      const int s = carry + incl - tiles;
+      P.tile_start[j] = s;
+      // CTA c starts at floor(total*c/grid): the c with s <= start < s + tiles
+      const int64_t c_lo = (static_cast<int64_t>(s) * grid + total - 1) / total;
+      const int64_t c_hi = (static_cast<int64_t>(s + tiles) * grid + total - 1) / total - 1;
+      for (int64_t c = c_lo; c <= c_hi && c < grid; ++c) {
+        const int b_lo = static_cast<int>(static_cast<int64_t>(total) * c / grid);
+        const int b_hi = static_cast<int>(static_cast<int64_t>(total) * (c + 1) / grid);
+        P.cta[c] = CtaWork{b_lo, b_hi, j, b_lo - s};
+      }
+    }
+    carry += tot;
+  }
+  if (threadIdx.x == 0) P.tile_start[nqb] = carry;
+  __syncthreads();
+}
+
+__device__ void plan_batch(const PlanArgs& p) {
+  __shared__ PlanSmem S;
+  if (threadIdx.x == 0 && p.qsl[p.num_decodes] != p.num_decode_tokens) flag_error(p.err, DSA_DEVERR_SEQ_RANGE);
+  // a segment without requests launches no score kernel: nothing to plan
+  if (p.num_decodes > 0)
+    plan_segment(p.qsl, p.seq_lens, 0, p.num_decodes, 1, p.num_tokens, p.bt_stride, p.grid, p.dec, p.err, S);
+  if (p.num_reqs > p.num_decodes)
+    plan_segment(p.qsl, p.seq_lens, p.num_decodes, p.num_reqs, 4, p.num_tokens, p.bt_stride, p.grid, p.pre, p.err,
+                 S);
+}
+
+// ---------------------------------------------------------------------------
+// One launch per F layer before the scores: CTA 0 plans (first layer of a
+// step only; being first it is dispatched first and overlaps the rest); the
+// others quantise the step's K into the cache and the q rows with the weight
+// fold, one warp per 128-value row, and zero the decode rows' score
+// histograms and top-k counters.
+constexpr int kPrologueThreads = 1024;
+
+__global__ void __launch_bounds__(kPrologueThreads) prologue_kernel(PrologueArgs a) {
+  pdl_launch_dependents();  // the score kernel may start its set-up now
+  if (a.plan && blockIdx.x == 0) {
+    plan_batch(a.p);
+    return;
+  }
+  const int first = a.plan ? 1 : 0;
+  const int work_ctas = gridDim.x - first;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(work_ctas) * (kPrologueThreads / 32);
+  const int64_t q_rows = a.q != nullptr ? static_cast<int64_t>(a.n_tokens) * kHeads : 0;
+  const int64_t k_rows = a.k_new != nullptr ? a.n_tokens : 0;
+  const int64_t z_rows = a.hist != nullptr ? a.hist_rows : 0;
+  // jobs: groups of 4 q rows (their loads are issued together), then K rows, then zeroing
+  constexpr int kGroup = 4;
+  const int64_t q_groups = (q_rows + kGroup - 1) / kGroup;
+  const int64_t jobs = q_groups + k_rows + z_rows;
+  for (int64_t j = static_cast<int64_t>(blockIdx.x - first) * (kPrologueThreads / 32) + (threadIdx.x >> 5); j < jobs;
+       j += warps) {
+    if (j < q_groups) {
+      const int64_t r0 = j * kGroup;
+      uint2 raw[kGroup];
+      float wv[kGroup];
+#pragma unroll
+      for (int u = 0; u < kGroup; ++u) {
+        const int64_t r = r0 + u;
+        raw[u] = r < q_rows ? __ldg(reinterpret_cast<const uint2*>(a.q + r * kDim) + lane) : make_uint2(0, 0);
+        wv[u] = (lane == 0 && r < q_rows) ? __ldg(a.w + r) : 0.0f;
+      }
+#pragma unroll
+      for (int u = 0; u < kGroup; ++u) {
+        const int64_t r = r0 + u;
+        if (r >= q_rows) break;  // warp-uniform
+        float s;
+        const uint32_t codes = quant_row_lane(raw[u], &s);
+        reinterpret_cast<uint32_t*>(a.q_fp8 + r * kDim)[lane] = codes;
+        if (lane == 0) a.w_folded[r] = __fmul_rn(__fmul_rn(__fmul_rn(wv[u], s), a.softmax_scale), 0.125f);
+      }
+    } else if (j < q_groups + k_rows) {
+      const int64_t t = j - q_groups;
+      const int64_t slot = __ldg(a.slot_mapping + t);
+      if (slot < 0) continue;
+      if (slot >= a.num_blocks * kBlock) {
+        if (lane == 0) flag_error(a.err, DSA_DEVERR_SLOT_RANGE);
+        continue;
+      }
+      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(a.k_new + t * kDim) + lane);
+      float s;
+      const uint32_t codes = quant_row_lane(raw, &s);
+      uint8_t* page = a.k_cache + (slot / kBlock) * kPageBytes;
+      const int off = static_cast<int>(slot % kBlock);
+      reinterpret_cast<uint32_t*>(page + off * kDim)[lane] = codes;
+      if (lane == 0) *reinterpret_cast<float*>(page + kScaleOffset + off * 4) = s;
+    } else {
+      const int64_t t = j - q_groups - k_rows;
+      uint4* h = reinterpret_cast<uint4*>(a.hist + t * kHistBins);
+#pragma unroll 4
+      for (int b = lane; b < kHistBins / 4; b += 32) h[b] = make_uint4(0, 0, 0, 0);
+      if (lane == 0) reinterpret_cast<uint4*>(a.counters)[t] = make_uint4(0, 0, 0, 0);
+    }
+  }
+}
+
+cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t stream) {
+  if (a.plan && (a.p.grid < 1 || a.p.grid > kMaxCtas)) return cudaErrorInvalidValue;
+  const int64_t q_groups = a.q != nullptr ? (static_cast<int64_t>(a.n_tokens) * kHeads + 3) / 4 : 0;
+  const int64_t jobs = q_groups + (a.k_new != nullptr ? a.n_tokens : 0) + (a.hist != nullptr ? a.hist_rows : 0);
+  int64_t quant = (jobs + kPrologueThreads / 32 - 1) / (kPrologueThreads / 32);  // one job per warp, if it fits
+  if (quant < 1) quant = 1;
+  if (quant > 1216) quant = 1216;  // ~4 waves of 2 CTAs per SM; the rest loops
+  prologue_kernel<<<static_cast<unsigned>(quant + (a.plan ? 1 : 0)), kPrologueThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace dsa

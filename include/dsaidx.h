@@ -92,10 +92,11 @@ DSA_API int dsa_check_device_error(const int32_t *dev_err, uint32_t *out, dsa_st
  * keys [0, position] (causal, itself included). Key s of request r lives in
  * slot block_table[r*bt_stride + s/64]*64 + s%64 of the paged cache. */
 typedef struct DsaBatch {
-  int32_t num_reqs;        /* B >= 0 */
-  int32_t num_decodes;     /* requests [0, num_decodes) are run by the decode kernel */
-  int32_t num_tokens;      /* T = query_start_loc[B] (host copy) */
-  int32_t max_seq_len;     /* host upper bound of seq_lens[*]; sizes the score rows */
+  int32_t num_reqs;          /* B >= 0 */
+  int32_t num_decodes;       /* requests [0, num_decodes) are run by the decode kernel */
+  int32_t num_decode_tokens; /* query_start_loc[num_decodes] (host copy) */
+  int32_t num_tokens;        /* T = query_start_loc[B] (host copy) */
+  int32_t max_seq_len;       /* host upper bound of seq_lens[*]; sizes the score rows */
   int64_t bt_stride;       /* row stride of block_table, int32 elements */
   int64_t num_blocks;      /* pages in the K cache */
   const int32_t *query_start_loc;  /* device [B+1] */
@@ -175,6 +176,17 @@ DSA_API int dsa_indexer_logits(const DsaBatch *batch, const uint8_t *q_fp8, cons
 DSA_API int dsa_indexer_topk(const DsaBatch *batch, const float *logits, int64_t logits_ld,
                      int32_t topk, int32_t *topk_out, void *ws, size_t ws_bytes,
                      dsa_stream_t stream);
+
+/* Measurement aid (not a step of the method): a launch timeline. On the
+ * calling host thread, the following calls of dsa_indexer_logits_topk,
+ * dsa_indexer_logits and dsa_layer_stack_run record events[0], events[1], ...
+ * in order: one before the first kernel of each fused call and one after
+ * every kernel they launch, until the n_events handles (cudaEvent_t created by
+ * the caller) are used up. Under CUDA-graph capture they become external
+ * event nodes. cudaEventElapsedTime between consecutive events then gives each
+ * kernel's device time on its own stream. n_events = 0 switches it off;
+ * at most 32 events; a NULL handle is DSA_EINVAL. Host-only. */
+DSA_API int dsa_set_launch_events(void *const *events, int32_t n_events);
 
 /* dsa_indexer_logits_topk for callers that cannot allocate device memory.
  * The pages have no counterpart: this is a service of this library. Callers

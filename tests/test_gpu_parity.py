@@ -105,6 +105,21 @@ def test_decode_requests_with_two_query_tokens():
     check_batch(hb)
 
 
+def test_identical_keys_every_score_ties():
+    # every key of a request identical: one score per row, so the boundary bin
+    # holds the whole row (per-row kernel past its candidate buffer; the
+    # multi-CTA select past its staged candidates)
+    hb = synth.make_batch(13, [9000, 20000], [], 256)
+    first = {}
+    for i, s in enumerate(hb.ctx_slots):
+        r = 0 if i < 8999 else 1
+        first.setdefault(r, hb.ctx_k[i].copy())
+        hb.ctx_k[i] = first[r]
+    for t in range(hb.num_tokens):
+        hb.k_new[t] = first[t]
+    check_batch(hb)
+
+
 def test_empty_batch():
     hb = synth.make_batch(10, [], [], 64)
     db = DeviceBatch(hb)

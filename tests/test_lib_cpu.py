@@ -68,11 +68,11 @@ def test_host_validation_without_gpu():
                                             None) == binding.DSA_EINVAL
     assert lib.dsa_topk_logical_to_physical(P(16), 4, 8192, P(16), P(16), 1, 0, P(16), None, None,
                                             None) == binding.DSA_EINVAL
-    b = binding.DsaBatchC(1, 2, 1, 10, 1, 1, 16, 16, 16, 16)  # num_decodes > num_reqs
+    b = binding.DsaBatchC(1, 2, 1, 1, 10, 1, 1, 16, 16, 16, 16)  # num_decodes > num_reqs
     assert lib.dsa_indexer_workspace_size(ctypes.byref(b), 64) == 0
     # empty batches are no-ops that succeed without a device
     assert lib.dsa_indexer_k_quant_write(None, 0, 128, None, P(16), 1, None, None) == binding.DSA_OK
-    empty = binding.DsaBatchC(0, 0, 0, 0, 1, 1, None, None, None, None)
+    empty = binding.DsaBatchC(0, 0, 0, 0, 0, 1, 1, None, None, None, None)
     assert lib.dsa_indexer_logits_topk(ctypes.byref(empty), None, None, None, 64, None, None, 0, None, None,
                                        None, None) == binding.DSA_OK
 
