@@ -120,10 +120,11 @@ int64_t logits_ld(const DsaBatch* b) {
 // Persistent logits grid: one CTA per SM. The plan and the launch must agree on it.
 int grid_ctas(int sms) { return sms < kMaxCtas ? sms : kMaxCtas; }
 
-// Workspace of the indexer: both segment plans, the score matrix, and for the
-// decode rows the score histograms, top-k counters and boundary candidates.
+// Workspace of the indexer: the prefill segment's plan (the decode score kernel
+// plans its own work), the score matrix, and for the decode rows the score
+// histograms, top-k counters and boundary candidates.
 struct IndexerWs {
-  SegmentPlan dec, pre;
+  SegmentPlan pre;
   float* logits;
   uint32_t* hist;
   uint32_t* counters;
@@ -145,19 +146,12 @@ IndexerWs carve(const DsaBatch* b, void* base) {
   const size_t B = static_cast<size_t>(b->num_reqs);
   const size_t Td = static_cast<size_t>(b->num_decode_tokens);
   const size_t ld = static_cast<size_t>(logits_ld(b));
-  const size_t max_dec = Td + 1;
   const size_t max_pre = T / 4 + B + 1;
-  w.dec.qb = static_cast<QBlock*>(take(max_dec * sizeof(QBlock)));
-  w.dec.tile_start = static_cast<int32_t*>(take((max_dec + 1) * 4));
-  w.dec.nqb = static_cast<int32_t*>(take(4));
-  w.dec.req_base = static_cast<int32_t*>(take((B + 1) * 4));
-  w.dec.cta = static_cast<CtaWork*>(take(kMaxCtas * sizeof(CtaWork)));
   w.pre.qb = static_cast<QBlock*>(take(max_pre * sizeof(QBlock)));
   w.pre.tile_start = static_cast<int32_t*>(take((max_pre + 1) * 4));
   w.pre.nqb = static_cast<int32_t*>(take(4));
   w.pre.req_base = static_cast<int32_t*>(take((B + 1) * 4));
   w.pre.cta = static_cast<CtaWork*>(take(kMaxCtas * sizeof(CtaWork)));
-  w.dec.max_qb = static_cast<int32_t>(max_dec);
   w.pre.max_qb = static_cast<int32_t>(max_pre);
   w.logits = static_cast<float*>(take(T * ld * 4));
   w.hist = static_cast<uint32_t*>(take(Td * kHistBins * 4));
@@ -169,13 +163,12 @@ IndexerWs carve(const DsaBatch* b, void* base) {
 }
 
 PlanArgs plan_args(const DsaBatch* b, const IndexerWs& ws, int sms, int32_t* dev_err) {
-  return PlanArgs{b->query_start_loc, b->seq_lens,    b->num_reqs, b->num_decodes, b->num_decode_tokens,
-                  b->num_tokens,      b->bt_stride,   grid_ctas(sms), ws.dec,     ws.pre,
-                  dev_err};
+  return PlanArgs{b->query_start_loc, b->seq_lens,    b->num_reqs,    b->num_decodes, b->num_decode_tokens,
+                  b->num_tokens,      b->bt_stride,   grid_ctas(sms), ws.pre,         dev_err};
 }
 
-// Prologue with no q: (optional) K quant + cache write, plan, and zeroed
-// decode-row histograms and counters.
+// Prologue with no q: (optional) K quant + cache write, the prefill plan (when
+// the batch has prefill requests), and zeroed decode-row histograms and counters.
 PrologueArgs plan_only(const DsaBatch* b, const IndexerWs& ws, int sms, const void* k_new,
                        const int64_t* slot_mapping, uint8_t* k_cache, int32_t* dev_err) {
   PrologueArgs pa{};
@@ -184,7 +177,7 @@ PrologueArgs plan_only(const DsaBatch* b, const IndexerWs& ws, int sms, const vo
   pa.k_cache = k_cache;
   pa.num_blocks = b->num_blocks;
   pa.n_tokens = b->num_tokens;
-  pa.plan = true;
+  pa.plan = b->num_reqs > b->num_decodes;
   pa.p = plan_args(b, ws, sms, dev_err);
   pa.hist = ws.hist;
   pa.counters = ws.counters;
@@ -221,11 +214,13 @@ int run_logits(const DsaBatch* b, const uint8_t* q_fp8, const float* w_folded, c
   if (st != DSA_OK) return st;
   CUtensorMap mk, mq1, mq4;
   if ((st = make_kcache_map(&mk, k_cache, b->num_blocks)) != DSA_OK) return st;
-  LogitsArgs a{w_folded, k_cache, b->block_table, b->bt_stride, b->num_blocks, logits, ld,
-               hist ? ws.hist : nullptr, hist ? ws.hist_rows : 0, dev_err};
+  LogitsArgs a{w_folded,          k_cache,    b->block_table,   b->bt_stride,   b->num_blocks,
+               logits,            ld,         hist ? ws.hist : nullptr,          hist ? ws.hist_rows : 0,
+               b->query_start_loc, b->seq_lens, b->req_id_per_token, b->num_decodes, b->num_decode_tokens,
+               dev_err};
   if (b->num_decodes > 0) {
     if ((st = make_q_map(&mq1, q_fp8, b->num_tokens, kHeads)) != DSA_OK) return st;
-    if ((st = launched(launch_logits(1, &mk, &mq1, ws.dec, a, grid_ctas(sms), stream), stream)) != DSA_OK) return st;
+    if ((st = launched(launch_logits(1, &mk, &mq1, SegmentPlan{}, a, grid_ctas(sms), stream), stream)) != DSA_OK) return st;
   }
   if (b->num_reqs > b->num_decodes) {
     if ((st = make_q_map(&mq4, q_fp8, b->num_tokens, 4 * kHeads)) != DSA_OK) return st;
@@ -485,7 +480,8 @@ int dsa_layer_stack_run(const DsaStackPlan* plan, const DsaBatch* batch, const i
       if (batch->num_tokens > 0) {
         const DsaLayerInputs& L = plan->layers[l];
         // one launch: this layer's K into its cache, q quant + weight fold, and
-        // (first F layer only: the batch layout is the same for every layer) the plan
+        // (first F layer only: the batch layout is the same for every layer) the
+        // prefill plan
         // (histograms and counters of the decode rows zeroed for this layer's top-k)
         PrologueArgs pa = plan_only(batch, w, sms, L.k_new, slot_mapping, L.k_cache, dev_err);
         pa.q = static_cast<const __nv_bfloat16*>(L.q);
@@ -493,7 +489,7 @@ int dsa_layer_stack_run(const DsaStackPlan* plan, const DsaBatch* batch, const i
         pa.softmax_scale = softmax_scale;
         pa.q_fp8 = q8;
         pa.w_folded = wf;
-        pa.plan = !planned;
+        pa.plan = pa.plan && !planned;
         if ((st = mark(stream)) != DSA_OK) return st;
         st = launched(launch_prologue(pa, stream), stream);
         if (st != DSA_OK) return st;

@@ -276,6 +276,32 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
+// Block-wide inclusive prefix sum of v; *total = the block's sum. sm: 33 ints of shared memory.
+__device__ __forceinline__ int block_scan_incl(int v, int* sm, int* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) sm[wid] = v;
+  __syncthreads();
+  if (wid == 0) {
+    int x = lane < nw ? sm[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int n = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += n;
+    }
+    if (lane < nw) sm[lane] = x;
+  }
+  __syncthreads();
+  const int res = v + (wid > 0 ? sm[wid - 1] : 0);
+  *total = sm[nw - 1];
+  __syncthreads();
+  return res;
+}
+
 // Order-preserving map of fp32 to uint32: a > b  <=>  key(a) > key(b).
 __device__ __forceinline__ uint32_t f32_key(float f) {
   uint32_t u = __float_as_uint(f);

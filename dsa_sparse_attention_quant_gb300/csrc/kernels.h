@@ -57,7 +57,7 @@ struct PlanArgs {
   int num_reqs, num_decodes, num_decode_tokens, num_tokens;
   int64_t bt_stride;
   int grid;  // CTAs of the score kernels
-  SegmentPlan dec, pre;
+  SegmentPlan pre;  // the prefill segment (the decode score kernel plans its own work)
   int32_t* err;
 };
 
@@ -100,6 +100,12 @@ struct LogitsArgs {
   int64_t ld;
   uint32_t* hist;  // [hist_rows][kHistBins] or nullptr: decode rows' score histograms (zeroed before)
   int hist_rows;
+  // request metadata, from which the decode score kernel plans its own slice
+  const int32_t* qsl;
+  const int32_t* seq_lens;
+  const int32_t* req_id;
+  int num_decodes;
+  int num_dec_tokens;
   int32_t* err;
 };
 
@@ -121,7 +127,9 @@ struct SelectArgs {
   uint2* cand;              // [n_rows][ld]: (key, id) of the boundary bin
 };
 
-// ntok_per_block = 1 (decode segment) or 4 (prefill segment).
+// ntok_per_block = 1 (decode segment: the kernel plans its slice from the
+// request metadata in `a`, `plan` is unused) or 4 (prefill segment, `plan`
+// written by the prologue).
 cudaError_t launch_logits(int ntok_per_block, const CUtensorMap* tmap_k, const CUtensorMap* tmap_q,
                           SegmentPlan plan, const LogitsArgs& a, int num_sms, cudaStream_t stream);
 

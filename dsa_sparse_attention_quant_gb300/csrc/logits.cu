@@ -43,9 +43,10 @@ struct LogitsCfg {
   static constexpr int kOffBar = kOffW + 2 * kWBytes;
   static constexpr int kNumBars = 2 * kStages + 4 + 2 * kAcc + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kOffMeta = kOffMisc + 16;  // 2 QMeta (2 x 24 B), the slice (4 ints), scan scratch (33 ints)
   // decode: one score histogram per epilogue warp (first radix round of the top-k)
   static constexpr int kHistBytes = NTOK == 1 ? kEpiWarps * kHistBins * 4 : 0;
-  static constexpr int kOffHist = (kOffMisc + 16 + 127) / 128 * 128;
+  static constexpr int kOffHist = (kOffMeta + 2 * 24 + 4 * 4 + 33 * 4 + 127) / 128 * 128;
   static constexpr int kSmemBytes = kOffHist + kHistBytes + 1024;  // + slack to align the base to 1024
   static constexpr uint32_t kIdesc = f8_idesc(128, N);
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -58,6 +59,74 @@ __device__ __forceinline__ bool mbar_wait_until(uint64_t* bar, uint32_t parity, 
     if (global_ns() > deadline) return false;
   }
   return true;
+}
+
+// The query block whose q / w' tile a q buffer holds, written by the producer
+// before it arrives on the buffer's barrier, read by the MMA and epilogue warps.
+struct QMeta {
+  QBlock qb;
+  int32_t tiles;  // tiles of the block inside this CTA's slice
+  int32_t kt0;    // the first of them
+};
+
+// Decode query block of token t (one token per block): request, position and
+// number of 128-key tiles; 0 tiles when the request metadata is inconsistent.
+__device__ __forceinline__ int decode_block(const LogitsArgs& a, int t, QBlock* out) {
+  const int r = __ldg(a.req_id + t);
+  QBlock b{r, t, 1, 0};
+  int tiles = 0;
+  if (r >= 0 && r < a.num_decodes) {
+    const int q0 = __ldg(a.qsl + r), q1 = __ldg(a.qsl + r + 1), sl = __ldg(a.seq_lens + r);
+    if (t >= q0 && t < q1 && sl >= q1 - q0 && static_cast<int64_t>(sl) <= a.bt_stride * kBlock) {
+      b.p0 = sl - (q1 - q0) + (t - q0);
+      tiles = (b.p0 + 1 + 127) / 128;
+    }
+  }
+  *out = b;
+  return tiles;
+}
+
+// Decode segment: this CTA's slice {it_begin, it_end, first token, first tile}
+// of the flat (token, tile) list, computed by the whole CTA from the request
+// metadata. slice[] is shared memory; scan[] is block-scan scratch.
+__device__ void decode_slice(const LogitsArgs& a, int* slice, int* scan) {
+  const int T = a.num_dec_tokens;
+  const int nt = blockDim.x, tid = threadIdx.x;
+  if (blockIdx.x == 0 && tid == 0 && (__ldg(a.qsl) != 0 || __ldg(a.qsl + a.num_decodes) != T))
+    flag_error(a.err, DSA_DEVERR_SEQ_RANGE);
+  int total = 0, tot;
+  for (int c0 = 0; c0 < T; c0 += nt) {
+    const int t = c0 + tid;
+    QBlock b;
+    const int tiles = t < T ? decode_block(a, t, &b) : 0;
+    if (t < T && tiles == 0 && blockIdx.x == 0) flag_error(a.err, DSA_DEVERR_SEQ_RANGE);
+    block_scan_incl(tiles, scan, &tot);
+    total += tot;
+  }
+  const int b0 = static_cast<int>(static_cast<int64_t>(total) * blockIdx.x / gridDim.x);
+  const int b1 = static_cast<int>(static_cast<int64_t>(total) * (blockIdx.x + 1) / gridDim.x);
+  if (tid == 0) {
+    slice[0] = b0;
+    slice[1] = b1;
+    slice[2] = 0;
+    slice[3] = 0;
+  }
+  if (b0 < b1) {
+    int carry = 0;
+    for (int c0 = 0; c0 < T; c0 += nt) {
+      const int t = c0 + tid;
+      QBlock b;
+      const int tiles = t < T ? decode_block(a, t, &b) : 0;
+      const int incl = block_scan_incl(tiles, scan, &tot);
+      const int s = carry + incl - tiles;
+      if (t < T && tiles > 0 && s <= b0 && b0 < s + tiles) {
+        slice[2] = t;
+        slice[3] = b0 - s;
+      }
+      carry += tot;
+    }
+  }
+  __syncthreads();
 }
 
 template <int NTOK>
@@ -78,6 +147,9 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
   uint64_t* done = tempty + A;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  QMeta* qmeta = reinterpret_cast<QMeta*>(smem + C::kOffMeta);
+  int* slice = reinterpret_cast<int*>(smem + C::kOffMeta + 2 * sizeof(QMeta));
+  int* scan = slice + 4;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -108,123 +180,137 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  // Everything above may overlap the previous kernel of the stream (programmatic
-  // dependent launch); the plan, q codes, weights and K cache are read below.
-  pdl_wait();
+  // This CTA's slice. Everything before pdl_wait() may overlap the previous
+  // kernel of the stream (programmatic dependent launch); the decode slice
+  // only needs the request metadata, an input of the step. The q codes, the
+  // weights, the K cache and the prefill plan are read after it.
+  int it_begin, it_end, j0, kt0;
+  if constexpr (NTOK == 1) {
+    decode_slice(a, slice, scan);
+    it_begin = slice[0];
+    it_end = slice[1];
+    j0 = slice[2];
+    kt0 = slice[3];
+    pdl_wait();
+  } else {
+    pdl_wait();
+    const CtaWork cw = plan.cta[blockIdx.x];
+    it_begin = cw.it_begin;
+    it_end = cw.it_end;
+    j0 = cw.qb0;
+    kt0 = cw.kt0;
+  }
   pdl_launch_dependents();
-  const CtaWork cw = plan.cta[blockIdx.x];  // this CTA's slice, laid out by the plan kernel
-  const int it_begin = cw.it_begin;         // an empty slice runs no loop iteration below
-  const int it_end = cw.it_end;
-  const int j0 = cw.qb0;  // first query block of this CTA's slice
+  const int items = it_end - it_begin;  // tiles of this CTA (an empty slice runs no loop)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    int j = j0;
-    QBlock qb = plan.qb[j];
-    int jt_end = plan.tile_start[j + 1];
-    int kt = cw.kt0;
-    int qcount = 0, n = 0, npages = 0, batch = -1;
-    int32_t cur_ids = -1, nxt_ids = -1;
-    const int32_t* bt_row = nullptr;
-    bool new_qb = true;
-    for (int it = it_begin; it < it_end; ++it, ++n, ++kt) {
-      if (it == jt_end) {
-        ++j;
-        qb = plan.qb[j];
-        jt_end = plan.tile_start[j + 1];
-        kt = 0;
-        new_qb = true;
+    auto block_at = [&](int j, QBlock* qb) -> int {  // block j and its tile count
+      if constexpr (NTOK == 1) {
+        return decode_block(a, j, qb);
+      } else {
+        *qb = plan.qb[j];
+        return plan.tile_start[j + 1] - plan.tile_start[j];
       }
-      if (new_qb) {
-        const int qs = qcount & 1;
-        int ok = 1;
-        if (lane == 0) ok = mbar_wait(&qempty[qs], ((qcount >> 1) & 1) ^ 1, abort_flag, a.err);
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&qfull[qs], C::kQBytes + qb.ntok * kHeads * 4);
-          tma_load_2d(smem + C::kOffQ + qs * C::kQBytes, &tmap_q, &qfull[qs], 0, qb.t0 * kHeads);
-          bulk_load(smem + C::kOffW + qs * C::kWBytes, a.w_folded + static_cast<int64_t>(qb.t0) * kHeads,
-                    qb.ntok * kHeads * 4, &qfull[qs]);
-        }
-        ++qcount;
-        npages = (qb.p0 + qb.ntok + kBlock - 1) / kBlock;
-        bt_row = a.block_table + static_cast<int64_t>(qb.req) * a.bt_stride;
-        batch = (2 * kt) >> 5;
-        const int p = batch * 32 + lane;
-        cur_ids = p < npages ? __ldg(bt_row + p) : -1;
-        nxt_ids = p + 32 < npages ? __ldg(bt_row + p + 32) : -1;
-        new_qb = false;
-      }
-      const int stage = n % S;
-      int ok = 1;
-      if (lane == 0) ok = mbar_wait(&empty[stage], ((n / S) & 1) ^ 1, abort_flag, a.err);
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      if (((2 * kt) >> 5) != batch) {  // moved into the next batch of 32 page ids
-        ++batch;
-        cur_ids = nxt_ids;
-        const int p = (batch + 1) * 32 + lane;
-        nxt_ids = p < npages ? __ldg(bt_row + p) : -1;
-      }
-      const int id0 = __shfl_sync(0xffffffffu, cur_ids, (2 * kt) & 31);
-      const int id1 = __shfl_sync(0xffffffffu, cur_ids, (2 * kt + 1) & 31);
+    };
+    int j = j0, kt = kt0, n = 0, qcount = 0;
+    bool ok = true;
+    QBlock qb{};
+    int block_tiles = items > 0 ? block_at(j, &qb) : 0;
+    while (ok && n < items) {
+      const int in_slice = min(block_tiles - kt, items - n);
+      const int qs = qcount & 1;
+      int w = 1;
+      if (lane == 0) w = mbar_wait(&qempty[qs], ((qcount >> 1) & 1) ^ 1, abort_flag, a.err);
+      if (!__shfl_sync(0xffffffffu, w, 0)) break;
       if (lane == 0) {
-        uint8_t* st = smem + stage * C::kStageBytes;
-        const bool in1 = 2 * kt + 1 < npages;
-        const bool v0 = id0 >= 0 && id0 < a.num_blocks;
-        const bool v1 = in1 && id1 >= 0 && id1 < a.num_blocks;
-        if (!v0 || (in1 && !v1)) flag_error(a.err, DSA_DEVERR_BLOCK_RANGE);
-        mbar_arrive_expect_tx(&full[stage], (v0 ? 8192 + 256 : 0) + (v1 ? 8192 + 256 : 0));
-        if (v0) {
-          tma_load_3d(st, &tmap_k, &full[stage], 0, 0, id0);
-          bulk_load(st + C::kScaleOff, a.k_cache + static_cast<int64_t>(id0) * kPageBytes + kScaleOffset, 256,
-                    &full[stage]);
+        qmeta[qs] = QMeta{qb, in_slice, kt};
+        mbar_arrive_expect_tx(&qfull[qs], C::kQBytes + qb.ntok * kHeads * 4);
+        tma_load_2d(smem + C::kOffQ + qs * C::kQBytes, &tmap_q, &qfull[qs], 0, qb.t0 * kHeads);
+        bulk_load(smem + C::kOffW + qs * C::kWBytes, a.w_folded + static_cast<int64_t>(qb.t0) * kHeads,
+                  qb.ntok * kHeads * 4, &qfull[qs]);
+      }
+      ++qcount;
+      // page ids of this block, 32 at a time across the warp, one batch ahead
+      const int npages = (qb.p0 + qb.ntok + kBlock - 1) / kBlock;
+      const int32_t* bt_row = a.block_table + static_cast<int64_t>(qb.req) * a.bt_stride;
+      int batch = (2 * kt) >> 5;
+      int p = batch * 32 + lane;
+      int32_t cur_ids = p < npages ? __ldg(bt_row + p) : -1;
+      int32_t nxt_ids = p + 32 < npages ? __ldg(bt_row + p + 32) : -1;
+      for (int e = 0; e < in_slice; ++e, ++n, ++kt) {
+        const int stage = n % S;
+        if (lane == 0) w = mbar_wait(&empty[stage], ((n / S) & 1) ^ 1, abort_flag, a.err);
+        if (!__shfl_sync(0xffffffffu, w, 0)) {
+          ok = false;
+          break;
         }
-        if (v1) {
-          tma_load_3d(st + 8192, &tmap_k, &full[stage], 0, 0, id1);
-          bulk_load(st + C::kScaleOff + 256, a.k_cache + static_cast<int64_t>(id1) * kPageBytes + kScaleOffset,
-                    256, &full[stage]);
+        if (((2 * kt) >> 5) != batch) {  // moved into the next batch of 32 page ids
+          ++batch;
+          cur_ids = nxt_ids;
+          p = (batch + 1) * 32 + lane;
+          nxt_ids = p < npages ? __ldg(bt_row + p) : -1;
+        }
+        const int id0 = __shfl_sync(0xffffffffu, cur_ids, (2 * kt) & 31);
+        const int id1 = __shfl_sync(0xffffffffu, cur_ids, (2 * kt + 1) & 31);
+        if (lane == 0) {
+          uint8_t* st = smem + stage * C::kStageBytes;
+          const bool in1 = 2 * kt + 1 < npages;
+          const bool v0 = id0 >= 0 && id0 < a.num_blocks;
+          const bool v1 = in1 && id1 >= 0 && id1 < a.num_blocks;
+          if (!v0 || (in1 && !v1)) flag_error(a.err, DSA_DEVERR_BLOCK_RANGE);
+          mbar_arrive_expect_tx(&full[stage], (v0 ? 8192 + 256 : 0) + (v1 ? 8192 + 256 : 0));
+          if (v0) {
+            tma_load_3d(st, &tmap_k, &full[stage], 0, 0, id0);
+            bulk_load(st + C::kScaleOff, a.k_cache + static_cast<int64_t>(id0) * kPageBytes + kScaleOffset, 256,
+                      &full[stage]);
+          }
+          if (v1) {
+            tma_load_3d(st + 8192, &tmap_k, &full[stage], 0, 0, id1);
+            bulk_load(st + C::kScaleOff + 256,
+                      a.k_cache + static_cast<int64_t>(id1) * kPageBytes + kScaleOffset, 256, &full[stage]);
+          }
         }
       }
+      ++j;
+      kt = 0;
+      if (ok && n < items) block_tiles = block_at(j, &qb);
     }
     if (lane == 0 && *abort_flag) {
       // let copies already issued land before the CTA's shared memory goes away
       const unsigned long long deadline = global_ns() + kWaitLimitNs;
       for (int m = (n > S ? n - S : 0); m < n; ++m) mbar_wait_until(&full[m % S], (m / S) & 1, deadline);
-      mbar_wait_until(&qfull[(qcount - 1) & 1], ((qcount - 1) >> 1) & 1, deadline);
+      if (qcount > 0) mbar_wait_until(&qfull[(qcount - 1) & 1], ((qcount - 1) >> 1) & 1, deadline);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int j = j0;
-      int jt_end = plan.tile_start[j + 1];
-      int qcount = 0, qs = 0, n = 0;
-      bool new_qb = true;
-      for (int it = it_begin; it < it_end; ++it, ++n) {
-        if (it == jt_end) {
-          ++j;
-          jt_end = plan.tile_start[j + 1];
-          new_qb = true;
-        }
-        if (new_qb) {
-          qs = qcount & 1;
-          if (!mbar_wait(&qfull[qs], (qcount >> 1) & 1, abort_flag, a.err)) break;
-          ++qcount;
-          new_qb = false;
-        }
-        const int stage = n % S;
-        const int acc = n % A;
-        if (!mbar_wait(&full[stage], (n / S) & 1, abort_flag, a.err)) break;
-        if (!mbar_wait(&tempty[acc], ((n / A) & 1) ^ 1, abort_flag, a.err)) break;
-        tc_fence_after();
-        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * C::N);
-        const uint32_t sa = smem_u32(smem + stage * C::kStageBytes);
+      int n = 0, qcount = 0;
+      bool ok = true;
+      while (ok && n < items) {
+        const int qs = qcount & 1;
+        if (!mbar_wait(&qfull[qs], (qcount >> 1) & 1, abort_flag, a.err)) break;
+        ++qcount;
+        const int in_slice = qmeta[qs].tiles;
         const uint32_t sb = smem_u32(smem + C::kOffQ + qs * C::kQBytes);
+        for (int e = 0; e < in_slice; ++e, ++n) {
+          const int stage = n % S;
+          const int acc = n % A;
+          if (!mbar_wait(&full[stage], (n / S) & 1, abort_flag, a.err) ||
+              !mbar_wait(&tempty[acc], ((n / A) & 1) ^ 1, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem_base + static_cast<uint32_t>(acc * C::N);
+          const uint32_t sa = smem_u32(smem + stage * C::kStageBytes);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_f8(d, sw128_kmajor_desc(sa + 32 * k), sw128_kmajor_desc(sb + 32 * k), C::kIdesc, k > 0 ? 1u : 0u);
-        mma_commit(&empty[stage]);
-        mma_commit(&tfull[acc]);
-        if (it + 1 == jt_end || it + 1 == it_end) mma_commit(&qempty[qs]);
+          for (int k = 0; k < 4; ++k)
+            mma_f8(d, sw128_kmajor_desc(sa + 32 * k), sw128_kmajor_desc(sb + 32 * k), C::kIdesc, k > 0 ? 1u : 0u);
+          mma_commit(&empty[stage]);
+          mma_commit(&tfull[acc]);
+        }
+        if (ok) mma_commit(&qempty[qs]);  // the block's q / w' buffer is free once its MMAs are done
       }
       mma_commit(done);  // completes once every MMA issued above has finished
       mbar_wait_until(done, 0, global_ns() + kWaitLimitNs);
@@ -234,118 +320,103 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
     const int g = (warp - 2) >> 2;        // warpgroup: takes every kEpiWG-th tile
     const int quarter = warp & 3;         // TMEM lanes this warp may read
     const int row = quarter * 32 + lane;  // key within the tile
-    int j = j0;
-    QBlock qb = plan.qb[j];
-    int jt_end = plan.tile_start[j + 1];
-    int kt = cw.kt0;
-    int qcount = 0, qs = 0, n = 0;
-    bool new_qb = true, aborted = false;
     float wr[NTOK == 1 ? kHeads : 1];
     // decode rows: this warp's histogram of the keys of its stored scores,
     // added to the row's global histogram when the warp leaves the row
     uint32_t* whist = reinterpret_cast<uint32_t*>(smem + C::kOffHist) + (warp - 2) * kHistBins;
-    bool use_hist = false;
-    auto flush_hist = [&](int row_t) {
-      __syncwarp();
-      uint32_t* dst = a.hist + static_cast<int64_t>(row_t) * kHistBins;
-      for (int b = lane; b < kHistBins; b += 32) {
-        const uint32_t v = whist[b];
-        if (v != 0) atomicAdd(dst + b, v);
-      }
-    };
-    for (int it = it_begin; it < it_end; ++it, ++n, ++kt) {
-      if (it == jt_end) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&qempty[qs]);  // done with this q/w' buffer
-        if constexpr (NTOK == 1) {
-          if (use_hist) flush_hist(qb.t0);
+    int n = 0, qcount = 0;
+    bool ok = true;
+    while (ok && n < items) {
+      const int qs = qcount & 1;
+      if (!mbar_wait(&qfull[qs], (qcount >> 1) & 1, abort_flag, a.err)) break;
+      ++qcount;
+      const QMeta meta = qmeta[qs];
+      const QBlock qb = meta.qb;
+      bool use_hist = false;
+      if constexpr (NTOK == 1) {
+        const float4* wsrc = reinterpret_cast<const float4*>(smem + C::kOffW + qs * C::kWBytes);
+#pragma unroll
+        for (int h = 0; h < kHeads / 4; ++h) {
+          const float4 v = wsrc[h];
+          wr[4 * h] = v.x;
+          wr[4 * h + 1] = v.y;
+          wr[4 * h + 2] = v.z;
+          wr[4 * h + 3] = v.w;
         }
-        ++j;
-        qb = plan.qb[j];
-        jt_end = plan.tile_start[j + 1];
-        kt = 0;
-        new_qb = true;
+        use_hist = a.hist != nullptr && qb.t0 < a.hist_rows;
+        if (use_hist) {
+          uint4* z = reinterpret_cast<uint4*>(whist);
+#pragma unroll 4
+          for (int b = lane; b < kHistBins / 4; b += 32) z[b] = make_uint4(0, 0, 0, 0);
+          __syncwarp();
+        }
       }
-      if (new_qb) {
-        qs = qcount & 1;
-        if (!mbar_wait(&qfull[qs], (qcount >> 1) & 1, abort_flag, a.err)) {
-          aborted = true;
+      for (int e = 0; e < meta.tiles; ++e, ++n) {
+        if ((n % C::kEpiWG) != g) continue;
+        const int stage = n % S;
+        const int acc = n % A;
+        if (!mbar_wait(&tfull[acc], (n / A) & 1, abort_flag, a.err) ||
+            !mbar_wait(&full[stage], (n / S) & 1, abort_flag, a.err)) {
+          ok = false;
           break;
         }
-        ++qcount;
-        new_qb = false;
-        if constexpr (NTOK == 1) {
-          const float4* wsrc = reinterpret_cast<const float4*>(smem + C::kOffW + qs * C::kWBytes);
+        tc_fence_after();
+        const float kscale = reinterpret_cast<const float*>(smem + stage * C::kStageBytes + C::kScaleOff)[row];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);
+        const int key = (meta.kt0 + e) * 128 + row;
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * C::N;
 #pragma unroll
-          for (int h = 0; h < kHeads / 4; ++h) {
-            const float4 v = wsrc[h];
-            wr[4 * h] = v.x;
-            wr[4 * h + 1] = v.y;
-            wr[4 * h + 2] = v.z;
-            wr[4 * h + 3] = v.w;
-          }
-          use_hist = a.hist != nullptr && qb.t0 < a.hist_rows;
-          if (use_hist) {
-            uint4* z = reinterpret_cast<uint4*>(whist);
-            for (int b = lane; b < kHistBins / 4; b += 32) z[b] = make_uint4(0, 0, 0, 0);
-            __syncwarp();
-          }
-        }
-      }
-      if ((n % C::kEpiWG) != g) continue;
-      const int stage = n % S;
-      const int acc = n % A;
-      if (!mbar_wait(&tfull[acc], (n / A) & 1, abort_flag, a.err) ||
-          !mbar_wait(&full[stage], (n / S) & 1, abort_flag, a.err)) {
-        aborted = true;
-        break;
-      }
-      tc_fence_after();
-      const float kscale =
-          reinterpret_cast<const float*>(smem + stage * C::kStageBytes + C::kScaleOff)[row];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);
-      const int key = kt * 128 + row;
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * C::N;
-#pragma unroll
-      for (int tok = 0; tok < NTOK; ++tok) {
-        if (tok < qb.ntok) {
-          const float* wt;
-          if constexpr (NTOK == 1) {
-            wt = wr;
-          } else {
-            wt = reinterpret_cast<const float*>(smem + C::kOffW + qs * C::kWBytes) + tok * kHeads;
-          }
-          float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            float v[32];
-            tmem_ld32(tbase + tok * kHeads + half * 32, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int h = 0; h < 32; h += 2) {
-              s0 = fmaf(wt[half * 32 + h], fmaxf(v[h], 0.f), s0);
-              s1 = fmaf(wt[half * 32 + h + 1], fmaxf(v[h + 1], 0.f), s1);
-            }
-          }
-          if (key <= qb.p0 + tok && key < a.ld) {
-            const float score = (s0 + s1) * kscale;
-            a.logits[static_cast<int64_t>(qb.t0 + tok) * a.ld + key] = score;
+        for (int tok = 0; tok < NTOK; ++tok) {
+          if (tok < qb.ntok) {
+            const float* wt;
             if constexpr (NTOK == 1) {
-              if (use_hist) atomicAdd(&whist[f32_key(score) >> kHistShift], 1u);
+              wt = wr;
+            } else {
+              wt = reinterpret_cast<const float*>(smem + C::kOffW + qs * C::kWBytes) + tok * kHeads;
+            }
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              float v[32];
+              tmem_ld32(tbase + tok * kHeads + half * 32, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int h = 0; h < 32; h += 2) {
+                s0 = fmaf(wt[half * 32 + h], fmaxf(v[h], 0.f), s0);
+                s1 = fmaf(wt[half * 32 + h + 1], fmaxf(v[h + 1], 0.f), s1);
+              }
+            }
+            if (key <= qb.p0 + tok && key < a.ld) {
+              const float score = (s0 + s1) * kscale;
+              a.logits[static_cast<int64_t>(qb.t0 + tok) * a.ld + key] = score;
+              if constexpr (NTOK == 1) {
+                if (use_hist) atomicAdd(&whist[f32_key(score) >> kHistShift], 1u);
+              }
             }
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
       }
-      tc_fence_before();
+      if (!ok) break;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
-    }
-    __syncwarp();
-    if (!aborted) {
-      if (lane == 0) mbar_arrive(&qempty[qs]);
+      if (lane == 0) mbar_arrive(&qempty[qs]);  // done with this block's q / w' buffer
       if constexpr (NTOK == 1) {
-        if (use_hist) flush_hist(qb.t0);
+        if (use_hist) {  // add the nonzero bins to the row's histogram, four bins per load
+          uint32_t* dst = a.hist + static_cast<int64_t>(qb.t0) * kHistBins;
+          const uint4* src = reinterpret_cast<const uint4*>(whist);
+#pragma unroll 4
+          for (int b = lane; b < kHistBins / 4; b += 32) {
+            const uint4 v = src[b];
+            if (v.x) atomicAdd(dst + 4 * b, v.x);
+            if (v.y) atomicAdd(dst + 4 * b + 1, v.y);
+            if (v.z) atomicAdd(dst + 4 * b + 2, v.z);
+            if (v.w) atomicAdd(dst + 4 * b + 3, v.w);
+          }
+          __syncwarp();
+        }
       }
     }
   }

@@ -14,31 +14,6 @@ namespace dsa {
 
 constexpr int kPlanStage = 2048;  // requests per segment staged in shared memory
 
-__device__ int block_scan_incl(int v, int* sm, int* total) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int n = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += n;
-  }
-  if (lane == 31) sm[wid] = v;
-  __syncthreads();
-  if (wid == 0) {
-    int x = lane < nw ? sm[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int n = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += n;
-    }
-    if (lane < nw) sm[lane] = x;
-  }
-  __syncthreads();
-  const int res = v + (wid > 0 ? sm[wid - 1] : 0);
-  *total = sm[nw - 1];
-  __syncthreads();
-  return res;
-}
-
 struct PlanSmem {
   int scan[33];
   int qsl[kPlanStage + 1];
@@ -151,9 +126,8 @@ __device__ void plan_segment(const int32_t* qsl_g, const int32_t* sl_g, int r_be
 __device__ void plan_batch(const PlanArgs& p) {
   __shared__ PlanSmem S;
   if (threadIdx.x == 0 && p.qsl[p.num_decodes] != p.num_decode_tokens) flag_error(p.err, DSA_DEVERR_SEQ_RANGE);
-  // a segment without requests launches no score kernel: nothing to plan
-  if (p.num_decodes > 0)
-    plan_segment(p.qsl, p.seq_lens, 0, p.num_decodes, 1, p.num_tokens, p.bt_stride, p.grid, p.dec, p.err, S);
+  // the decode segment is planned by its score kernel; a segment without
+  // requests launches no score kernel
   if (p.num_reqs > p.num_decodes)
     plan_segment(p.qsl, p.seq_lens, p.num_decodes, p.num_reqs, 4, p.num_tokens, p.bt_stride, p.grid, p.pre, p.err,
                  S);
