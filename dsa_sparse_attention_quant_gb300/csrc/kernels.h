@@ -90,6 +90,23 @@ cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t stream);
 constexpr int kHistBins = 2048;
 constexpr int kHistShift = 21;
 
+// Optional S5 fused into the top-k output: physical ids and valid counts.
+struct TopkPhys {
+  const int32_t* block_table;
+  int64_t bt_stride;
+  int stride_rows;
+  int32_t* physical;
+  int32_t* valid_counts;  // may be nullptr
+  int32_t* err;
+};
+
+// Per decode row: out count, candidate count, finished chunks (multi-CTA
+// select), tiles scored (score kernel).
+constexpr int kRowCounters = 4;
+
+// Rows up to this many scores are staged in shared memory by the top-k.
+constexpr int kTopkRowCap = 12288;
+
 struct LogitsArgs {
   const float* w_folded;
   const uint8_t* k_cache;
@@ -106,11 +123,14 @@ struct LogitsArgs {
   const int32_t* req_id;
   int num_decodes;
   int num_dec_tokens;
+  // decode rows' top-k, selected in the score kernel by the CTA that scores a
+  // row's last tile (rows of at most kTopkRowCap keys; topk_out == nullptr: none)
+  int topk;
+  int32_t* topk_out;    // [T, topk]
+  uint32_t* counters;   // [hist_rows][kRowCounters], zeroed before; [3] = tiles scored
+  TopkPhys phys;        // phys.physical == nullptr: logical ids only
   int32_t* err;
 };
-
-// Per decode row: out count, candidate count, finished chunks, spare.
-constexpr int kRowCounters = 4;
 
 struct SelectArgs {
   const float* logits;
@@ -132,19 +152,6 @@ struct SelectArgs {
 // written by the prologue).
 cudaError_t launch_logits(int ntok_per_block, const CUtensorMap* tmap_k, const CUtensorMap* tmap_q,
                           SegmentPlan plan, const LogitsArgs& a, int num_sms, cudaStream_t stream);
-
-// Optional S5 fused into the top-k output: physical ids and valid counts.
-struct TopkPhys {
-  const int32_t* block_table;
-  int64_t bt_stride;
-  int stride_rows;
-  int32_t* physical;
-  int32_t* valid_counts;  // may be nullptr
-  int32_t* err;
-};
-
-// Rows up to this many scores are staged in shared memory by the per-row top-k.
-constexpr int kTopkRowCap = 12288;
 
 // Rows [row_begin, n_tokens): one CTA per row. Rows t < hist_rows take their
 // first radix round from hist (the score kernel's histograms; may be nullptr).

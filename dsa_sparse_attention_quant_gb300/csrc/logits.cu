@@ -18,9 +18,11 @@
 //  * Warp roles: warp 0 issues TMA (K pages, K scales, q block, w' block),
 //    warp 1 issues the MMAs, the remaining warps read TMEM and apply
 //    ReLU, the w' reduction and the K scale, and store fp32 scores.
+//  * Decode rows also get their score histogram (round 1 of the top-k radix
+//    select) and, when they fit in shared memory, their top-k: the CTA that
+//    scores a row's last tile selects it in the freed K-tile ring.
 //  * Every wait is bounded in time (DSA_DEVERR_TIMEOUT, then an orderly exit).
-#include "common.cuh"
-#include "kernels.h"
+#include "select.cuh"
 
 namespace dsa {
 
@@ -71,18 +73,22 @@ struct QMeta {
 
 // Decode query block of token t (one token per block): request, position and
 // number of 128-key tiles; 0 tiles when the request metadata is inconsistent.
-__device__ __forceinline__ int decode_block(const LogitsArgs& a, int t, QBlock* out) {
+// *first_new = position of the request's first token of this step: pages
+// below first_new / 64 hold no slot written in this step.
+__device__ __forceinline__ int decode_block(const LogitsArgs& a, int t, QBlock* out, int* first_new = nullptr) {
   const int r = __ldg(a.req_id + t);
   QBlock b{r, t, 1, 0};
-  int tiles = 0;
+  int tiles = 0, fn = 0;
   if (r >= 0 && r < a.num_decodes) {
     const int q0 = __ldg(a.qsl + r), q1 = __ldg(a.qsl + r + 1), sl = __ldg(a.seq_lens + r);
     if (t >= q0 && t < q1 && sl >= q1 - q0 && static_cast<int64_t>(sl) <= a.bt_stride * kBlock) {
-      b.p0 = sl - (q1 - q0) + (t - q0);
+      fn = sl - (q1 - q0);
+      b.p0 = fn + (t - q0);
       tiles = (b.p0 + 1 + 127) / 128;
     }
   }
   *out = b;
+  if (first_new != nullptr) *first_new = fn;
   return tiles;
 }
 
@@ -94,13 +100,21 @@ __device__ void decode_slice(const LogitsArgs& a, int* slice, int* scan) {
   const int nt = blockDim.x, tid = threadIdx.x;
   if (blockIdx.x == 0 && tid == 0 && (__ldg(a.qsl) != 0 || __ldg(a.qsl + a.num_decodes) != T))
     flag_error(a.err, DSA_DEVERR_SEQ_RANGE);
-  int total = 0, tot;
+  if (tid == 0) {
+    slice[2] = 0;
+    slice[3] = 0;
+  }
+  // pass 1: the segment's tile count (and, when the tokens fit in one chunk,
+  // each thread's exclusive prefix, so no second pass is needed)
+  int total = 0, tot, my_tiles = 0, my_prefix = 0;
   for (int c0 = 0; c0 < T; c0 += nt) {
     const int t = c0 + tid;
     QBlock b;
     const int tiles = t < T ? decode_block(a, t, &b) : 0;
     if (t < T && tiles == 0 && blockIdx.x == 0) flag_error(a.err, DSA_DEVERR_SEQ_RANGE);
-    block_scan_incl(tiles, scan, &tot);
+    const int incl = block_scan_incl(tiles, scan, &tot);
+    my_tiles = tiles;
+    my_prefix = total + incl - tiles;
     total += tot;
   }
   const int b0 = static_cast<int>(static_cast<int64_t>(total) * blockIdx.x / gridDim.x);
@@ -108,25 +122,172 @@ __device__ void decode_slice(const LogitsArgs& a, int* slice, int* scan) {
   if (tid == 0) {
     slice[0] = b0;
     slice[1] = b1;
-    slice[2] = 0;
-    slice[3] = 0;
   }
   if (b0 < b1) {
-    int carry = 0;
-    for (int c0 = 0; c0 < T; c0 += nt) {
-      const int t = c0 + tid;
-      QBlock b;
-      const int tiles = t < T ? decode_block(a, t, &b) : 0;
-      const int incl = block_scan_incl(tiles, scan, &tot);
-      const int s = carry + incl - tiles;
-      if (t < T && tiles > 0 && s <= b0 && b0 < s + tiles) {
-        slice[2] = t;
-        slice[3] = b0 - s;
+    if (T <= nt) {
+      if (tid < T && my_tiles > 0 && my_prefix <= b0 && b0 < my_prefix + my_tiles) {
+        slice[2] = tid;
+        slice[3] = b0 - my_prefix;
       }
-      carry += tot;
+    } else {
+      int carry = 0;
+      for (int c0 = 0; c0 < T; c0 += nt) {
+        const int t = c0 + tid;
+        QBlock b;
+        const int tiles = t < T ? decode_block(a, t, &b) : 0;
+        const int incl = block_scan_incl(tiles, scan, &tot);
+        const int s = carry + incl - tiles;
+        if (t < T && tiles > 0 && s <= b0 && b0 < s + tiles) {
+          slice[2] = t;
+          slice[3] = b0 - s;
+        }
+        carry += tot;
+      }
     }
   }
   __syncthreads();
+}
+
+// Shared memory of the decode top-k tail, carved from the K-tile ring once
+// every tile of the CTA is consumed.
+struct TailLayout {
+  static constexpr int kHist = 0;
+  static constexpr int kCkey = kHist + kSelBins * 4;
+  static constexpr int kCidx = kCkey + kCandCap * 4;
+  static constexpr int kOid = kCidx + kCandCap * 4;
+  static constexpr int kKeys = kOid + kMaxTopk * 4;
+  static constexpr int kBts = kKeys + kTopkRowCap * 4;
+  static constexpr int kState = kBts + kTopkRowCap / kBlock * 4;
+  static constexpr int kList = kState + static_cast<int>(sizeof(SelState));
+  static constexpr int kCtl = kList + 32 * 4;
+  static constexpr int kBytes = kCtl + 8;
+};
+
+// Decode rows of at most kTopkRowCap keys: the CTA that scores a row's last
+// tile selects the row's top-k (all of the row's scores and histogram adds are
+// complete then). Tiles of the row are counted in counters[t][3] (zeroed
+// before the launch); this CTA's tiles are the slice [j0/kt0, +items).
+template <int NT>
+__device__ void decode_topk_tail(const LogitsArgs& a, int j0, int kt0, int items, uint8_t* ring) {
+  uint32_t* hist = reinterpret_cast<uint32_t*>(ring + TailLayout::kHist);
+  uint32_t* ckey = reinterpret_cast<uint32_t*>(ring + TailLayout::kCkey);
+  uint32_t* cidx = reinterpret_cast<uint32_t*>(ring + TailLayout::kCidx);
+  uint32_t* oid = reinterpret_cast<uint32_t*>(ring + TailLayout::kOid);
+  uint32_t* keys = reinterpret_cast<uint32_t*>(ring + TailLayout::kKeys);
+  int32_t* bts = reinterpret_cast<int32_t*>(ring + TailLayout::kBts);
+  SelState& st = *reinterpret_cast<SelState*>(ring + TailLayout::kState);
+  int* list = reinterpret_cast<int*>(ring + TailLayout::kList);
+  int* ctl = reinterpret_cast<int*>(ring + TailLayout::kCtl);  // [0] rows listed, [1] walk not finished
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int T = a.num_dec_tokens;
+  bool bad = false;
+
+  // The walk over the slice's rows, 32 rows at a time by warp 0: lane L takes
+  // row t + L, its tiles in the slice come from a scan, and the lanes add them
+  // to the rows' counters at once. The barrier and warp 0's fence publish the
+  // CTA's scores and histogram adds before they are counted.
+  __syncthreads();
+  int t = j0, kt = kt0, rem = items;  // walk state (warp 0, uniform)
+  while (true) {
+    if (tid < 32) {
+      if (t == j0 && kt == kt0) __threadfence();
+      int nl = 0;
+      while (rem > 0 && t < T && nl == 0) {
+        const int row = t + lane;
+        QBlock qb;
+        const int tiles = row < T ? decode_block(a, row, &qb) : 0;
+        const int avail = max(tiles - (lane == 0 ? kt : 0), 0);
+        int incl = avail;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        const int in = min(avail, max(rem - (incl - avail), 0));
+        bool last = false;
+        if (in > 0) {
+          const uint32_t done =
+              atomicAdd(a.counters + static_cast<int64_t>(row) * kRowCounters + 3, static_cast<uint32_t>(in)) + in;
+          last = done == static_cast<uint32_t>(tiles);
+        }
+        const unsigned lm = __ballot_sync(0xffffffffu, last);
+        if (last) list[__popc(lm & ((1u << lane) - 1u))] = row;
+        nl = __popc(lm);
+        const int used = __shfl_sync(0xffffffffu, incl, 31);
+        rem -= min(used, rem);
+        t += 32;
+        kt = 0;
+      }
+      if (nl > 0) __threadfence();  // the other CTAs' scores and histogram adds of those rows are visible
+      if (lane == 0) {
+        ctl[0] = nl;
+        ctl[1] = rem > 0 && t < T;
+      }
+    }
+    __syncthreads();
+    const int nl = ctl[0];
+    const bool more = ctl[1] != 0;
+    for (int i = 0; i < nl; ++i) {
+      const int row = list[i];
+      QBlock qb;
+      decode_block(a, row, &qb);
+      const int n = static_cast<int>(min(static_cast<int64_t>(qb.p0) + 1, a.ld));
+      RowOut o;
+      o.orow = a.topk_out + static_cast<int64_t>(row) * a.topk;
+      o.prow = a.phys.physical != nullptr ? a.phys.physical + static_cast<int64_t>(row) * a.topk : nullptr;
+      o.bt_row = o.prow != nullptr ? a.phys.block_table + static_cast<int64_t>(qb.req) * a.phys.bt_stride : nullptr;
+      o.bt_stride = a.phys.bt_stride;
+      o.stride_rows = a.phys.stride_rows;
+      if (o.prow != nullptr && a.phys.valid_counts != nullptr && tid == 0)
+        a.phys.valid_counts[row] = n < a.topk ? n : a.topk;
+      if (n <= a.topk) {
+        write_short_row(n, a.topk, o, &bad);
+        continue;
+      }
+      // the row's histogram, scores and block-table row, loads issued together
+      const uint4* hrow = reinterpret_cast<const uint4*>(a.hist + static_cast<int64_t>(row) * kSelBins);
+      for (int b = tid; b < kSelBins / 4; b += NT) reinterpret_cast<uint4*>(hist)[b] = __ldcg(hrow + b);
+      if (o.prow != nullptr) {
+        const int pages = (n + kBlock - 1) / kBlock;  // <= kTopkRowCap / kBlock
+        for (int p = tid; p < pages; p += NT) bts[p] = p < a.phys.bt_stride ? __ldg(o.bt_row + p) : -1;
+        o.bt_row = bts;
+      }
+      const float4* l4 = reinterpret_cast<const float4*>(a.logits + static_cast<int64_t>(row) * a.ld);
+      const int n4 = (n + 3) >> 2;  // rows are 16-byte aligned and ld is a multiple of 4
+      for (int base = 0; base < n4; base += 8 * NT) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i4 = base + u * NT + tid;
+          v[u] = i4 < n4 ? __ldcg(l4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i4 = base + u * NT + tid;
+          if (i4 < n4) reinterpret_cast<uint4*>(keys)[i4] =
+              make_uint4(f32_key(v[u].x), f32_key(v[u].y), f32_key(v[u].z), f32_key(v[u].w));
+        }
+      }
+      __syncthreads();
+      select_row_staged<NT>(keys, n, hist, ckey, cidx, oid, a.topk, o, st, &bad);
+    }
+    __syncthreads();  // before warp 0 lists the next rows
+    if (!more) break;
+  }
+  // rows of decode tokens whose request metadata is inconsistent (already
+  // flagged) are scored by no CTA: CTA 0 fills them with -1
+  if (blockIdx.x == 0) {
+    for (int r = tid; r < T; r += NT) {
+      QBlock qb;
+      if (decode_block(a, r, &qb) > 0) continue;
+      for (int i = 0; i < a.topk; ++i) a.topk_out[static_cast<int64_t>(r) * a.topk + i] = -1;
+      if (a.phys.physical != nullptr) {
+        for (int i = 0; i < a.topk; ++i) a.phys.physical[static_cast<int64_t>(r) * a.topk + i] = -1;
+        if (a.phys.valid_counts != nullptr) a.phys.valid_counts[r] = 0;
+      }
+    }
+  }
+  if (bad) flag_error(a.err, DSA_DEVERR_ID_RANGE);
 }
 
 template <int NTOK>
@@ -181,9 +342,10 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   // This CTA's slice. Everything before pdl_wait() may overlap the previous
-  // kernel of the stream (programmatic dependent launch); the decode slice
-  // only needs the request metadata, an input of the step. The q codes, the
-  // weights, the K cache and the prefill plan are read after it.
+  // kernel of the stream (programmatic dependent launch): the decode slice
+  // needs only the request metadata, an input of the step, and the producer
+  // may already fetch K pages that hold no slot written in this step. The q
+  // codes, the weights, the new K rows and the prefill plan are read after it.
   int it_begin, it_end, j0, kt0;
   if constexpr (NTOK == 1) {
     decode_slice(a, slice, scan);
@@ -191,7 +353,6 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
     it_end = slice[1];
     j0 = slice[2];
     kt0 = slice[3];
-    pdl_wait();
   } else {
     pdl_wait();
     const CtaWork cw = plan.cta[blockIdx.x];
@@ -200,23 +361,67 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
     j0 = cw.qb0;
     kt0 = cw.kt0;
   }
-  pdl_launch_dependents();
   const int items = it_end - it_begin;  // tiles of this CTA (an empty slice runs no loop)
+  pdl_launch_dependents();
+  if constexpr (NTOK == 1) {
+    if (warp != 0) pdl_wait();  // the producer waits after its early loads
+  }
+
+  // Issue the loads of tile kt of a block (pages 2kt, 2kt+1) into a stage.
+  auto issue_tile = [&](int stage, int kt, int npages, int id0, int id1) {
+    uint8_t* st = smem + stage * C::kStageBytes;
+    const bool in1 = 2 * kt + 1 < npages;
+    const bool v0 = id0 >= 0 && id0 < a.num_blocks;
+    const bool v1 = in1 && id1 >= 0 && id1 < a.num_blocks;
+    if (!v0 || (in1 && !v1)) flag_error(a.err, DSA_DEVERR_BLOCK_RANGE);
+    mbar_arrive_expect_tx(&full[stage], (v0 ? 8192 + 256 : 0) + (v1 ? 8192 + 256 : 0));
+    if (v0) {
+      tma_load_3d(st, &tmap_k, &full[stage], 0, 0, id0);
+      bulk_load(st + C::kScaleOff, a.k_cache + static_cast<int64_t>(id0) * kPageBytes + kScaleOffset, 256,
+                &full[stage]);
+    }
+    if (v1) {
+      tma_load_3d(st + 8192, &tmap_k, &full[stage], 0, 0, id1);
+      bulk_load(st + C::kScaleOff + 256, a.k_cache + static_cast<int64_t>(id1) * kPageBytes + kScaleOffset, 256,
+                &full[stage]);
+    }
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    auto block_at = [&](int j, QBlock* qb) -> int {  // block j and its tile count
+    auto block_at = [&](int j, QBlock* qb, int* first_new) -> int {  // block j and its tile count
       if constexpr (NTOK == 1) {
-        return decode_block(a, j, qb);
+        return decode_block(a, j, qb, first_new);
       } else {
         *qb = plan.qb[j];
+        *first_new = 0;
         return plan.tile_start[j + 1] - plan.tile_start[j];
       }
     };
     int j = j0, kt = kt0, n = 0, qcount = 0;
     bool ok = true;
     QBlock qb{};
-    int block_tiles = items > 0 ? block_at(j, &qb) : 0;
+    int first_new = 0;
+    int block_tiles = items > 0 ? block_at(j, &qb, &first_new) : 0;
+    // decode: before the wait, fill the ring with tiles of the first block
+    // whose two pages lie below the first page this step writes
+    int npre = 0;
+    if constexpr (NTOK == 1) {
+      const int safe_pages = first_new / kBlock;
+      int cnt = min(min(block_tiles - kt, items), S);
+      while (cnt > 0 && 2 * (kt + cnt - 1) + 1 >= safe_pages) --cnt;
+      if (cnt > 0) {
+        const int32_t* bt_row = a.block_table + static_cast<int64_t>(qb.req) * a.bt_stride;
+        const int32_t id = lane < 2 * cnt ? __ldg(bt_row + 2 * kt + lane) : -1;
+        for (int e = 0; e < cnt; ++e) {
+          const int id0 = __shfl_sync(0xffffffffu, id, 2 * e);
+          const int id1 = __shfl_sync(0xffffffffu, id, 2 * e + 1);
+          if (lane == 0) issue_tile(e, kt + e, 2 * (kt + e) + 2, id0, id1);
+        }
+        npre = cnt;
+      }
+      pdl_wait();
+    }
     while (ok && n < items) {
       const int in_slice = min(block_tiles - kt, items - n);
       const int qs = qcount & 1;
@@ -239,6 +444,7 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
       int32_t cur_ids = p < npages ? __ldg(bt_row + p) : -1;
       int32_t nxt_ids = p + 32 < npages ? __ldg(bt_row + p + 32) : -1;
       for (int e = 0; e < in_slice; ++e, ++n, ++kt) {
+        if (n < npre) continue;  // loaded before the wait
         const int stage = n % S;
         if (lane == 0) w = mbar_wait(&empty[stage], ((n / S) & 1) ^ 1, abort_flag, a.err);
         if (!__shfl_sync(0xffffffffu, w, 0)) {
@@ -253,33 +459,17 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
         }
         const int id0 = __shfl_sync(0xffffffffu, cur_ids, (2 * kt) & 31);
         const int id1 = __shfl_sync(0xffffffffu, cur_ids, (2 * kt + 1) & 31);
-        if (lane == 0) {
-          uint8_t* st = smem + stage * C::kStageBytes;
-          const bool in1 = 2 * kt + 1 < npages;
-          const bool v0 = id0 >= 0 && id0 < a.num_blocks;
-          const bool v1 = in1 && id1 >= 0 && id1 < a.num_blocks;
-          if (!v0 || (in1 && !v1)) flag_error(a.err, DSA_DEVERR_BLOCK_RANGE);
-          mbar_arrive_expect_tx(&full[stage], (v0 ? 8192 + 256 : 0) + (v1 ? 8192 + 256 : 0));
-          if (v0) {
-            tma_load_3d(st, &tmap_k, &full[stage], 0, 0, id0);
-            bulk_load(st + C::kScaleOff, a.k_cache + static_cast<int64_t>(id0) * kPageBytes + kScaleOffset, 256,
-                      &full[stage]);
-          }
-          if (v1) {
-            tma_load_3d(st + 8192, &tmap_k, &full[stage], 0, 0, id1);
-            bulk_load(st + C::kScaleOff + 256,
-                      a.k_cache + static_cast<int64_t>(id1) * kPageBytes + kScaleOffset, 256, &full[stage]);
-          }
-        }
+        if (lane == 0) issue_tile(stage, kt, npages, id0, id1);
       }
       ++j;
       kt = 0;
-      if (ok && n < items) block_tiles = block_at(j, &qb);
+      if (ok && n < items) block_tiles = block_at(j, &qb, &first_new);
     }
     if (lane == 0 && *abort_flag) {
       // let copies already issued land before the CTA's shared memory goes away
       const unsigned long long deadline = global_ns() + kWaitLimitNs;
       for (int m = (n > S ? n - S : 0); m < n; ++m) mbar_wait_until(&full[m % S], (m / S) & 1, deadline);
+      for (int m = n; m < npre; ++m) mbar_wait_until(&full[m % S], 0, deadline);
       if (qcount > 0) mbar_wait_until(&qfull[(qcount - 1) & 1], ((qcount - 1) >> 1) & 1, deadline);
     }
   } else if (warp == 1) {
@@ -375,20 +565,18 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
             } else {
               wt = reinterpret_cast<const float*>(smem + C::kOffW + qs * C::kWBytes) + tok * kHeads;
             }
-            float s0 = 0.f, s1 = 0.f;
+            float v[kHeads];
+            tmem_ld64_sync(tbase + tok * kHeads, v);
+            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;  // four chains: the FMA latency overlaps
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              float v[32];
-              tmem_ld32(tbase + tok * kHeads + half * 32, v);
-              tmem_wait_ld();
-#pragma unroll
-              for (int h = 0; h < 32; h += 2) {
-                s0 = fmaf(wt[half * 32 + h], fmaxf(v[h], 0.f), s0);
-                s1 = fmaf(wt[half * 32 + h + 1], fmaxf(v[h + 1], 0.f), s1);
-              }
+            for (int h = 0; h < kHeads; h += 4) {
+              s0 = fmaf(wt[h], fmaxf(v[h], 0.f), s0);
+              s1 = fmaf(wt[h + 1], fmaxf(v[h + 1], 0.f), s1);
+              s2 = fmaf(wt[h + 2], fmaxf(v[h + 2], 0.f), s2);
+              s3 = fmaf(wt[h + 3], fmaxf(v[h + 3], 0.f), s3);
             }
             if (key <= qb.p0 + tok && key < a.ld) {
-              const float score = (s0 + s1) * kscale;
+              const float score = ((s0 + s1) + (s2 + s3)) * kscale;
               a.logits[static_cast<int64_t>(qb.t0 + tok) * a.ld + key] = score;
               if constexpr (NTOK == 1) {
                 if (use_hist) atomicAdd(&whist[f32_key(score) >> kHistShift], 1u);
@@ -426,6 +614,10 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+  if constexpr (NTOK == 1) {
+    static_assert(TailLayout::kBytes <= C::kStages * C::kStageBytes, "top-k tail fits in the K-tile ring");
+    if (a.topk_out != nullptr && !*abort_flag) decode_topk_tail<C::kThreads>(a, j0, kt0, items, smem);
   }
 }
 

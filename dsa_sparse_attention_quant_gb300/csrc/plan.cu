@@ -123,8 +123,7 @@ __device__ void plan_segment(const int32_t* qsl_g, const int32_t* sl_g, int r_be
   __syncthreads();
 }
 
-__device__ void plan_batch(const PlanArgs& p) {
-  __shared__ PlanSmem S;
+__device__ void plan_batch(const PlanArgs& p, PlanSmem& S) {
   if (threadIdx.x == 0 && p.qsl[p.num_decodes] != p.num_decode_tokens) flag_error(p.err, DSA_DEVERR_SEQ_RANGE);
   // the decode segment is planned by its score kernel; a segment without
   // requests launches no score kernel
@@ -139,12 +138,16 @@ __device__ void plan_batch(const PlanArgs& p) {
 // others quantise the step's K into the cache and the q rows with the weight
 // fold, one warp per 128-value row, and zero the decode rows' score
 // histograms and top-k counters.
-constexpr int kPrologueThreads = 1024;
+// 256 threads and at most 40 registers a thread, and the plan's staging in
+// dynamic shared memory (requested only when there is a plan), so prologue
+// CTAs fit beside a score-kernel CTA that starts early on the same SM.
+constexpr int kPrologueThreads = 256;
 
-__global__ void __launch_bounds__(kPrologueThreads) prologue_kernel(PrologueArgs a) {
+__global__ void __launch_bounds__(kPrologueThreads, 6) prologue_kernel(PrologueArgs a) {
+  extern __shared__ __align__(16) uint8_t plan_smem[];
   pdl_launch_dependents();  // the score kernel may start its set-up now
   if (a.plan && blockIdx.x == 0) {
-    plan_batch(a.p);
+    plan_batch(a.p, *reinterpret_cast<PlanSmem*>(plan_smem));
     return;
   }
   const int first = a.plan ? 1 : 0;
@@ -210,8 +213,10 @@ cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t stream) {
   const int64_t jobs = q_groups + (a.k_new != nullptr ? a.n_tokens : 0) + (a.hist != nullptr ? a.hist_rows : 0);
   int64_t quant = (jobs + kPrologueThreads / 32 - 1) / (kPrologueThreads / 32);  // one job per warp, if it fits
   if (quant < 1) quant = 1;
-  if (quant > 1216) quant = 1216;  // ~4 waves of 2 CTAs per SM; the rest loops
-  prologue_kernel<<<static_cast<unsigned>(quant + (a.plan ? 1 : 0)), kPrologueThreads, 0, stream>>>(a);
+  if (quant > 1216) quant = 1216;  // one wave of 8 CTAs per SM; the rest loops
+  const size_t smem = a.plan ? sizeof(PlanSmem) : 0;
+  static_assert(sizeof(PlanSmem) <= 48 * 1024, "plan staging fits the default dynamic shared memory");
+  prologue_kernel<<<static_cast<unsigned>(quant + (a.plan ? 1 : 0)), kPrologueThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,344 @@
+// select.cuh — exact per-row top-k by radix select over order-preserving
+// 32-bit keys of fp32 scores (a > b iff key(a) > key(b)), shared by the top-k
+// kernels and the decode score kernel's tail (sm_103a).
+//
+// The top-k op of "IndexCache：DeepSeek 稀疏注意力中的跨层索引复用" (atomage.cn)
+// fills a row of the shared `topk_indices_buffer` with the ids of the
+// `index_topk` highest-scoring keys, -1 past the visible keys; "vllm.v1.
+// attention.backends.mla.index_group" (`_convert_once`) gives the consumers
+// physical slots, block_table[req][id/64] * block_stride_rows + id%64. Ids are
+// emitted in no particular order.
+//
+// Round 1 bins the keys by their top 11 bits; the bin holding the k-th
+// largest key (the boundary bin) is found by a block-wide scan from the top.
+// Every key above that bin is taken in one pass while the bin's keys are
+// gathered; two more rounds (11 and 10 bits) on the gathered keys find the
+// k-th key exactly, and the keys above it plus as many equal keys as are
+// still needed are taken. The ids are collected in shared memory and written
+// out (with their physical slots) in one coalesced pass.
+#pragma once
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dsa {
+
+constexpr int kSelBins = kHistBins;  // 2048: round-1 bins = the score kernel's histograms
+constexpr int kCandCap = 4096;       // boundary-bin keys gathered in shared memory
+constexpr int kMaxTopk = 4096;       // largest k the library accepts
+
+// Scalars of one selection, in shared memory.
+struct SelState {
+  uint32_t sm[33];  // scan scratch
+  int bin;
+  uint32_t above, cnt, eq;
+};
+
+// Bin b, scanning from the top, at which the running count reaches `need`;
+// s.above = the count in bins above b. Ends with __syncthreads().
+template <int NT>
+__device__ void find_bin(const uint32_t* hist, uint32_t need, SelState& s) {
+  static_assert(NT % 32 == 0 && NT / 32 <= 32, "block size");
+  constexpr int kPer = (kSelBins + NT - 1) / NT;  // bins per thread; thread 0 holds the top bins
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, wid = tid >> 5;
+  const int hi = kSelBins - kPer * tid;  // bins [hi - kPer, hi), clipped at 0
+  uint32_t local = 0;
+#pragma unroll
+  for (int b = 0; b < kPer; ++b) local += hi - 1 - b >= 0 ? hist[hi - 1 - b] : 0u;
+  uint32_t incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) s.sm[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    uint32_t x = lane < NT / 32 ? s.sm[lane] : 0u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += v;
+    }
+    if (lane < NT / 32) s.sm[lane] = x;
+  }
+  __syncthreads();
+  incl += wid > 0 ? s.sm[wid - 1] : 0u;
+  uint32_t above = incl - local;
+  if (above < need && need <= incl) {
+    for (int b = 0; b < kPer; ++b) {
+      const uint32_t c = hi - 1 - b >= 0 ? hist[hi - 1 - b] : 0u;
+      if (above + c >= need) {
+        s.bin = hi - 1 - b;
+        s.above = above;
+        break;
+      }
+      above += c;
+    }
+  }
+  __syncthreads();
+}
+
+// Where a row's ids go: logical ids, and optionally physical slots.
+struct RowOut {
+  int32_t* orow;          // [topk] logical ids
+  int32_t* prow;          // [topk] physical slots, or nullptr
+  const int32_t* bt_row;  // the request's block-table row (global or shared memory)
+  int64_t bt_stride;
+  int stride_rows;
+};
+
+__device__ __forceinline__ void emit(const RowOut& o, uint32_t pos, int id, bool* bad) {
+  o.orow[pos] = id;
+  if (o.prow != nullptr) {
+    const int64_t page = id / kBlock;
+    const int32_t blk = page < o.bt_stride ? o.bt_row[page] : -1;
+    if (blk < 0) *bad = true;
+    o.prow[pos] = blk < 0 ? -1 : blk * o.stride_rows + id % kBlock;
+  }
+}
+
+// Rows with at most k visible keys: every key, then -1.
+__device__ __forceinline__ void write_short_row(int n, int topk, const RowOut& o, bool* bad) {
+  for (int i = threadIdx.x; i < topk; i += blockDim.x) {
+    if (i < n) {
+      emit(o, i, i, bad);
+    } else {
+      o.orow[i] = -1;
+      if (o.prow != nullptr) o.prow[i] = -1;
+    }
+  }
+}
+
+// Warp-aggregated slot reservation: lanes with `take` get consecutive slots of *ctr.
+__device__ __forceinline__ uint32_t warp_reserve(bool take, uint32_t* ctr) {
+  const unsigned mask = __ballot_sync(0xffffffffu, take);
+  if (mask == 0) return 0;
+  const int lane = threadIdx.x & 31;
+  const int leader = __ffs(mask) - 1;
+  uint32_t base = 0;
+  if (lane == leader) base = atomicAdd(ctr, static_cast<uint32_t>(__popc(mask)));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  return base + static_cast<uint32_t>(__popc(mask & ((1u << lane) - 1u)));
+}
+
+// Ids collected in shared memory go out in one coalesced pass (positions
+// never filled, which consistent histograms rule out, become -1).
+template <int NT>
+__device__ void write_ids(const uint32_t* oid, int topk, const RowOut& o, bool* bad) {
+  for (int i = threadIdx.x; i < topk; i += NT) {
+    const int id = static_cast<int>(oid[i]);
+    if (id >= 0) {
+      emit(o, static_cast<uint32_t>(i), id, bad);
+    } else {
+      o.orow[i] = -1;
+      if (o.prow != nullptr) o.prow[i] = -1;
+    }
+  }
+}
+
+// Rounds 2 and 3 on the boundary bin b1's keys cand_key(0..m) (ids cand_id),
+// of which `need` are still to be taken after the n_up keys above the bin;
+// the keys above the k-th and as many ties as needed are appended to oid
+// from position n_up. hist holds round 1 on entry and is reused.
+template <int NT, typename CandKey, typename CandId>
+__device__ void resolve_boundary(CandKey cand_key, CandId cand_id, uint32_t m, uint32_t b1, uint32_t need,
+                                 uint32_t n_up, uint32_t* hist, uint32_t* oid, int topk, SelState& s) {
+  const int tid = threadIdx.x;
+  uint32_t prefix = b1;
+  int shift = kHistShift;
+  constexpr int kShifts[2] = {10, 0};
+  constexpr int kWidths[2] = {11, 10};
+  if (hist[b1] != need) {  // else the whole bin is taken
+    for (int lvl = 0; lvl < 2; ++lvl) {
+      const uint32_t mask = (1u << kWidths[lvl]) - 1u;
+      __syncthreads();
+      for (int b = tid; b < kSelBins; b += NT) hist[b] = 0;
+      if (tid == 0) {
+        s.bin = 0;
+        s.above = 0;
+      }
+      __syncthreads();
+      for (uint32_t j = tid; j < m; j += NT) {
+        const uint32_t k = cand_key(j);
+        if ((k >> shift) == prefix) atomicAdd(&hist[(k >> kShifts[lvl]) & mask], 1u);
+      }
+      __syncthreads();
+      find_bin<NT>(hist, need, s);
+      const int b = s.bin;
+      need -= s.above;
+      prefix = (prefix << kWidths[lvl]) | static_cast<uint32_t>(b);
+      shift = kShifts[lvl];
+      if (hist[b] == need) break;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    s.cnt = n_up;
+    s.eq = 0;
+  }
+  __syncthreads();
+  for (uint32_t j0 = 0; j0 < m; j0 += NT) {
+    const uint32_t j = j0 + tid;
+    const uint32_t k = j < m ? cand_key(j) : 0u;
+    const bool in_bin = j < m && (k >> kHistShift) == b1;  // row fallback: only the boundary bin
+    const uint32_t pk = k >> shift;
+    const bool up = in_bin && pk > prefix;
+    const bool tie = in_bin && pk == prefix;
+    const uint32_t tq = warp_reserve(tie, &s.eq);
+    const bool take = up || (tie && tq < need);
+    const uint32_t pos = warp_reserve(take, &s.cnt);
+    if (take && pos < static_cast<uint32_t>(topk)) oid[pos] = cand_id(j);
+  }
+  __syncthreads();
+}
+
+// Top `topk` of the n > topk keys key_at(0..n) of one row (read from L2),
+// written through o. Warp w owns a contiguous chunk of the row: it counts,
+// a scan over the warps gives each its offsets, and it places its keys in
+// order, so the reads stay coalesced. hist (shared, kSelBins) holds the
+// keys' round-1 histogram on entry; ckey / cidx (shared, kCandCap each) take
+// the boundary bin's keys; oid (shared, topk) collects the ids.
+template <int NT, typename KeyAt>
+__device__ void select_row(KeyAt key_at, int n, uint32_t* hist, uint32_t* ckey, uint32_t* cidx, uint32_t* oid,
+                           int topk, const RowOut& o, SelState& s, bool* bad) {
+  constexpr int kWarps = NT / 32;
+  static_assert(kWarps <= 16, "per-warp counts use s.sm[0..16) and s.sm[16..32)");
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, wid = tid >> 5;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  if (tid == 0) {
+    s.bin = 0;
+    s.above = 0;
+  }
+  for (int i = tid; i < topk; i += NT) oid[i] = 0xffffffffu;
+  __syncthreads();
+  find_bin<NT>(hist, static_cast<uint32_t>(topk), s);
+  const uint32_t b1 = static_cast<uint32_t>(s.bin);
+  const uint32_t n_up = s.above;
+  const bool gather = hist[b1] <= static_cast<uint32_t>(kCandCap);
+
+  const int per = ((n + kWarps - 1) / kWarps + 31) & ~31;
+  const int lo = wid * per, hi = min(n, lo + per);
+  uint32_t c_up = 0, c_eq = 0;
+  for (int i0 = lo; i0 < hi; i0 += 32) {
+    const int i = i0 + lane;
+    const uint32_t bin = i < hi ? key_at(i) >> kHistShift : 0u;
+    c_up += __popc(__ballot_sync(0xffffffffu, i < hi && bin > b1));
+    c_eq += __popc(__ballot_sync(0xffffffffu, i < hi && bin == b1));
+  }
+  if (lane == 0) {
+    s.sm[wid] = c_up;
+    s.sm[16 + wid] = c_eq;
+  }
+  __syncthreads();
+  uint32_t p_up = 0, p_eq = 0, total_eq = 0;
+#pragma unroll
+  for (int v = 0; v < kWarps; ++v) {
+    const uint32_t u = s.sm[v], e = s.sm[16 + v];
+    if (v < wid) {
+      p_up += u;
+      p_eq += e;
+    }
+    total_eq += e;
+  }
+  for (int i0 = lo; i0 < hi; i0 += 32) {
+    const int i = i0 + lane;
+    const uint32_t key = i < hi ? key_at(i) : 0u;
+    const uint32_t bin = key >> kHistShift;
+    const bool up = i < hi && bin > b1;
+    const bool eq = i < hi && bin == b1;
+    const uint32_t m_up = __ballot_sync(0xffffffffu, up);
+    const uint32_t m_eq = __ballot_sync(0xffffffffu, eq);
+    const uint32_t q_up = p_up + __popc(m_up & lt_mask);
+    const uint32_t q_eq = p_eq + __popc(m_eq & lt_mask);
+    if (up && q_up < static_cast<uint32_t>(topk)) oid[q_up] = static_cast<uint32_t>(i);
+    if (gather && eq && q_eq < static_cast<uint32_t>(kCandCap)) {
+      ckey[q_eq] = key;
+      cidx[q_eq] = static_cast<uint32_t>(i);
+    }
+    p_up += __popc(m_up);
+    p_eq += __popc(m_eq);
+  }
+  __syncthreads();
+  // the boundary bin: candidates j < m (or, past kCandCap, the row filtered to the bin)
+  const uint32_t m = gather ? min(total_eq, static_cast<uint32_t>(kCandCap)) : static_cast<uint32_t>(n);
+  resolve_boundary<NT>([&](uint32_t j) -> uint32_t { return gather ? ckey[j] : key_at(static_cast<int>(j)); },
+                       [&](uint32_t j) -> uint32_t { return gather ? cidx[j] : j; }, m, b1,
+                       static_cast<uint32_t>(topk) - n_up, n_up, hist, oid, topk, s);
+  write_ids<NT>(oid, topk, o, bad);
+  __syncthreads();
+}
+
+// Top `topk` of the kTopkRowCap >= n > topk keys staged in shared memory
+// (keys, 16-byte aligned), written through o. Thread i owns a contiguous
+// range of 4*q keys (q odd: the 16-byte loads of a warp hit distinct banks);
+// one block scan of the packed counts gives every thread its offsets.
+template <int NT>
+__device__ void select_row_staged(const uint32_t* keys, int n, uint32_t* hist, uint32_t* ckey, uint32_t* cidx,
+                                  uint32_t* oid, int topk, const RowOut& o, SelState& s, bool* bad) {
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    s.bin = 0;
+    s.above = 0;
+  }
+  for (int i = tid; i < topk; i += NT) oid[i] = 0xffffffffu;
+  __syncthreads();
+  find_bin<NT>(hist, static_cast<uint32_t>(topk), s);
+  const uint32_t b1 = static_cast<uint32_t>(s.bin);
+  const uint32_t n_up = s.above;
+  const bool gather = hist[b1] <= static_cast<uint32_t>(kCandCap);
+
+  int q4 = ((n + NT - 1) / NT + 3) >> 2;
+  q4 += (q4 & 1) ^ 1;  // odd
+  const int lo = tid * 4 * q4, hi = min(n, lo + 4 * q4);
+  const uint4* k4 = reinterpret_cast<const uint4*>(keys);
+  int c_up = 0, c_eq = 0;
+  for (int i = lo; i < hi; i += 4) {
+    const uint4 v = k4[i >> 2];
+    const uint32_t kk[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t bin = kk[c] >> kHistShift;
+      const bool in = i + c < hi;
+      c_up += in && bin > b1;
+      c_eq += in && bin == b1;
+    }
+  }
+  // counts <= kTopkRowCap < 2^16: up in the high half, boundary-bin keys in the low
+  int total;
+  const int packed = (c_up << 16) | c_eq;
+  const int excl = block_scan_incl(packed, reinterpret_cast<int*>(s.sm), &total) - packed;
+  uint32_t p_up = static_cast<uint32_t>(excl) >> 16, p_eq = static_cast<uint32_t>(excl) & 0xffffu;
+  const uint32_t total_eq = static_cast<uint32_t>(total) & 0xffffu;
+  for (int i = lo; i < hi; i += 4) {
+    const uint4 v = k4[i >> 2];
+    const uint32_t kk[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t bin = kk[c] >> kHistShift;
+      if (i + c < hi) {
+        if (bin > b1) {
+          if (p_up < static_cast<uint32_t>(topk)) oid[p_up] = static_cast<uint32_t>(i + c);
+          ++p_up;
+        } else if (bin == b1 && gather) {
+          if (p_eq < static_cast<uint32_t>(kCandCap)) {
+            ckey[p_eq] = kk[c];
+            cidx[p_eq] = static_cast<uint32_t>(i + c);
+          }
+          ++p_eq;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const uint32_t m = gather ? min(total_eq, static_cast<uint32_t>(kCandCap)) : static_cast<uint32_t>(n);
+  resolve_boundary<NT>([&](uint32_t j) -> uint32_t { return gather ? ckey[j] : keys[j]; },
+                       [&](uint32_t j) -> uint32_t { return gather ? cidx[j] : j; }, m, b1,
+                       static_cast<uint32_t>(topk) - n_up, n_up, hist, oid, topk, s);
+  write_ids<NT>(oid, topk, o, bad);
+  __syncthreads();
+}
+
+}  // namespace dsa
