@@ -213,15 +213,12 @@ def run_ours(args):
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     layers = [[dict(q=r.q, w=r.w, k_new=r.k_new, k_cache=r.k_cache)] for r in reps]
     # per step: fused prologue (S1 K quant + cache write, S2a q quant + fold, plan),
-    # the score kernel(s) (S2b), top-k with the id conversion fused (S3 + S5).
-    # Decode rows of at most 12288 keys are selected inside the decode score
-    # kernel; longer ones by the multi-CTA select kernel.
+    # the score kernel(s) (S2b), top-k with the id conversion fused (S3 + S5):
+    # the multi-CTA select for the decode rows, one CTA per prefill row
     has_dec = hb.num_decodes > 0
     has_pre = hb.num_reqs > hb.num_decodes
-    ld = (int(hb.seq_lens.max()) + 3) // 4 * 4 if hb.num_reqs else 4
-    fused = ld <= 12288
     kernels = ["prologue"] + (["logits<1>"] if has_dec else []) + (["logits<4>"] if has_pre else []) + \
-        (["select"] if has_dec and not fused else []) + (["topk"] if has_pre else [])
+        (["select"] if has_dec else []) + (["topk"] if has_pre else [])
     launches_per_step = len(kernels)
 
     def step(i, ev=None):
@@ -366,9 +363,7 @@ def run_ours(args):
         algo_bytes = pairs * (132 + 4) + T * (64 * 128 + 64 * 4)
         achieved = algo_bytes / (kernel_avg_ms / 1e3) / 1e9
         roofline = {
-            "bound": "hbm",
-            "kernel": "dsa::logits_kernel<1> (decode scores, tcgen05 FP8"
-                      + (", with the rows' top-k selection)" if fused else ")"),
+            "bound": "hbm", "kernel": "dsa::logits_kernel<1> (decode scores, tcgen05 FP8)",
             "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
             "traffic": traffic, "algorithmic_bytes_per_launch": algo_bytes,
             "peak_source": f"{peak_src}: MEASURED_PEAKS.json hbm_gbs (copy bandwidth)",

@@ -204,15 +204,10 @@ int launched(cudaError_t e, cudaStream_t stream) {
   return st != DSA_OK ? st : mark(stream);
 }
 
-// Whether the decode score kernel selects the decode rows' top-k itself.
-bool decode_topk_fused(int64_t ld) { return ld <= kTopkRowCap; }
-
 // Scores for both segments (the prefill plan is already in ws). With `hist`,
-// the decode kernel also accumulates the decode rows' histograms (zeroed
-// before) and, with `topk_out` and rows that fit, selects their top-k.
+// the decode kernel also accumulates the decode rows' histograms (zeroed before).
 int run_logits(const DsaBatch* b, const uint8_t* q_fp8, const float* w_folded, const uint8_t* k_cache,
-               float* logits, int64_t ld, const IndexerWs& ws, bool hist, int32_t topk, int32_t* topk_out,
-               const TopkPhys* phys, int32_t* dev_err, cudaStream_t stream) {
+               float* logits, int64_t ld, const IndexerWs& ws, bool hist, int32_t* dev_err, cudaStream_t stream) {
   if (b->num_tokens == 0) return DSA_OK;
   int sms = 0;
   int st = device_sms(&sms);
@@ -222,13 +217,7 @@ int run_logits(const DsaBatch* b, const uint8_t* q_fp8, const float* w_folded, c
   LogitsArgs a{w_folded,          k_cache,    b->block_table,   b->bt_stride,   b->num_blocks,
                logits,            ld,         hist ? ws.hist : nullptr,          hist ? ws.hist_rows : 0,
                b->query_start_loc, b->seq_lens, b->req_id_per_token, b->num_decodes, b->num_decode_tokens,
-               0,                 nullptr,    nullptr,          TopkPhys{},     dev_err};
-  if (hist && topk_out != nullptr && decode_topk_fused(ld)) {
-    a.topk = topk;
-    a.topk_out = topk_out;
-    a.counters = ws.counters;
-    if (phys != nullptr) a.phys = *phys;
-  }
+               dev_err};
   if (b->num_decodes > 0) {
     if ((st = make_q_map(&mq1, q_fp8, b->num_tokens, kHeads)) != DSA_OK) return st;
     if ((st = launched(launch_logits(1, &mk, &mq1, SegmentPlan{}, a, grid_ctas(sms), stream), stream)) != DSA_OK) return st;
@@ -240,23 +229,15 @@ int run_logits(const DsaBatch* b, const uint8_t* q_fp8, const float* w_folded, c
   return DSA_OK;
 }
 
-// Top-k of the rows the score kernel did not select, from scores built with
-// the decode rows' histograms. Rows that fit in shared memory: the decode
-// rows were selected by the score kernel; one CTA per prefill row. Longer
-// rows: the multi-CTA select for the decode rows, one CTA per row for the
-// others.
+// Top-k of every row from scores built with the decode rows' histograms:
+// the decode rows by the multi-CTA select (chunks of each row in parallel,
+// round 1 from the histograms), the others by one CTA per row.
 int run_topk(const DsaBatch* b, const IndexerWs& ws, int64_t ld, int32_t topk, int32_t* out, const TopkPhys* phys,
-             cudaStream_t stream) {
-  if (decode_topk_fused(ld)) {
-    if (b->num_tokens <= ws.hist_rows) return DSA_OK;
-    return launched(launch_topk(ws.logits, ld, b->query_start_loc, b->seq_lens, b->req_id_per_token, b->num_reqs,
-                                ws.hist_rows, b->num_tokens, topk, out, phys, nullptr, 0, stream),
-                    stream);
-  }
+             int sms, cudaStream_t stream) {
   SelectArgs sa{ws.logits, ld, b->query_start_loc, b->seq_lens, b->req_id_per_token, b->num_reqs,
                 ws.hist_rows, topk, out, ws.hist, ws.counters, ws.cand};
   int st = DSA_OK;
-  if (ws.hist_rows > 0 && (st = launched(launch_select(sa, phys, stream), stream)) != DSA_OK) return st;
+  if (ws.hist_rows > 0 && (st = launched(launch_select(sa, phys, sms, stream), stream)) != DSA_OK) return st;
   if (b->num_tokens > ws.hist_rows)
     st = launched(launch_topk(ws.logits, ld, b->query_start_loc, b->seq_lens, b->req_id_per_token, b->num_reqs,
                               ws.hist_rows, b->num_tokens, topk, out, phys, nullptr, 0, stream),
@@ -355,8 +336,7 @@ int dsa_indexer_logits(const DsaBatch* batch, const uint8_t* q_fp8, const float*
   if (!aligned16(q_fp8) || !aligned16(w_folded) || !aligned16(k_cache) || !aligned16(ws)) return DSA_EINVAL;
   IndexerWs w = carve(batch, ws);
   if (ws_bytes < w.bytes) return DSA_ENOSPACE;
-  return run_logits(batch, q_fp8, w_folded, k_cache, logits, logits_ld, w, false, 0, nullptr, nullptr, dev_err,
-                    stream);
+  return run_logits(batch, q_fp8, w_folded, k_cache, logits, logits_ld, w, false, dev_err, stream);
 }
 
 int dsa_indexer_topk(const DsaBatch* batch, const float* logits, int64_t logits_ld, int32_t topk, int32_t* topk_out,
@@ -396,9 +376,9 @@ int dsa_indexer_logits_topk(const DsaBatch* batch, const uint8_t* q_fp8, const f
   st = launched(launch_prologue(plan_only(batch, w, sms, k_new, slot_mapping, k_cache, dev_err), stream), stream);
   if (st != DSA_OK) return st;
   const int64_t ld = logits_ld(batch);
-  st = run_logits(batch, q_fp8, w_folded, k_cache, w.logits, ld, w, true, topk, topk_out, nullptr, dev_err, stream);
+  st = run_logits(batch, q_fp8, w_folded, k_cache, w.logits, ld, w, true, dev_err, stream);
   if (st != DSA_OK) return st;
-  return run_topk(batch, w, ld, topk, topk_out, nullptr, stream);
+  return run_topk(batch, w, ld, topk, topk_out, nullptr, sms, stream);
 }
 
 int dsa_topk_logical_to_physical(const int32_t* logical, int64_t n_tokens, int32_t topk,
@@ -512,9 +492,9 @@ int dsa_layer_stack_run(const DsaStackPlan* plan, const DsaBatch* batch, const i
         // S3 with S5 fused into its output pass: logical ids, physical ids, valid counts
         TopkPhys tp{batch->block_table, batch->bt_stride,
                     plan->block_stride_rows > 0 ? plan->block_stride_rows : kBlock, phys_buf, valid_buf, dev_err};
-        st = run_logits(batch, q8, wf, L.k_cache, w.logits, ld, w, true, plan->topk, topk_buf, &tp, dev_err, stream);
+        st = run_logits(batch, q8, wf, L.k_cache, w.logits, ld, w, true, dev_err, stream);
         if (st != DSA_OK) return st;
-        st = run_topk(batch, w, ld, plan->topk, topk_buf, &tp, stream);
+        st = run_topk(batch, w, ld, plan->topk, topk_buf, &tp, sms, stream);
         if (st != DSA_OK) return st;
       }
     }

@@ -100,8 +100,8 @@ struct TopkPhys {
   int32_t* err;
 };
 
-// Per decode row: out count, candidate count, finished chunks (multi-CTA
-// select), tiles scored (score kernel).
+// Per decode row (multi-CTA select): ids out, boundary-bin candidates,
+// finished chunks, spare.
 constexpr int kRowCounters = 4;
 
 // Rows up to this many scores are staged in shared memory by the top-k.
@@ -123,12 +123,6 @@ struct LogitsArgs {
   const int32_t* req_id;
   int num_decodes;
   int num_dec_tokens;
-  // decode rows' top-k, selected in the score kernel by the CTA that scores a
-  // row's last tile (rows of at most kTopkRowCap keys; topk_out == nullptr: none)
-  int topk;
-  int32_t* topk_out;    // [T, topk]
-  uint32_t* counters;   // [hist_rows][kRowCounters], zeroed before; [3] = tiles scored
-  TopkPhys phys;        // phys.physical == nullptr: logical ids only
   int32_t* err;
 };
 
@@ -160,7 +154,8 @@ cudaError_t launch_topk(const float* logits, int64_t ld, const int32_t* qsl, con
                         const TopkPhys* phys, const uint32_t* hist, int hist_rows, cudaStream_t stream);
 
 // Decode rows [0, a.n_rows) whose score histograms the score kernel built:
-// several CTAs per row, the last one of a row resolves the boundary bin.
-cudaError_t launch_select(const SelectArgs& a, const TopkPhys* phys, cudaStream_t stream);
+// each row in chunks sized so that all rows' chunks run at once, one CTA per
+// chunk; the last CTA of a row resolves its boundary bin.
+cudaError_t launch_select(const SelectArgs& a, const TopkPhys* phys, int num_sms, cudaStream_t stream);
 
 }  // namespace dsa

@@ -19,10 +19,10 @@
 //    warp 1 issues the MMAs, the remaining warps read TMEM and apply
 //    ReLU, the w' reduction and the K scale, and store fp32 scores.
 //  * Decode rows also get their score histogram (round 1 of the top-k radix
-//    select) and, when they fit in shared memory, their top-k: the CTA that
-//    scores a row's last tile selects it in the freed K-tile ring.
+//    select), so the top-k never scans a decode row to find its boundary bin.
 //  * Every wait is bounded in time (DSA_DEVERR_TIMEOUT, then an orderly exit).
-#include "select.cuh"
+#include "common.cuh"
+#include "kernels.h"
 
 namespace dsa {
 
@@ -146,148 +146,6 @@ __device__ void decode_slice(const LogitsArgs& a, int* slice, int* scan) {
     }
   }
   __syncthreads();
-}
-
-// Shared memory of the decode top-k tail, carved from the K-tile ring once
-// every tile of the CTA is consumed.
-struct TailLayout {
-  static constexpr int kHist = 0;
-  static constexpr int kCkey = kHist + kSelBins * 4;
-  static constexpr int kCidx = kCkey + kCandCap * 4;
-  static constexpr int kOid = kCidx + kCandCap * 4;
-  static constexpr int kKeys = kOid + kMaxTopk * 4;
-  static constexpr int kBts = kKeys + kTopkRowCap * 4;
-  static constexpr int kState = kBts + kTopkRowCap / kBlock * 4;
-  static constexpr int kList = kState + static_cast<int>(sizeof(SelState));
-  static constexpr int kCtl = kList + 32 * 4;
-  static constexpr int kBytes = kCtl + 8;
-};
-
-// Decode rows of at most kTopkRowCap keys: the CTA that scores a row's last
-// tile selects the row's top-k (all of the row's scores and histogram adds are
-// complete then). Tiles of the row are counted in counters[t][3] (zeroed
-// before the launch); this CTA's tiles are the slice [j0/kt0, +items).
-template <int NT>
-__device__ void decode_topk_tail(const LogitsArgs& a, int j0, int kt0, int items, uint8_t* ring) {
-  uint32_t* hist = reinterpret_cast<uint32_t*>(ring + TailLayout::kHist);
-  uint32_t* ckey = reinterpret_cast<uint32_t*>(ring + TailLayout::kCkey);
-  uint32_t* cidx = reinterpret_cast<uint32_t*>(ring + TailLayout::kCidx);
-  uint32_t* oid = reinterpret_cast<uint32_t*>(ring + TailLayout::kOid);
-  uint32_t* keys = reinterpret_cast<uint32_t*>(ring + TailLayout::kKeys);
-  int32_t* bts = reinterpret_cast<int32_t*>(ring + TailLayout::kBts);
-  SelState& st = *reinterpret_cast<SelState*>(ring + TailLayout::kState);
-  int* list = reinterpret_cast<int*>(ring + TailLayout::kList);
-  int* ctl = reinterpret_cast<int*>(ring + TailLayout::kCtl);  // [0] rows listed, [1] walk not finished
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int T = a.num_dec_tokens;
-  bool bad = false;
-
-  // The walk over the slice's rows, 32 rows at a time by warp 0: lane L takes
-  // row t + L, its tiles in the slice come from a scan, and the lanes add them
-  // to the rows' counters at once. The barrier and warp 0's fence publish the
-  // CTA's scores and histogram adds before they are counted.
-  __syncthreads();
-  int t = j0, kt = kt0, rem = items;  // walk state (warp 0, uniform)
-  while (true) {
-    if (tid < 32) {
-      if (t == j0 && kt == kt0) __threadfence();
-      int nl = 0;
-      while (rem > 0 && t < T && nl == 0) {
-        const int row = t + lane;
-        QBlock qb;
-        const int tiles = row < T ? decode_block(a, row, &qb) : 0;
-        const int avail = max(tiles - (lane == 0 ? kt : 0), 0);
-        int incl = avail;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int v = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += v;
-        }
-        const int in = min(avail, max(rem - (incl - avail), 0));
-        bool last = false;
-        if (in > 0) {
-          const uint32_t done =
-              atomicAdd(a.counters + static_cast<int64_t>(row) * kRowCounters + 3, static_cast<uint32_t>(in)) + in;
-          last = done == static_cast<uint32_t>(tiles);
-        }
-        const unsigned lm = __ballot_sync(0xffffffffu, last);
-        if (last) list[__popc(lm & ((1u << lane) - 1u))] = row;
-        nl = __popc(lm);
-        const int used = __shfl_sync(0xffffffffu, incl, 31);
-        rem -= min(used, rem);
-        t += 32;
-        kt = 0;
-      }
-      if (nl > 0) __threadfence();  // the other CTAs' scores and histogram adds of those rows are visible
-      if (lane == 0) {
-        ctl[0] = nl;
-        ctl[1] = rem > 0 && t < T;
-      }
-    }
-    __syncthreads();
-    const int nl = ctl[0];
-    const bool more = ctl[1] != 0;
-    for (int i = 0; i < nl; ++i) {
-      const int row = list[i];
-      QBlock qb;
-      decode_block(a, row, &qb);
-      const int n = static_cast<int>(min(static_cast<int64_t>(qb.p0) + 1, a.ld));
-      RowOut o;
-      o.orow = a.topk_out + static_cast<int64_t>(row) * a.topk;
-      o.prow = a.phys.physical != nullptr ? a.phys.physical + static_cast<int64_t>(row) * a.topk : nullptr;
-      o.bt_row = o.prow != nullptr ? a.phys.block_table + static_cast<int64_t>(qb.req) * a.phys.bt_stride : nullptr;
-      o.bt_stride = a.phys.bt_stride;
-      o.stride_rows = a.phys.stride_rows;
-      if (o.prow != nullptr && a.phys.valid_counts != nullptr && tid == 0)
-        a.phys.valid_counts[row] = n < a.topk ? n : a.topk;
-      if (n <= a.topk) {
-        write_short_row(n, a.topk, o, &bad);
-        continue;
-      }
-      // the row's histogram, scores and block-table row, loads issued together
-      const uint4* hrow = reinterpret_cast<const uint4*>(a.hist + static_cast<int64_t>(row) * kSelBins);
-      for (int b = tid; b < kSelBins / 4; b += NT) reinterpret_cast<uint4*>(hist)[b] = __ldcg(hrow + b);
-      if (o.prow != nullptr) {
-        const int pages = (n + kBlock - 1) / kBlock;  // <= kTopkRowCap / kBlock
-        for (int p = tid; p < pages; p += NT) bts[p] = p < a.phys.bt_stride ? __ldg(o.bt_row + p) : -1;
-        o.bt_row = bts;
-      }
-      const float4* l4 = reinterpret_cast<const float4*>(a.logits + static_cast<int64_t>(row) * a.ld);
-      const int n4 = (n + 3) >> 2;  // rows are 16-byte aligned and ld is a multiple of 4
-      for (int base = 0; base < n4; base += 8 * NT) {
-        float4 v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int i4 = base + u * NT + tid;
-          v[u] = i4 < n4 ? __ldcg(l4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int i4 = base + u * NT + tid;
-          if (i4 < n4) reinterpret_cast<uint4*>(keys)[i4] =
-              make_uint4(f32_key(v[u].x), f32_key(v[u].y), f32_key(v[u].z), f32_key(v[u].w));
-        }
-      }
-      __syncthreads();
-      select_row_staged<NT>(keys, n, hist, ckey, cidx, oid, a.topk, o, st, &bad);
-    }
-    __syncthreads();  // before warp 0 lists the next rows
-    if (!more) break;
-  }
-  // rows of decode tokens whose request metadata is inconsistent (already
-  // flagged) are scored by no CTA: CTA 0 fills them with -1
-  if (blockIdx.x == 0) {
-    for (int r = tid; r < T; r += NT) {
-      QBlock qb;
-      if (decode_block(a, r, &qb) > 0) continue;
-      for (int i = 0; i < a.topk; ++i) a.topk_out[static_cast<int64_t>(r) * a.topk + i] = -1;
-      if (a.phys.physical != nullptr) {
-        for (int i = 0; i < a.topk; ++i) a.phys.physical[static_cast<int64_t>(r) * a.topk + i] = -1;
-        if (a.phys.valid_counts != nullptr) a.phys.valid_counts[r] = 0;
-      }
-    }
-  }
-  if (bad) flag_error(a.err, DSA_DEVERR_ID_RANGE);
 }
 
 template <int NTOK>
@@ -614,10 +472,6 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
-  }
-  if constexpr (NTOK == 1) {
-    static_assert(TailLayout::kBytes <= C::kStages * C::kStageBytes, "top-k tail fits in the K-tile ring");
-    if (a.topk_out != nullptr && !*abort_flag) decode_topk_tail<C::kThreads>(a, j0, kt0, items, smem);
   }
 }
 

@@ -140,11 +140,12 @@ __device__ void write_ids(const uint32_t* oid, int topk, const RowOut& o, bool* 
 
 // Rounds 2 and 3 on the boundary bin b1's keys cand_key(0..m) (ids cand_id),
 // of which `need` are still to be taken after the n_up keys above the bin;
-// the keys above the k-th and as many ties as needed are appended to oid
-// from position n_up. hist holds round 1 on entry and is reused.
-template <int NT, typename CandKey, typename CandId>
+// the keys above the k-th and as many ties as needed go to put(position, id)
+// at positions n_up, n_up + 1, ... (below topk). hist holds round 1 of the
+// row on entry and is reused.
+template <int NT, typename CandKey, typename CandId, typename Put>
 __device__ void resolve_boundary(CandKey cand_key, CandId cand_id, uint32_t m, uint32_t b1, uint32_t need,
-                                 uint32_t n_up, uint32_t* hist, uint32_t* oid, int topk, SelState& s) {
+                                 uint32_t n_up, uint32_t* hist, Put put, int topk, SelState& s) {
   const int tid = threadIdx.x;
   uint32_t prefix = b1;
   int shift = kHistShift;
@@ -189,7 +190,7 @@ __device__ void resolve_boundary(CandKey cand_key, CandId cand_id, uint32_t m, u
     const uint32_t tq = warp_reserve(tie, &s.eq);
     const bool take = up || (tie && tq < need);
     const uint32_t pos = warp_reserve(take, &s.cnt);
-    if (take && pos < static_cast<uint32_t>(topk)) oid[pos] = cand_id(j);
+    if (take && pos < static_cast<uint32_t>(topk)) put(pos, cand_id(j));
   }
   __syncthreads();
 }
@@ -266,7 +267,8 @@ __device__ void select_row(KeyAt key_at, int n, uint32_t* hist, uint32_t* ckey, 
   const uint32_t m = gather ? min(total_eq, static_cast<uint32_t>(kCandCap)) : static_cast<uint32_t>(n);
   resolve_boundary<NT>([&](uint32_t j) -> uint32_t { return gather ? ckey[j] : key_at(static_cast<int>(j)); },
                        [&](uint32_t j) -> uint32_t { return gather ? cidx[j] : j; }, m, b1,
-                       static_cast<uint32_t>(topk) - n_up, n_up, hist, oid, topk, s);
+                       static_cast<uint32_t>(topk) - n_up, n_up, hist,
+                       [&](uint32_t pos, uint32_t id) { oid[pos] = id; }, topk, s);
   write_ids<NT>(oid, topk, o, bad);
   __syncthreads();
 }
@@ -336,7 +338,8 @@ __device__ void select_row_staged(const uint32_t* keys, int n, uint32_t* hist, u
   const uint32_t m = gather ? min(total_eq, static_cast<uint32_t>(kCandCap)) : static_cast<uint32_t>(n);
   resolve_boundary<NT>([&](uint32_t j) -> uint32_t { return gather ? ckey[j] : keys[j]; },
                        [&](uint32_t j) -> uint32_t { return gather ? cidx[j] : j; }, m, b1,
-                       static_cast<uint32_t>(topk) - n_up, n_up, hist, oid, topk, s);
+                       static_cast<uint32_t>(topk) - n_up, n_up, hist,
+                       [&](uint32_t pos, uint32_t id) { oid[pos] = id; }, topk, s);
   write_ids<NT>(oid, topk, o, bad);
   __syncthreads();
 }

@@ -14,11 +14,10 @@
 //  * topk_kernel: one CTA per row. Round 1 comes from the histogram the score
 //    kernel built when there is one, else from the row. Rows that fit are
 //    staged once in shared memory; longer rows are re-read from L2.
-//  * select_kernel: decode rows too long to stage, whose round-1 histogram
-//    the score kernel accumulated. Several CTAs per row emit the keys above
-//    the boundary bin and collect the boundary bin's keys; the last CTA of the
-//    row to finish resolves the boundary bin on those candidates only.
-// Decode rows short enough to stage are selected inside the score kernel.
+//  * select_kernel: decode rows, whose round-1 histogram the score kernel
+//    accumulated. Several CTAs per row place the keys above the boundary bin
+//    and collect the boundary bin's keys; the last CTA of the row to finish
+//    resolves the boundary bin on those candidates only.
 #include "select.cuh"
 
 namespace dsa {
@@ -185,12 +184,19 @@ cudaError_t launch_topk(const float* logits, int64_t ld, const int32_t* qsl, con
 }
 
 // ---------------------------------------------------------------------------
-// Multi-CTA select for decode rows: CTA (c, t) takes scores [c*8192, (c+1)*8192) of row t.
-__global__ void __launch_bounds__(kTopkThreads) select_kernel(SelectArgs a, PhysOut po) {
-  extern __shared__ uint32_t sh[];
-  uint32_t* hist = sh;                                       // kSelBins
-  uint2* cands = reinterpret_cast<uint2*>(sh + kSelBins);    // staged candidates (finishing CTA)
-  uint32_t* ckeys = sh + kSelBins;                           // the chunk's keys, shared with `cands`
+// Multi-CTA select for decode rows: CTA (c, t) takes scores [c*chunk,
+// (c+1)*chunk) of row t. Round 1 is the score kernel's histogram of the row,
+// so every chunk knows the boundary bin at once: it places its keys above the
+// bin (one global reservation per CTA) and its boundary-bin keys (as
+// candidates in global memory); the row's last CTA resolves the candidates.
+constexpr int kSelectThreads = 512;
+
+__global__ void __launch_bounds__(kSelectThreads) select_kernel(SelectArgs a, PhysOut po, int chunk) {
+  extern __shared__ __align__(16) uint32_t sh[];
+  uint32_t* hist = sh;              // kSelBins
+  uint32_t* keys = sh + kSelBins;   // chunk: the chunk's keys
+  uint32_t* ids = keys + chunk;     // chunk: its ids above the boundary bin, in order
+  uint2* cands = reinterpret_cast<uint2*>(keys);  // the finishing CTA: up to `chunk` candidates
   __shared__ SelState s;
   __shared__ uint32_t s_base_up, s_base_eq;
   __shared__ int s_last;
@@ -199,12 +205,12 @@ __global__ void __launch_bounds__(kTopkThreads) select_kernel(SelectArgs a, Phys
   const int c = blockIdx.x;
   const int tid = threadIdx.x;
   int r;
-  const int n = row_length(t, a.qsl, a.seq_lens, a.req_id, a.num_reqs, a.ld, &r);
+  const int n = row_length(t, a.qsl, a.seq_lens, a.req_id, a.num_reqs, a.ld, &r);  // inputs of the step
+  const RowOut o = row_out(po, a.out, a.topk, t, r, a.num_reqs);
   pdl_wait();  // the scores come from the previous kernel
   pdl_launch_dependents();
-  const int chunks = n > 0 ? (n + kSelectChunk - 1) / kSelectChunk : 1;
+  const int chunks = n > 0 ? (n + chunk - 1) / chunk : 1;
   if (c >= chunks) return;
-  const RowOut o = row_out(po, a.out, a.topk, t, r, a.num_reqs);
   bool bad = false;
   if (n <= a.topk) {
     if (c == 0) {
@@ -217,29 +223,26 @@ __global__ void __launch_bounds__(kTopkThreads) select_kernel(SelectArgs a, Phys
   if (c == 0 && o.prow != nullptr && po.valid_counts != nullptr && tid == 0) po.valid_counts[t] = a.topk;
   uint32_t* cnt = a.counters + static_cast<int64_t>(t) * kRowCounters;
   uint2* crow = a.cand + static_cast<int64_t>(t) * a.ld;
-  const float* lrow = a.logits + static_cast<int64_t>(t) * a.ld;
-  const int lo = c * kSelectChunk;
-  const int hi = min(n, lo + kSelectChunk);
+  const int lo = c * chunk;
+  const int len = min(n, lo + chunk) - lo;
 
-  // the boundary bin of round 1, from the histogram the score kernel built,
-  // and the chunk's keys: 16-byte loads, issued together
-  const uint32_t* hrow = a.hist + static_cast<int64_t>(t) * kSelBins;
-  for (int b = tid; b < kSelBins / 4; b += kTopkThreads)
-    reinterpret_cast<uint4*>(hist)[b] = __ldcg(reinterpret_cast<const uint4*>(hrow) + b);
+  // the row's histogram and the chunk's keys, loads issued together
+  const uint4* hrow = reinterpret_cast<const uint4*>(a.hist + static_cast<int64_t>(t) * kSelBins);
+  for (int b = tid; b < kSelBins / 4; b += kSelectThreads) reinterpret_cast<uint4*>(hist)[b] = __ldcg(hrow + b);
   {
-    const float4* l4 = reinterpret_cast<const float4*>(lrow + lo);  // lo is a multiple of 4
-    const int n4 = (hi - lo + 3) >> 2;
-    for (int b4 = 0; b4 < n4; b4 += 4 * kTopkThreads) {
+    const float4* l4 = reinterpret_cast<const float4*>(a.logits + static_cast<int64_t>(t) * a.ld + lo);
+    const int n4 = (len + 3) >> 2;  // lo and ld are multiples of 4
+    for (int base = 0; base < n4; base += 4 * kSelectThreads) {
       float4 v[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int i4 = b4 + u * kTopkThreads + tid;
+        const int i4 = base + u * kSelectThreads + tid;
         v[u] = i4 < n4 ? __ldcg(l4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int i4 = b4 + u * kTopkThreads + tid;
-        if (i4 < n4) reinterpret_cast<uint4*>(ckeys)[i4] =
+        const int i4 = base + u * kSelectThreads + tid;
+        if (i4 < n4) reinterpret_cast<uint4*>(keys)[i4] =
             make_uint4(f32_key(v[u].x), f32_key(v[u].y), f32_key(v[u].z), f32_key(v[u].w));
       }
     }
@@ -247,116 +250,106 @@ __global__ void __launch_bounds__(kTopkThreads) select_kernel(SelectArgs a, Phys
   if (tid == 0) {  // defaults if the histogram were inconsistent with the row
     s.bin = 0;
     s.above = 0;
-    s.cnt = 0;
-    s.eq = 0;
   }
   __syncthreads();
-  find_bin<kTopkThreads>(hist, static_cast<uint32_t>(a.topk), s);
+  find_bin<kSelectThreads>(hist, static_cast<uint32_t>(a.topk), s);
   const uint32_t b1 = static_cast<uint32_t>(s.bin);
   const uint32_t above = s.above;
 
-  // this chunk: emit keys above the boundary bin, collect the boundary bin's
-  // keys. Count in shared memory first, reserve the row slots with one global
-  // atomic per CTA, then write (no global atomics inside the loop).
-  for (int base = lo; base < hi; base += kTopkThreads) {
-    const int i = base + tid;
-    const uint32_t key = i < hi ? ckeys[i - lo] : 0u;
-    const uint32_t bin = key >> kHistShift;
-    const uint32_t n_up = __popc(__ballot_sync(0xffffffffu, i < hi && bin > b1));
-    const uint32_t n_eq = __popc(__ballot_sync(0xffffffffu, i < hi && bin == b1));
-    if ((tid & 31) == 0) {
-      if (n_up) atomicAdd(&s.cnt, n_up);
-      if (n_eq) atomicAdd(&s.eq, n_eq);
+  // thread ranges of 4*q keys (q odd), one packed scan for the offsets
+  int q4 = ((len + kSelectThreads - 1) / kSelectThreads + 3) >> 2;
+  q4 += (q4 & 1) ^ 1;
+  const int tl = tid * 4 * q4, th = min(len, tl + 4 * q4);
+  const uint4* k4 = reinterpret_cast<const uint4*>(keys);
+  int c_up = 0, c_eq = 0;
+  for (int i = tl; i < th; i += 4) {
+    const uint4 v = k4[i >> 2];
+    const uint32_t kk[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t bin = kk[u] >> kHistShift;
+      const bool in = i + u < th;
+      c_up += in && bin > b1;
+      c_eq += in && bin == b1;
+    }
+  }
+  int total;
+  const int packed = (c_up << 16) | c_eq;  // counts <= chunk <= 8192
+  const int excl = block_scan_incl(packed, reinterpret_cast<int*>(s.sm), &total) - packed;
+  const uint32_t total_up = static_cast<uint32_t>(total) >> 16, total_eq = static_cast<uint32_t>(total) & 0xffffu;
+  if (tid == 0) {
+    s_base_up = total_up ? atomicAdd(&cnt[0], total_up) : 0;
+    s_base_eq = total_eq ? atomicAdd(&cnt[1], total_eq) : 0;
+  }
+  uint32_t p_up = static_cast<uint32_t>(excl) >> 16, p_eq = static_cast<uint32_t>(excl) & 0xffffu;
+  __syncthreads();
+  const uint32_t base_eq = s_base_eq;
+  for (int i = tl; i < th; i += 4) {
+    const uint4 v = k4[i >> 2];
+    const uint32_t kk[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t bin = kk[u] >> kHistShift;
+      if (i + u < th) {
+        if (bin > b1) {
+          ids[p_up++] = static_cast<uint32_t>(lo + i + u);
+        } else if (bin == b1) {
+          if (base_eq + p_eq < static_cast<uint32_t>(a.ld))
+            crow[base_eq + p_eq] = make_uint2(kk[u], static_cast<uint32_t>(lo + i + u));
+          ++p_eq;
+        }
+      }
     }
   }
   __syncthreads();
-  if (tid == 0) {
-    s_base_up = s.cnt ? atomicAdd(&cnt[0], s.cnt) : 0;
-    s_base_eq = s.eq ? atomicAdd(&cnt[1], s.eq) : 0;
-    s.cnt = 0;
-    s.eq = 0;
-  }
-  __syncthreads();
-  for (int base = lo; base < hi; base += kTopkThreads) {
-    const int i = base + tid;
-    const uint32_t key = i < hi ? ckeys[i - lo] : 0;
-    const uint32_t bin = key >> kHistShift;
-    const bool up = i < hi && bin > b1;
-    const bool eq = i < hi && bin == b1;
-    const uint32_t p_up = s_base_up + warp_reserve(up, &s.cnt);
-    const uint32_t p_eq = s_base_eq + warp_reserve(eq, &s.eq);
-    if (up && p_up < static_cast<uint32_t>(a.topk)) emit(o, p_up, i, &bad);
-    if (eq && p_eq < static_cast<uint32_t>(a.ld)) crow[p_eq] = make_uint2(key, static_cast<uint32_t>(i));
-  }
+  // this chunk's ids above the bin, coalesced, at its reserved positions of the row
+  const uint32_t base_up = s_base_up;
+  for (uint32_t j = tid; j < total_up; j += kSelectThreads)
+    if (base_up + j < static_cast<uint32_t>(a.topk)) emit(o, base_up + j, static_cast<int>(ids[j]), &bad);
+
   // the last CTA of the row to finish resolves the boundary bin
-  __threadfence();
   __syncthreads();
-  if (tid == 0) s_last = atomicAdd(&cnt[2], 1u) == static_cast<uint32_t>(chunks - 1);
+  if (tid == 0) {
+    __threadfence();
+    s_last = atomicAdd(&cnt[2], 1u) == static_cast<uint32_t>(chunks - 1);
+    if (s_last) __threadfence();
+  }
   __syncthreads();
   if (s_last) {
-    __threadfence();
     const uint32_t m = min(__ldcg(&cnt[1]), static_cast<uint32_t>(a.ld));
-    uint32_t need = static_cast<uint32_t>(a.topk) - above;  // 1 <= need <= m
-    const bool staged = m <= kTopkRowCap / 2;
+    const bool staged = m <= static_cast<uint32_t>(chunk);
     if (staged) {
-      for (uint32_t j = tid; j < m; j += kTopkThreads) cands[j] = __ldcg(crow + j);
+      for (uint32_t j = tid; j < m; j += kSelectThreads) cands[j] = __ldcg(crow + j);
       __syncthreads();
     }
     auto cand_at = [&](uint32_t j) -> uint2 { return staged ? cands[j] : __ldcg(crow + j); };
-    uint32_t prefix = b1;
-    int shift = kHistShift;
-    constexpr int kShifts[2] = {10, 0};
-    constexpr int kWidths[2] = {11, 10};
-    for (int lvl = 0; lvl < 2; ++lvl) {
-      const uint32_t mask = (1u << kWidths[lvl]) - 1u;
-      for (int b = tid; b < kSelBins; b += kTopkThreads) hist[b] = 0;
-      if (tid == 0) {
-        s.bin = 0;
-        s.above = 0;
-      }
-      __syncthreads();
-      for (uint32_t j = tid; j < m; j += kTopkThreads) {
-        const uint32_t k = cand_at(j).x;
-        if ((k >> shift) == prefix) atomicAdd(&hist[(k >> kShifts[lvl]) & mask], 1u);
-      }
-      __syncthreads();
-      find_bin<kTopkThreads>(hist, need, s);
-      const int b = s.bin;
-      need -= s.above;
-      prefix = (prefix << kWidths[lvl]) | static_cast<uint32_t>(b);
-      shift = kShifts[lvl];
-      const bool whole = hist[b] == need;
-      __syncthreads();
-      if (whole) break;
-    }
-    if (tid == 0) s.eq = 0;
-    __syncthreads();
-    for (uint32_t j = tid; j < m; j += kTopkThreads) {
-      const uint2 kv = cand_at(j);
-      const uint32_t pk = kv.x >> shift;
-      bool take = pk > prefix;
-      if (!take && pk == prefix) take = atomicAdd(&s.eq, 1u) < need;
-      if (take) {
-        const uint32_t pos = atomicAdd(&cnt[0], 1u);
-        if (pos < static_cast<uint32_t>(a.topk)) emit(o, pos, static_cast<int>(kv.y), &bad);
-      }
-    }
+    // hist still holds the row's round 1: 1 <= need <= m
+    resolve_boundary<kSelectThreads>([&](uint32_t j) -> uint32_t { return cand_at(j).x; },
+                                     [&](uint32_t j) -> uint32_t { return cand_at(j).y; }, m, b1,
+                                     static_cast<uint32_t>(a.topk) - above, above, hist,
+                                     [&](uint32_t pos, uint32_t id) { emit(o, pos, static_cast<int>(id), &bad); },
+                                     a.topk, s);
   }
   if (bad) flag_error(po.err, DSA_DEVERR_ID_RANGE);
 }
 
-cudaError_t launch_select(const SelectArgs& a, const TopkPhys* phys, cudaStream_t stream) {
+cudaError_t launch_select(const SelectArgs& a, const TopkPhys* phys, int num_sms, cudaStream_t stream) {
   if (a.n_rows <= 0) return cudaSuccess;
-  const int smem = kSelBins * 4 + (kTopkRowCap / 2) * 8;
+  // chunks of 1024..8192 scores, the smallest that keeps every row's chunks
+  // within about two CTAs per SM
+  int chunk = 1024;
+  while (chunk < 8192 && static_cast<int64_t>(a.n_rows) * a.ld / chunk > 2 * static_cast<int64_t>(num_sms)) chunk *= 2;
+  const int max_smem = (kSelBins + 2 * 8192) * 4;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const int64_t chunks = (a.ld + kSelectChunk - 1) / kSelectChunk;
+  const int64_t chunks = (a.ld + chunk - 1) / chunk;
   dim3 grid(static_cast<unsigned>(chunks < 1 ? 1 : chunks), static_cast<unsigned>(a.n_rows));
-  return launch_pdl(select_kernel, grid, dim3(kTopkThreads), smem, stream, a, phys_out(phys));
+  return launch_pdl(select_kernel, grid, dim3(kSelectThreads), (kSelBins + 2 * chunk) * 4, stream, a, phys_out(phys),
+                    chunk);
 }
 
 }  // namespace dsa
