@@ -54,7 +54,16 @@ def workload(name: str):
                                      "shuffled pages, K quant + cache write fused with logits/top-k, top-2048")
     if name == "prefill512":
         return synth.prefill512(), "prefill512: 1 request, causal prefill of 512 tokens, RoPE inputs, top-128"
+    if name == "stack61":  # the oracle's sample: one F layer of the stack, drawn on the host
+        return synth.stack_layer(0), STACK_DESC
     raise SystemExit(f"unknown workload {name}")
+
+
+STACK_LAYERS, STACK_FREQ = 61, 4
+STACK_DESC = ("stack61: 61 DSA layers, IndexCache freq=4 (skip = max(l-1,0)%4 != 0: 16 F layers run the indexer, "
+              "45 S layers reuse the persistent top-k buffer); per F layer a mixed batch of 64 decode tokens at 32768 "
+              "context + one fresh 4096-token prefill chunk, independent per-layer K caches, top-2048; compared "
+              "with freq=1 (all 61 layers run the indexer)")
 
 
 def kernel_source_sha() -> str:
@@ -425,6 +434,240 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# --------------------------------------------------------------------- stack61
+
+def stack_inputs(meta, n_layers, dev, dsa, torch):
+    """Per-layer q, w, new K and K cache of the stack, drawn on the device.
+
+    Layer l draws from torch's CUDA generator seeded with 5000 + l (N(0,1),
+    rounded to bf16 where the path reads bf16); the metadata (lengths, block
+    table, slots) is the host generator's. Drawing 61 caches of 2M tokens on
+    the host would take minutes.
+    """
+    slots_ctx = torch.from_numpy(meta.ctx_slots).to(dev)
+    n_ctx, T = int(meta.ctx_slots.shape[0]), meta.num_tokens
+    layers = []
+    for l in range(n_layers):
+        g = torch.Generator(device=dev)
+        g.manual_seed(5000 + l)
+        cache = torch.zeros((meta.num_blocks, 8448), dtype=torch.uint8, device=dev)
+        for c0 in range(0, n_ctx, 1 << 20):
+            c1 = min(n_ctx, c0 + (1 << 20))
+            k = torch.randn((c1 - c0, 128), generator=g, device=dev).to(torch.bfloat16)
+            dsa.indexer_k_quant_write(k, slots_ctx[c0:c1], cache)
+        q = torch.randn((T, 64, 128), generator=g, device=dev).to(torch.bfloat16)
+        w = torch.randn((T, 64), generator=g, device=dev)
+        kn = torch.randn((T, 128), generator=g, device=dev).to(torch.bfloat16)
+        layers.append(dict(q=q, w=w, k_new=kn, k_cache=cache))
+    torch.cuda.synchronize()
+    return layers
+
+
+def stack_host_batch(meta, dev, torch):
+    """Layer 0 of the stack as a host batch (the same draws), for the oracle's sample."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(5000)
+    n_ctx, T = int(meta.ctx_slots.shape[0]), meta.num_tokens
+    ks = []
+    for c0 in range(0, n_ctx, 1 << 20):
+        c1 = min(n_ctx, c0 + (1 << 20))
+        ks.append(torch.randn((c1 - c0, 128), generator=g, device=dev).to(torch.bfloat16).cpu())
+    q = torch.randn((T, 64, 128), generator=g, device=dev).to(torch.bfloat16).cpu()
+    w = torch.randn((T, 64), generator=g, device=dev).cpu()
+    kn = torch.randn((T, 128), generator=g, device=dev).to(torch.bfloat16).cpu()
+    import dataclasses
+    u16 = lambda t: t.view(torch.int16).numpy().view(np.uint16)
+    return dataclasses.replace(meta, q=u16(q), w=w.numpy(), k_new=u16(kn), ctx_k=u16(torch.cat(ks)))
+
+
+def run_stack(args):
+    """The 61-layer IndexCache stack: one step = one forward through the 61
+    layers (the indexer on the F layers, the S layers reuse the buffer)."""
+    import torch
+
+    import dsa_sparse_attention_quant_gb300 as dsa
+
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1:
+        raise SystemExit("stack61 runs on one GPU")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    meta = synth.stack_layer(0, with_data=False)
+    T, k = meta.num_tokens, meta.topk
+    batch = dsa.Batch.from_host(meta, dev)
+    slots = torch.from_numpy(meta.slot_mapping).to(dev)
+    fs4, _ = dsa.schedule_build(STACK_LAYERS, True, STACK_FREQ)
+    fs1, _ = dsa.schedule_build(STACK_LAYERS, True, 1)
+    n_f = fs4.count("F")
+    layers = stack_inputs(meta, STACK_LAYERS, dev, dsa, torch)
+    l4 = [layers[l] if fs4[l] == "F" else None for l in range(STACK_LAYERS)]
+    ws = torch.empty(dsa.layer_stack_workspace_size(batch, k), dtype=torch.uint8, device=dev)
+    topk = torch.empty((T, k), dtype=torch.int32, device=dev)
+    phys = torch.empty((T, k), dtype=torch.int32, device=dev)
+    valid = torch.empty(T, dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def run(fs, L, ev=None):
+        if ev is not None:
+            dsa.binding.set_launch_events(ev)
+        dsa.layer_stack_run(batch, fs, L, k, slot_mapping=slots, topk_buf=topk, phys_buf=phys, valid_buf=valid,
+                            ws=ws, dev_err=err)
+        if ev is not None:
+            dsa.binding.set_launch_events(())
+
+    for _ in range(args.warmup):
+        run(fs4, l4)
+        run(fs1, layers)
+    torch.cuda.synchronize()
+    if dsa.check_device_error(err):
+        raise SystemExit(f"device error word set: {int(err.item()):#x}")
+
+    # one F layer alone, with a timeline event after each of its kernels
+    kernels = ["prologue", "logits<1>", "logits<4>", "select", "topk"]
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(kernels) + 1)] for _ in range(args.steps)]
+    stream = torch.cuda.current_stream()
+    for evs in kev:
+        for e in evs:
+            e.record(stream)
+    cap = torch.cuda.Stream()
+    cap.wait_stream(stream)
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            fn()
+        return g
+
+    g4 = capture(lambda: run(fs4, l4))
+    g1 = capture(lambda: run(fs1, layers))
+    one = [capture(lambda i=i: run("F", [layers[i % STACK_LAYERS]], kev[i])) for i in range(args.steps)]
+    stream.wait_stream(cap)
+    torch.cuda.synchronize()
+
+    def timed(g, steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(steps):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        t_warm = time.perf_counter()
+        while time.perf_counter() - t_warm < args.clock_window:
+            g4.replay()
+            torch.cuda.synchronize()
+        wall0 = time.perf_counter()
+        ms4 = timed(g4, args.steps)
+        wall1 = time.perf_counter()
+        ms1 = timed(g1, args.steps)
+        for g in one:
+            g.replay()
+        torch.cuda.synchronize()
+        per_kernel = np.array([[evs[j].elapsed_time(evs[j + 1]) for j in range(len(kernels))] for evs in kev])
+
+        # end to end: the F layers' q, w and new K and the step's metadata from
+        # pinned host memory, the stack, the physical ids back
+        host = [dict(q=L["q"].cpu().pin_memory(), w=L["w"].cpu().pin_memory(), k_new=L["k_new"].cpu().pin_memory())
+                if L is not None else None for L in l4]
+        meta_host = {
+            "slots": torch.from_numpy(meta.slot_mapping).pin_memory(),
+            "qsl": torch.from_numpy(meta.query_start_loc.astype(np.int32)).pin_memory(),
+            "seq": torch.from_numpy(meta.seq_lens.astype(np.int32)).pin_memory(),
+            "bt": torch.from_numpy(meta.block_table.astype(np.int32)).pin_memory(),
+            "req": torch.from_numpy(meta.req_id_per_token.astype(np.int32)).pin_memory(),
+        }
+        out_phys = torch.empty((T, k), dtype=torch.int32).pin_memory()
+        out_valid = torch.empty(T, dtype=torch.int32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for h in host if h is not None for t in h.values()) + \
+            sum(t.numel() * t.element_size() for t in meta_host.values())
+        d2h = out_phys.numel() * 4 + out_valid.numel() * 4
+
+        def e2e_step():
+            for L, h in zip(l4, host):
+                if L is None:
+                    continue
+                for name in ("q", "w", "k_new"):
+                    L[name].copy_(h[name], non_blocking=True)
+            slots.copy_(meta_host["slots"], non_blocking=True)
+            batch.query_start_loc.copy_(meta_host["qsl"], non_blocking=True)
+            batch.seq_lens.copy_(meta_host["seq"], non_blocking=True)
+            batch.block_table.copy_(meta_host["bt"], non_blocking=True)
+            batch.req_id_per_token.copy_(meta_host["req"], non_blocking=True)
+            run(fs4, l4)
+            out_phys.copy_(phys, non_blocking=True)
+            out_valid.copy_(valid, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        for _ in range(args.warmup):
+            e2e_step()
+        e0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        e2e_s = (time.perf_counter() - e0) / args.steps
+    torch.cuda.synchronize()
+    if dsa.check_device_error(err):
+        raise SystemExit(f"device error word set: {int(err.item()):#x}")
+
+    layer_pairs = meta.num_pairs()
+    pairs = n_f * layer_pairs
+    n_dec = meta.num_decodes
+    dec_pairs = int((meta.positions[:n_dec] + 1).sum())
+    pre_pairs = layer_pairs - dec_pairs
+    hbm_peak, bf16_burst, bf16_sustained, peak_src = read_peaks()
+    ms = {name: float(per_kernel[:, j].mean()) for j, name in enumerate(kernels)}
+    dec_bytes = dec_pairs * (132 + 4) + n_dec * (64 * 128 + 64 * 4)
+    dec_gbs = dec_bytes / (ms["logits<1>"] / 1e3) / 1e9
+    pre_tflops = pre_pairs * 64 * 128 * 2 / (ms["logits<4>"] / 1e3) / 1e12
+    fp8_peak = 2.0 * bf16_sustained
+    phases = {
+        "decode_scores": {"kernel": "dsa::logits_kernel<1>", "bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak,
+                          "unit": "GB/s", "frac": dec_gbs / hbm_peak, "avg_launch_ms": ms["logits<1>"]},
+        "prefill_scores": {"kernel": "dsa::logits_kernel<4>", "bound": "tensor", "achieved": pre_tflops,
+                           "peak": fp8_peak, "unit": "TFLOP/s", "frac": pre_tflops / fp8_peak,
+                           "avg_launch_ms": ms["logits<4>"]},
+    }
+    dom = "prefill_scores" if ms["logits<4>"] >= ms["logits<1>"] else "decode_scores"
+    roofline = dict(phases[dom])
+    roofline.update({"traffic": None, "phases": phases,
+                     "peak_source": f"{peak_src}: MEASURED_PEAKS.json (FP8 = 2 x bf16_tflops_sustained)",
+                     "timing": "CUDA events around each kernel of one F layer, replayed alone"})
+    line = {
+        "metric": METRIC,
+        "value": pairs / (ms4 / 1e3),
+        "unit": "pairs/s",
+        "topk_rows_per_s": n_f * T / (ms4 / 1e3),
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms4,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp8_e4m3 x fp8_e4m3 -> fp32",
+        "data": "synthetic (seeded normals, bf16-rounded; per-layer tensors from torch's seeded CUDA generator)",
+        "config": {
+            "workload": STACK_DESC,
+            "layers": STACK_LAYERS, "freq": STACK_FREQ, "f_layers": n_f,
+            "query_tokens_per_layer": T, "pairs_per_step": pairs, "topk": k,
+            "freq1_ms_per_step": ms1,
+            "freq4_speedup_vs_freq1": ms1 / ms4,
+            "l2": f"inputs larger than L2: every F layer reads its own {meta.num_blocks * 8448 / 1e6:.0f} MB K cache",
+            "parallelism": "1 GPU",
+        },
+        "roofline": roofline,
+        "breakdown_us": {name: v * 1e3 for name, v in ms.items()},
+        "e2e": {"value": pairs / e2e_s, "unit": "pairs/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_s * 1e3},
+        "gpu_launches": args.steps * sum(5 for c in fs4 if c == "F"),
+        "clocks": clocks.summary(),
+        "wall_s_timed_region": wall1 - wall0,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(stack_host_batch(meta, dev, torch), args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
 # --------------------------------------------------------------------- oracle
 
 def oracle_state(hb):
@@ -447,14 +690,16 @@ def oracle_step(ora, hb, cache, rows):
 def cpu_baseline(hb, budget_s: float):
     ora, cache = oracle_state(hb)
     T = hb.num_tokens
-    t0 = time.perf_counter()
-    oracle_step(ora, hb, cache, np.arange(min(T, 1), dtype=np.int64))
-    t_one = max(time.perf_counter() - t0, 1e-4)
-    n_rows = int(max(1, min(T, budget_s / t_one)))
-    rows = np.arange(n_rows, dtype=np.int64)
-    t0 = time.perf_counter()
-    p = oracle_step(ora, hb, cache, rows)
-    dt = time.perf_counter() - t0
+    # size the sample: grow the row count until one pass takes about the budget
+    n_rows, dt, p = 1, 0.0, 0
+    while True:
+        rows = np.arange(n_rows, dtype=np.int64)
+        t0 = time.perf_counter()
+        p = oracle_step(ora, hb, cache, rows)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s / 2 or n_rows >= T:
+            break
+        n_rows = int(min(T, max(2 * n_rows, n_rows * budget_s / max(dt, 1e-3))))
     return {"value": p / dt, "unit": "pairs/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{n_rows} of {T} query rows of the same step ({p} pairs; K write of all {T} new tokens, "
                       f"fp64 scores, full-sort top-k, conversion), {dt:.1f} s, OpenMP over rows"}
@@ -519,6 +764,8 @@ def main():
         raise SystemExit("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "stack61":
+        run_stack(args)
     else:
         run_ours(args)
 

@@ -212,6 +212,7 @@ def make_batch(
     spare_blocks: int = 0,
     bt_pad: int = 0,
     table_seed: int | None = None,
+    with_data: bool = True,
 ) -> Batch:
     """Build a seeded batch.
 
@@ -219,7 +220,9 @@ def make_batch(
     decode request.  ``prefills``: list of ``(seq_len, q_len)`` with
     ``q_len <= seq_len``; the first ``seq_len - q_len`` tokens are already in
     the cache.  Pages of all requests are drawn from one seeded permutation of
-    ``[0, num_blocks)`` unless ``identity_table``.
+    ``[0, num_blocks)`` unless ``identity_table``.  ``with_data=False`` draws
+    the metadata only: ``q``, ``w``, ``k_new`` and ``ctx_k`` keep their
+    leading dimension and have width 0.
     """
     seq = [int(x) for x in decode_seq_lens] + [int(s) for s, _ in prefills]
     qlen = [1] * len(decode_seq_lens) + [int(q) for _, q in prefills]
@@ -259,6 +262,13 @@ def make_batch(
     ctx_slots = block_table[ctx_req, ctx_positions // bs].astype(np.int64) * bs + ctx_positions % bs
     n_ctx = int(ctx_slots.shape[0])
 
+    if not with_data:
+        return Batch(
+            name=name, topk=int(topk), num_decodes=len(decode_seq_lens), seq_lens=np.asarray(seq, dtype=np.int32),
+            query_start_loc=qsl, req_id_per_token=req, positions=pos, block_table=block_table,
+            num_blocks=num_blocks, q=np.zeros((T, 0, 0), np.uint16), w=np.zeros((T, 0), np.float32),
+            k_new=np.zeros((T, 0), np.uint16), slot_mapping=slot_new, ctx_k=np.zeros((n_ctx, 0), np.uint16),
+            ctx_slots=ctx_slots)
     qf = normal(seed, STREAM_Q, T * N_HEADS * HEAD_DIM).reshape(T, N_HEADS, HEAD_DIM)
     kn = normal(seed, STREAM_K_NEW, T * HEAD_DIM).reshape(T, HEAD_DIM)
     kc = normal(seed, STREAM_K_CTX, n_ctx * HEAD_DIM).reshape(n_ctx, HEAD_DIM)
@@ -323,7 +333,7 @@ STACK_LAYERS = 61
 STACK_FREQ = 4
 
 
-def stack_layer(layer: int, scale: float = 1.0, n_decode: int = 64) -> Batch:
+def stack_layer(layer: int, scale: float = 1.0, n_decode: int = 64, with_data: bool = True) -> Batch:
     """One F layer's batch of the 61-layer stack: 64 decodes at 32768 + a 4096-token prefill.
 
     Every F layer has its own seeded q, w, new K and K cache (seed 5000+layer);
@@ -332,7 +342,8 @@ def stack_layer(layer: int, scale: float = 1.0, n_decode: int = 64) -> Batch:
     L = max(2, int(32768 * scale))
     P = max(8, int(4096 * scale))
     topk = 2048 if scale >= 1.0 else max(16, int(2048 * scale) // 4 * 4)
-    return make_batch(1000 * 5 + layer, [L] * n_decode, [(P, P)], topk, name=f"stack61.l{layer}", table_seed=5)
+    return make_batch(1000 * 5 + layer, [L] * n_decode, [(P, P)], topk, name=f"stack61.l{layer}", table_seed=5,
+                      with_data=with_data)
 
 
 WORKLOADS = {
