@@ -31,8 +31,15 @@ template <int NTOK>
 struct LogitsCfg {
   static constexpr int N = 64 * NTOK;                     // MMA N: heads x tokens
   static constexpr int kStages = NTOK == 1 ? 8 : 6;       // K-tile ring
+  // Epilogue: two teams take the tiles in turn. A decode team is one
+  // warpgroup (its scores ran no faster with more); a prefill team is two
+  // warpgroups that split a tile's four tokens, so that more warps hide the
+  // TMEM-load and FMA latency of the 64-head reduction.
+  static constexpr int kTeams = 2;
+  static constexpr int kTeamWG = NTOK == 1 ? 1 : 2;      // warpgroups per team
+  static constexpr int kEpiWG = kTeams * kTeamWG;
+  static constexpr int kTokPerWG = NTOK / kTeamWG;       // tokens of a tile one warpgroup reduces
   static constexpr int kAcc = NTOK == 1 ? 4 : 2;          // TMEM accumulator ring
-  static constexpr int kEpiWG = 2;                        // epilogue warpgroups (take tiles in turn)
   static constexpr int kEpiWarps = 4 * kEpiWG;
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr uint32_t kTmemCols = N * kAcc;         // 256 or 512
@@ -43,11 +50,11 @@ struct LogitsCfg {
   static constexpr int kOffQ = kStages * kStageBytes;
   static constexpr int kOffW = kOffQ + 2 * kQBytes;
   static constexpr int kOffBar = kOffW + 2 * kWBytes;
-  static constexpr int kNumBars = 2 * kStages + 4 + 2 * kAcc + 1;
+  static constexpr int kNumBars = 2 * kStages + 4 + 2 * kAcc + 1 + kEpiWG;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffMeta = kOffMisc + 16;  // 2 QMeta (2 x 24 B), the slice (4 ints), scan scratch (33 ints)
-  // decode: one score histogram per epilogue warp (first radix round of the top-k)
-  static constexpr int kHistBytes = NTOK == 1 ? kEpiWarps * kHistBins * 4 : 0;
+  // decode: one score histogram per epilogue warpgroup (first radix round of the top-k)
+  static constexpr int kHistBytes = NTOK == 1 ? kEpiWG * kHistBins * 4 : 0;
   static constexpr int kOffHist = (kOffMeta + 2 * 24 + 4 * 4 + 33 * 4 + 127) / 128 * 128;
   static constexpr int kSmemBytes = kOffHist + kHistBytes + 1024;  // + slack to align the base to 1024
   static constexpr uint32_t kIdesc = f8_idesc(128, N);
@@ -164,6 +171,7 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
   uint64_t* tfull = qempty + 2;
   uint64_t* tempty = tfull + A;
   uint64_t* done = tempty + A;
+  uint64_t* wgbar = done + 1;  // per epilogue warpgroup: its 4 warps meet around the histogram
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   QMeta* qmeta = reinterpret_cast<QMeta*>(smem + C::kOffMeta);
@@ -175,7 +183,7 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1 + 4);  // MMA commit + the 4 epilogue warps that read the tile's scales
+      mbar_init(&empty[s], 1 + 4 * C::kTeamWG);  // MMA commit + the tile's epilogue warps (they read its scales)
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(&qfull[q], 1);
@@ -183,9 +191,10 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
     }
     for (int c = 0; c < A; ++c) {
       mbar_init(&tfull[c], 1);
-      mbar_init(&tempty[c], 4);
+      mbar_init(&tempty[c], 4 * C::kTeamWG);
     }
     mbar_init(done, 1);
+    for (int g = 0; g < C::kEpiWG; ++g) mbar_init(&wgbar[g], 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -365,13 +374,25 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int g = (warp - 2) >> 2;        // warpgroup: takes every kEpiWG-th tile
-    const int quarter = warp & 3;         // TMEM lanes this warp may read
-    const int row = quarter * 32 + lane;  // key within the tile
-    float wr[NTOK == 1 ? kHeads : 1];
-    // decode rows: this warp's histogram of the keys of its stored scores,
-    // added to the row's global histogram when the warp leaves the row
-    uint32_t* whist = reinterpret_cast<uint32_t*>(smem + C::kOffHist) + (warp - 2) * kHistBins;
+    const int g = (warp - 2) >> 2;                     // warpgroup
+    const int team = g / C::kTeamWG;                   // takes every kTeams-th tile
+    const int tok0 = (g % C::kTeamWG) * C::kTokPerWG;  // the tokens of a tile this warpgroup reduces
+    const int quarter = warp & 3;                      // TMEM lanes this warp may read
+    const int row = quarter * 32 + lane;               // key within the tile
+    const int part = (warp - 2) & 3;                   // this warp's quarter of the group's histogram bins
+    // decode rows: the warpgroup's histogram of the keys of its stored
+    // scores, added to the row's global histogram when the group leaves the row
+    uint32_t* ghist = reinterpret_cast<uint32_t*>(smem + C::kOffHist) + g * kHistBins;
+    uint32_t hphase = 0;
+    // the group's 4 warps meet (bounded wait; false once the CTA aborts)
+    auto group_sync = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&wgbar[g]);
+      int w = 1;
+      if (lane == 0) w = mbar_wait(&wgbar[g], hphase & 1, abort_flag, a.err);
+      ++hphase;
+      return __shfl_sync(0xffffffffu, w, 0) != 0;
+    };
     int n = 0, qcount = 0;
     bool ok = true;
     while (ok && n < items) {
@@ -380,27 +401,19 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
       ++qcount;
       const QMeta meta = qmeta[qs];
       const QBlock qb = meta.qb;
+      const float* wq = reinterpret_cast<const float*>(smem + C::kOffW + qs * C::kWBytes);  // w' of the block
       bool use_hist = false;
       if constexpr (NTOK == 1) {
-        const float4* wsrc = reinterpret_cast<const float4*>(smem + C::kOffW + qs * C::kWBytes);
-#pragma unroll
-        for (int h = 0; h < kHeads / 4; ++h) {
-          const float4 v = wsrc[h];
-          wr[4 * h] = v.x;
-          wr[4 * h + 1] = v.y;
-          wr[4 * h + 2] = v.z;
-          wr[4 * h + 3] = v.w;
-        }
         use_hist = a.hist != nullptr && qb.t0 < a.hist_rows;
         if (use_hist) {
-          uint4* z = reinterpret_cast<uint4*>(whist);
-#pragma unroll 4
-          for (int b = lane; b < kHistBins / 4; b += 32) z[b] = make_uint4(0, 0, 0, 0);
-          __syncwarp();
+          uint4* z = reinterpret_cast<uint4*>(ghist) + part * (kHistBins / 16);
+#pragma unroll
+          for (int b = lane; b < kHistBins / 16; b += 32) z[b] = make_uint4(0, 0, 0, 0);
+          if (!group_sync()) break;
         }
       }
       for (int e = 0; e < meta.tiles; ++e, ++n) {
-        if ((n % C::kEpiWG) != g) continue;
+        if ((n % C::kTeams) != team) continue;
         const int stage = n % S;
         const int acc = n % A;
         if (!mbar_wait(&tfull[acc], (n / A) & 1, abort_flag, a.err) ||
@@ -415,29 +428,27 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
         const int key = (meta.kt0 + e) * 128 + row;
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * C::N;
 #pragma unroll
-        for (int tok = 0; tok < NTOK; ++tok) {
+        for (int tt = 0; tt < C::kTokPerWG; ++tt) {
+          const int tok = tok0 + tt;
           if (tok < qb.ntok) {
-            const float* wt;
-            if constexpr (NTOK == 1) {
-              wt = wr;
-            } else {
-              wt = reinterpret_cast<const float*>(smem + C::kOffW + qs * C::kWBytes) + tok * kHeads;
-            }
+            const float4* wt = reinterpret_cast<const float4*>(wq + tok * kHeads);
             float v[kHeads];
             tmem_ld64_sync(tbase + tok * kHeads, v);
-            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;  // four chains: the FMA latency overlaps
+            // four chains (heads h mod 4), two per packed fma (one issue slot
+            // for two chains' steps)
+            uint64_t s01 = 0, s23 = 0;
 #pragma unroll
             for (int h = 0; h < kHeads; h += 4) {
-              s0 = fmaf(wt[h], fmaxf(v[h], 0.f), s0);
-              s1 = fmaf(wt[h + 1], fmaxf(v[h + 1], 0.f), s1);
-              s2 = fmaf(wt[h + 2], fmaxf(v[h + 2], 0.f), s2);
-              s3 = fmaf(wt[h + 3], fmaxf(v[h + 3], 0.f), s3);
+              const float4 w4 = wt[h / 4];  // the same address across the warp: one broadcast load
+              s01 = fma_f32x2(pack_f32x2(w4.x, w4.y), pack_f32x2(fmaxf(v[h], 0.f), fmaxf(v[h + 1], 0.f)), s01);
+              s23 = fma_f32x2(pack_f32x2(w4.z, w4.w), pack_f32x2(fmaxf(v[h + 2], 0.f), fmaxf(v[h + 3], 0.f)), s23);
             }
             if (key <= qb.p0 + tok && key < a.ld) {
-              const float score = ((s0 + s1) + (s2 + s3)) * kscale;
+              const float2 p01 = unpack_f32x2(s01), p23 = unpack_f32x2(s23);
+              const float score = ((p01.x + p01.y) + (p23.x + p23.y)) * kscale;
               a.logits[static_cast<int64_t>(qb.t0 + tok) * a.ld + key] = score;
               if constexpr (NTOK == 1) {
-                if (use_hist) atomicAdd(&whist[f32_key(score) >> kHistShift], 1u);
+                if (use_hist) atomicAdd(&ghist[f32_key(score) >> kHistShift], 1u);
               }
             }
           }
@@ -450,18 +461,19 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&qempty[qs]);  // done with this block's q / w' buffer
       if constexpr (NTOK == 1) {
-        if (use_hist) {  // add the nonzero bins to the row's histogram, four bins per load
-          uint32_t* dst = a.hist + static_cast<int64_t>(qb.t0) * kHistBins;
-          const uint4* src = reinterpret_cast<const uint4*>(whist);
-#pragma unroll 4
-          for (int b = lane; b < kHistBins / 4; b += 32) {
+        if (use_hist) {  // the group's adds are done: add its nonzero bins to the row's histogram
+          if (!group_sync()) break;
+          uint32_t* dst = a.hist + static_cast<int64_t>(qb.t0) * kHistBins + part * (kHistBins / 4);
+          const uint4* src = reinterpret_cast<const uint4*>(ghist) + part * (kHistBins / 16);
+#pragma unroll
+          for (int b = lane; b < kHistBins / 16; b += 32) {
             const uint4 v = src[b];
             if (v.x) atomicAdd(dst + 4 * b, v.x);
             if (v.y) atomicAdd(dst + 4 * b + 1, v.y);
             if (v.z) atomicAdd(dst + 4 * b + 2, v.z);
             if (v.w) atomicAdd(dst + 4 * b + 3, v.w);
           }
-          __syncwarp();
+          if (!group_sync()) break;  // read before the next block zeroes it
         }
       }
     }
