@@ -2,17 +2,18 @@
 // callers that cannot allocate device memory.
 //
 // Some callers cannot call cudaMalloc or hand the library a scratch buffer:
-// code running inside a CUDA-graph capture owned by someone else, plugins that
-// only receive the tensors of an op (inputs and outputs, no allocator), and
-// latency-critical loops that must not touch the allocator. For them this
+// plugins that only receive the tensors of an op (inputs and outputs, no
+// allocator), code whose device memory belongs to a framework allocator it may
+// not call, and latency-critical loops that must not touch the allocator. For them this
 // entry point takes its scratch from one statically sized device array that
 // belongs to the library: every GPU that loads the library holds
 // kStaticWorkspaceBytes of device memory for it until the process exits.
 //
 // The array is shared by every call on a device and keeps the last call's
-// contents. Nothing in it has to start at zero: the plan kernel writes every
-// field that the later kernels read. Calls whose kernels overlap on the GPU
-// (two streams, or two host threads) race on the array; serialise them.
+// contents. Each call's first kernel (the prologue) writes the plan and clears
+// the score histograms and top-k counters before the later kernels read them.
+// Calls whose kernels overlap on the GPU (two streams, or two host threads)
+// race on the array; serialise them.
 #include <cuda_runtime.h>
 
 #include <mutex>

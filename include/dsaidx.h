@@ -90,7 +90,11 @@ DSA_API int dsa_check_device_error(const int32_t *dev_err, uint32_t *out, dsa_st
  * tokens and seq_lens[r] keys in total, this step's tokens included; query
  * token i of request r sits at position seq_lens[r] - q_len[r] + i and sees
  * keys [0, position] (causal, itself included). Key s of request r lives in
- * slot block_table[r*bt_stride + s/64]*64 + s%64 of the paged cache. */
+ * slot block_table[r*bt_stride + s/64]*64 + s%64 of the paged cache. A step
+ * writes the K of its own tokens only, at their own slots (positions
+ * [seq_lens[r] - q_len[r], seq_lens[r]) of each request), and no request
+ * reads another's pages that the step writes: the decode score kernel may
+ * fetch a request's earlier pages while this step's K write is still running. */
 typedef struct DsaBatch {
   int32_t num_reqs;          /* B >= 0 */
   int32_t num_decodes;       /* requests [0, num_decodes) are run by the decode kernel */
@@ -190,10 +194,11 @@ DSA_API int dsa_set_launch_events(void *const *events, int32_t n_events);
 
 /* dsa_indexer_logits_topk for callers that cannot allocate device memory.
  * The pages have no counterpart: this is a service of this library. Callers
- * that cannot call cudaMalloc or supply a scratch buffer — code inside a
- * CUDA-graph capture that someone else owns, plugins that are handed only an
- * op's input and output tensors, loops that must not touch an allocator — get
- * the same computation with the scratch taken from a device array of
+ * that cannot call cudaMalloc or supply a scratch buffer — plugins that are
+ * handed only an op's input and output tensors, code whose device memory
+ * belongs to a framework allocator it may not call, loops that must not touch
+ * an allocator — get the same computation with the scratch taken from a
+ * device array of
  * DSA_STATIC_WORKSPACE_BYTES inside the library. Every GPU that loads the
  * library holds that array until the process exits. Arguments are those of
  * dsa_indexer_logits_topk without ws/ws_bytes; the caller still passes all
@@ -201,12 +206,13 @@ DSA_API int dsa_set_launch_events(void *const *events, int32_t n_events);
  * allocating library call.
  *  - A batch whose dsa_indexer_workspace_size() exceeds
  *    DSA_STATIC_WORKSPACE_BYTES is rejected with DSA_ENOSPACE before any
- *    launch (32 MiB holds, e.g., the score rows of 256 decode tokens at 32K
- *    context).
+ *    launch (32 MiB holds, e.g., 83 decode tokens at 32K context or 310 at
+ *    8K: their score rows, histograms and boundary candidates).
  *  - The first call on a device looks up the array's device address (with
  *    that device current); make that first call before any stream capture.
- *  - All calls share the array and it keeps the last call's contents (nothing
- *    in it needs to start at zero). Calls whose kernels overlap on the GPU —
+ *  - All calls share the array and it keeps the last call's contents; each
+ *    call's first kernel writes the plan and clears the histograms and
+ *    counters that must start at zero. Calls whose kernels overlap on the GPU —
  *    on two streams, or from two host threads — race on it: serialise them. */
 #define DSA_STATIC_WORKSPACE_BYTES (32u << 20)
 DSA_API int dsa_indexer_logits_topk_static(const DsaBatch *batch, const uint8_t *q_fp8,

@@ -1,7 +1,7 @@
 """The allocation-free indexer entry point, dsa_indexer_logits_topk_static.
 
-It serves callers that cannot allocate device memory (inside someone else's
-graph capture, plugins handed only an op's tensors): its scratch is a static
+It serves callers that cannot allocate device memory (plugins handed only an
+op's tensors, code that may not call the allocator): its scratch is a static
 device array inside the library. Here it is called through the C ABI twice in
 a row, on two different batches, and each result is checked against the
 allocating entry point dsa_indexer_logits_topk on the same inputs, with the
