@@ -24,7 +24,7 @@
 namespace dsa {
 
 constexpr int kSelBins = kHistBins;  // 2048: round-1 bins = the score kernel's histograms
-constexpr int kCandCap = 4096;       // boundary-bin keys gathered in shared memory
+constexpr int kCandCap = 4096;       // most boundary-bin keys ever gathered in shared memory
 constexpr int kMaxTopk = 4096;       // largest k the library accepts
 
 // Scalars of one selection, in shared memory.
@@ -199,11 +199,11 @@ __device__ void resolve_boundary(CandKey cand_key, CandId cand_id, uint32_t m, u
 // written through o. Warp w owns a contiguous chunk of the row: it counts,
 // a scan over the warps gives each its offsets, and it places its keys in
 // order, so the reads stay coalesced. hist (shared, kSelBins) holds the
-// keys' round-1 histogram on entry; ckey / cidx (shared, kCandCap each) take
+// keys' round-1 histogram on entry; ckey / cidx (shared, cap each) take
 // the boundary bin's keys; oid (shared, topk) collects the ids.
 template <int NT, typename KeyAt>
 __device__ void select_row(KeyAt key_at, int n, uint32_t* hist, uint32_t* ckey, uint32_t* cidx, uint32_t* oid,
-                           int topk, const RowOut& o, SelState& s, bool* bad) {
+                           int topk, uint32_t cap, const RowOut& o, SelState& s, bool* bad) {
   constexpr int kWarps = NT / 32;
   static_assert(kWarps <= 16, "per-warp counts use s.sm[0..16) and s.sm[16..32)");
   const int tid = threadIdx.x;
@@ -218,7 +218,7 @@ __device__ void select_row(KeyAt key_at, int n, uint32_t* hist, uint32_t* ckey, 
   find_bin<NT>(hist, static_cast<uint32_t>(topk), s);
   const uint32_t b1 = static_cast<uint32_t>(s.bin);
   const uint32_t n_up = s.above;
-  const bool gather = hist[b1] <= static_cast<uint32_t>(kCandCap);
+  const bool gather = hist[b1] <= cap;
 
   const int per = ((n + kWarps - 1) / kWarps + 31) & ~31;
   const int lo = wid * per, hi = min(n, lo + per);
@@ -255,7 +255,7 @@ __device__ void select_row(KeyAt key_at, int n, uint32_t* hist, uint32_t* ckey, 
     const uint32_t q_up = p_up + __popc(m_up & lt_mask);
     const uint32_t q_eq = p_eq + __popc(m_eq & lt_mask);
     if (up && q_up < static_cast<uint32_t>(topk)) oid[q_up] = static_cast<uint32_t>(i);
-    if (gather && eq && q_eq < static_cast<uint32_t>(kCandCap)) {
+    if (gather && eq && q_eq < cap) {
       ckey[q_eq] = key;
       cidx[q_eq] = static_cast<uint32_t>(i);
     }
@@ -263,8 +263,8 @@ __device__ void select_row(KeyAt key_at, int n, uint32_t* hist, uint32_t* ckey, 
     p_eq += __popc(m_eq);
   }
   __syncthreads();
-  // the boundary bin: candidates j < m (or, past kCandCap, the row filtered to the bin)
-  const uint32_t m = gather ? min(total_eq, static_cast<uint32_t>(kCandCap)) : static_cast<uint32_t>(n);
+  // the boundary bin: candidates j < m (or, past cap, the row filtered to the bin)
+  const uint32_t m = gather ? min(total_eq, cap) : static_cast<uint32_t>(n);
   resolve_boundary<NT>([&](uint32_t j) -> uint32_t { return gather ? ckey[j] : key_at(static_cast<int>(j)); },
                        [&](uint32_t j) -> uint32_t { return gather ? cidx[j] : j; }, m, b1,
                        static_cast<uint32_t>(topk) - n_up, n_up, hist,
@@ -279,7 +279,7 @@ __device__ void select_row(KeyAt key_at, int n, uint32_t* hist, uint32_t* ckey, 
 // one block scan of the packed counts gives every thread its offsets.
 template <int NT>
 __device__ void select_row_staged(const uint32_t* keys, int n, uint32_t* hist, uint32_t* ckey, uint32_t* cidx,
-                                  uint32_t* oid, int topk, const RowOut& o, SelState& s, bool* bad) {
+                                  uint32_t* oid, int topk, uint32_t cap, const RowOut& o, SelState& s, bool* bad) {
   const int tid = threadIdx.x;
   if (tid == 0) {
     s.bin = 0;
@@ -290,7 +290,7 @@ __device__ void select_row_staged(const uint32_t* keys, int n, uint32_t* hist, u
   find_bin<NT>(hist, static_cast<uint32_t>(topk), s);
   const uint32_t b1 = static_cast<uint32_t>(s.bin);
   const uint32_t n_up = s.above;
-  const bool gather = hist[b1] <= static_cast<uint32_t>(kCandCap);
+  const bool gather = hist[b1] <= cap;
 
   int q4 = ((n + NT - 1) / NT + 3) >> 2;
   q4 += (q4 & 1) ^ 1;  // odd
@@ -325,7 +325,7 @@ __device__ void select_row_staged(const uint32_t* keys, int n, uint32_t* hist, u
           if (p_up < static_cast<uint32_t>(topk)) oid[p_up] = static_cast<uint32_t>(i + c);
           ++p_up;
         } else if (bin == b1 && gather) {
-          if (p_eq < static_cast<uint32_t>(kCandCap)) {
+          if (p_eq < cap) {
             ckey[p_eq] = kk[c];
             cidx[p_eq] = static_cast<uint32_t>(i + c);
           }
@@ -335,7 +335,7 @@ __device__ void select_row_staged(const uint32_t* keys, int n, uint32_t* hist, u
     }
   }
   __syncthreads();
-  const uint32_t m = gather ? min(total_eq, static_cast<uint32_t>(kCandCap)) : static_cast<uint32_t>(n);
+  const uint32_t m = gather ? min(total_eq, cap) : static_cast<uint32_t>(n);
   resolve_boundary<NT>([&](uint32_t j) -> uint32_t { return gather ? ckey[j] : keys[j]; },
                        [&](uint32_t j) -> uint32_t { return gather ? cidx[j] : j; }, m, b1,
                        static_cast<uint32_t>(topk) - n_up, n_up, hist,

@@ -11,7 +11,8 @@
 //
 // Both kernels are exact radix selects (select.cuh); ids are emitted in no
 // particular order.
-//  * topk_kernel: one CTA per row. Round 1 comes from the histogram the score
+//  * topk_kernel: one 256-thread CTA per row, shared memory sized to the row
+//    (several rows run per SM). Round 1 comes from the histogram the score
 //    kernel built when there is one, else from the row. Rows that fit are
 //    staged once in shared memory; longer rows are re-read from L2.
 //  * select_kernel: decode rows, whose round-1 histogram the score kernel
@@ -22,8 +23,11 @@
 
 namespace dsa {
 
-constexpr int kTopkThreads = 512;
-constexpr int kSelectChunk = 8192;  // scores per select CTA
+constexpr int kRowThreads = 256;  // topk_kernel: small CTAs, so that several rows run per SM
+// Boundary-bin keys a staged row gathers (a larger bin takes the exact
+// fallback over the row). With k = 2048 and rows of 8192 keys a CTA then
+// needs 55 KB of shared memory, and four run per SM.
+constexpr int kStagedCandCap = 768;
 
 // Visible keys of row t (clipped to ld); *req = its request.
 __device__ __forceinline__ int row_length(int t, const int32_t* qsl, const int32_t* seq_lens, const int32_t* req_id,
@@ -71,19 +75,21 @@ __device__ __forceinline__ RowOut row_out(const PhysOut& po, int32_t* out, int t
   return o;
 }
 
-// One CTA per row (rows row_begin + blockIdx.x).
+// One CTA per row (rows row_begin + blockIdx.x). Shared memory, sized by the
+// launch: the histogram, `cap` boundary-bin candidates (keys, ids), the row's
+// ids (topk, rounded up to 4) and, when staged, its keys.
 template <bool kStaged>
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restrict__ logits, int64_t ld,
-                                                            const int32_t* qsl, const int32_t* seq_lens,
-                                                            const int32_t* req_id, int num_reqs, int row_begin,
-                                                            int topk, int32_t* __restrict__ out, PhysOut po,
-                                                            const uint32_t* hist_g, int hist_rows) {
-  extern __shared__ uint32_t sh[];
+__global__ void __launch_bounds__(kRowThreads) topk_kernel(const float* __restrict__ logits, int64_t ld,
+                                                           const int32_t* qsl, const int32_t* seq_lens,
+                                                           const int32_t* req_id, int num_reqs, int row_begin,
+                                                           int topk, int32_t* __restrict__ out, PhysOut po,
+                                                           const uint32_t* hist_g, int hist_rows, int cap) {
+  extern __shared__ __align__(16) uint32_t sh[];
   uint32_t* hist = sh;
   uint32_t* ckey = sh + kSelBins;
-  uint32_t* cidx = ckey + kCandCap;
-  uint32_t* oid = cidx + kCandCap;  // kMaxTopk
-  uint32_t* keys = oid + kMaxTopk;  // kTopkRowCap, when staged
+  uint32_t* cidx = ckey + cap;
+  uint32_t* oid = cidx + cap;
+  uint32_t* keys = oid + ((topk + 3) & ~3);
   __shared__ SelState s;
   __shared__ int32_t bts[kTopkRowCap / kBlock];
 
@@ -97,7 +103,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
   if (kStaged && o.prow != nullptr && n > topk) {  // the request's block-table row, for emit
     const int cap = po.bt_stride < kTopkRowCap / kBlock ? static_cast<int>(po.bt_stride) : kTopkRowCap / kBlock;
     const int pages = min((n + kBlock - 1) / kBlock, cap);
-    for (int p = tid; p < pages; p += kTopkThreads) bts[p] = __ldg(o.bt_row + p);
+    for (int p = tid; p < pages; p += kRowThreads) bts[p] = __ldg(o.bt_row + p);
     o.bt_row = bts;
   }
   pdl_wait();  // the scores come from the previous kernel
@@ -113,24 +119,24 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
   const bool have_hist = hist_g != nullptr && t < hist_rows;
   if (have_hist) {
     const uint4* hrow = reinterpret_cast<const uint4*>(hist_g + static_cast<int64_t>(t) * kSelBins);
-    for (int b = tid; b < kSelBins / 4; b += kTopkThreads) reinterpret_cast<uint4*>(hist)[b] = __ldcg(hrow + b);
+    for (int b = tid; b < kSelBins / 4; b += kRowThreads) reinterpret_cast<uint4*>(hist)[b] = __ldcg(hrow + b);
   } else {
-    for (int b = tid; b < kSelBins; b += kTopkThreads) hist[b] = 0;
+    for (int b = tid; b < kSelBins; b += kRowThreads) hist[b] = 0;
   }
   if constexpr (kStaged) {
-    // rows are 16-byte aligned (ld is a multiple of 4): float4 loads, up to six in flight per thread
+    // rows are 16-byte aligned (ld is a multiple of 4): float4 loads, up to twelve in flight per thread
     const float4* l4 = reinterpret_cast<const float4*>(lrow);
     const int n4 = (n + 3) >> 2;
-    for (int base = 0; base < n4; base += 6 * kTopkThreads) {
-      float4 v[6];
+    for (int base = 0; base < n4; base += 12 * kRowThreads) {
+      float4 v[12];
 #pragma unroll
-      for (int u = 0; u < 6; ++u) {
-        const int i4 = base + u * kTopkThreads + tid;
+      for (int u = 0; u < 12; ++u) {
+        const int i4 = base + u * kRowThreads + tid;
         v[u] = i4 < n4 ? __ldcg(l4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
-      for (int u = 0; u < 6; ++u) {
-        const int i4 = base + u * kTopkThreads + tid;
+      for (int u = 0; u < 12; ++u) {
+        const int i4 = base + u * kRowThreads + tid;
         if (i4 < n4) reinterpret_cast<uint4*>(keys)[i4] =
             make_uint4(f32_key(v[u].x), f32_key(v[u].y), f32_key(v[u].z), f32_key(v[u].w));
       }
@@ -142,13 +148,13 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
     else return f32_key(__ldcg(lrow + i));
   };
   if (!have_hist) {
-    for (int i = tid; i < n; i += kTopkThreads) atomicAdd(&hist[key_at(i) >> kHistShift], 1u);
+    for (int i = tid; i < n; i += kRowThreads) atomicAdd(&hist[key_at(i) >> kHistShift], 1u);
     __syncthreads();
   }
   if constexpr (kStaged) {
-    select_row_staged<kTopkThreads>(keys, n, hist, ckey, cidx, oid, topk, o, s, &bad);
+    select_row_staged<kRowThreads>(keys, n, hist, ckey, cidx, oid, topk, static_cast<uint32_t>(cap), o, s, &bad);
   } else {
-    select_row<kTopkThreads>(key_at, n, hist, ckey, cidx, oid, topk, o, s, &bad);
+    select_row<kRowThreads>(key_at, n, hist, ckey, cidx, oid, topk, static_cast<uint32_t>(cap), o, s, &bad);
   }
   if (bad) flag_error(po.err, DSA_DEVERR_ID_RANGE);
 }
@@ -159,27 +165,31 @@ cudaError_t launch_topk(const float* logits, int64_t ld, const int32_t* qsl, con
   const int rows = n_tokens - row_begin;
   if (rows <= 0) return cudaSuccess;
   const PhysOut po = phys_out(phys);
-  const int base_smem = (kSelBins + 2 * kCandCap + kMaxTopk) * 4;
+  const int ids = (topk + 3) & ~3;
   if (ld <= kTopkRowCap) {
-    const int smem = base_smem + kTopkRowCap * 4;
+    const int cap = kStagedCandCap;
+    const int smem = (kSelBins + 2 * cap + ids + static_cast<int>((ld + 3) & ~3)) * 4;
     static bool configured = false;
-    if (!configured) {
-      cudaError_t e = cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (!configured) {  // the largest layout: k = kMaxTopk, ld = kTopkRowCap
+      cudaError_t e = cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (kSelBins + 2 * kStagedCandCap + kMaxTopk + kTopkRowCap) * 4);
       if (e != cudaSuccess) return e;
       configured = true;
     }
-    return launch_pdl(topk_kernel<true>, dim3(rows), dim3(kTopkThreads), smem, stream, logits, ld, qsl, seq_lens,
-                      req_id, num_reqs, row_begin, topk, out, po, hist, hist_rows);
+    return launch_pdl(topk_kernel<true>, dim3(rows), dim3(kRowThreads), smem, stream, logits, ld, qsl, seq_lens,
+                      req_id, num_reqs, row_begin, topk, out, po, hist, hist_rows, cap);
   } else {
+    const int cap = kCandCap;
+    const int smem = (kSelBins + 2 * cap + ids) * 4;
     static bool configured = false;
     if (!configured) {
-      cudaError_t e =
-          cudaFuncSetAttribute(topk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, base_smem);
+      cudaError_t e = cudaFuncSetAttribute(topk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (kSelBins + 2 * kCandCap + kMaxTopk) * 4);
       if (e != cudaSuccess) return e;
       configured = true;
     }
-    return launch_pdl(topk_kernel<false>, dim3(rows), dim3(kTopkThreads), base_smem, stream, logits, ld, qsl,
-                      seq_lens, req_id, num_reqs, row_begin, topk, out, po, hist, hist_rows);
+    return launch_pdl(topk_kernel<false>, dim3(rows), dim3(kRowThreads), smem, stream, logits, ld, qsl, seq_lens,
+                      req_id, num_reqs, row_begin, topk, out, po, hist, hist_rows, cap);
   }
 }
 

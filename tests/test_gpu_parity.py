@@ -120,6 +120,16 @@ def test_identical_keys_every_score_ties():
     check_batch(hb)
 
 
+def test_identical_keys_prefill_rows_tie():
+    # a prefill whose keys are all identical: every row's boundary bin holds
+    # the whole row, past the per-row kernel's staged candidate buffer
+    hb = synth.make_batch(14, [300], [(3000, 3000)], 256)
+    kv = hb.k_new[hb.num_decodes].copy()
+    hb.ctx_k[:] = kv
+    hb.k_new[:] = kv
+    check_batch(hb)
+
+
 def test_empty_batch():
     hb = synth.make_batch(10, [], [], 64)
     db = DeviceBatch(hb)
