@@ -5,6 +5,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 import torch
 
@@ -83,3 +84,19 @@ def test_valid_call_without_gpu_reports_no_device():
     P = ctypes.c_void_p
     st = lib.dsa_indexer_k_quant_write(P(256), 4, 128, P(256), P(256), 1, None, None)
     assert st == binding.DSA_ENODEV
+
+
+def test_ue8m0_exponent_rule_equals_division_for_every_bf16_amax():
+    # The GPU quantiser takes the ue8m0 scale from amax's exponent bits (e = E - 8,
+    # plus one when the significand exceeds 1.75) instead of dividing by 448; for
+    # every finite bf16 amax (and the 1e-10 floor) that equals the oracle's rule,
+    # RN(amax / 448) rounded up to a power of two.
+    b = np.arange(0x0000, 0x7F80, dtype=np.uint32)
+    a = np.maximum((b << 16).view(np.float32), np.float32(1e-10))
+    ref = np.array([oracle.ue8m0_scale(float(x)) for x in a[::97]], np.float32)
+    u = a.view(np.uint32)
+    rule = (((u >> 23) - 8 + ((u & 0x7FFFFF) > 0x600000)) << 23).astype(np.uint32).view(np.float32)
+    assert np.array_equal(rule[::97].view(np.uint32), ref.view(np.uint32))
+    r = (a / np.float32(448.0)).astype(np.float32).view(np.uint32)
+    up = np.where((r & 0x7FFFFF) != 0, (r & 0x7F800000) + 0x800000, r).astype(np.uint32)
+    assert np.array_equal(rule.view(np.uint32), up)
