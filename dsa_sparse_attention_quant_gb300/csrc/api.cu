@@ -146,7 +146,7 @@ IndexerWs carve(const DsaBatch* b, void* base) {
   const size_t B = static_cast<size_t>(b->num_reqs);
   const size_t Td = static_cast<size_t>(b->num_decode_tokens);
   const size_t ld = static_cast<size_t>(logits_ld(b));
-  const size_t max_pre = T / 4 + B + 1;
+  const size_t max_pre = T / kPrefillTok + B + 1;
   w.pre.qb = static_cast<QBlock*>(take(max_pre * sizeof(QBlock)));
   w.pre.tile_start = static_cast<int32_t*>(take((max_pre + 1) * 4));
   w.pre.nqb = static_cast<int32_t*>(take(4));
@@ -223,8 +223,9 @@ int run_logits(const DsaBatch* b, const uint8_t* q_fp8, const float* w_folded, c
     if ((st = launched(launch_logits(1, &mk, &mq1, SegmentPlan{}, a, grid_ctas(sms), stream), stream)) != DSA_OK) return st;
   }
   if (b->num_reqs > b->num_decodes) {
-    if ((st = make_q_map(&mq4, q_fp8, b->num_tokens, 4 * kHeads)) != DSA_OK) return st;
-    if ((st = launched(launch_logits(4, &mk, &mq4, ws.pre, a, grid_ctas(sms), stream), stream)) != DSA_OK) return st;
+    if ((st = make_q_map(&mq4, q_fp8, b->num_tokens, kPrefillTok * kHeads)) != DSA_OK) return st;
+    if ((st = launched(launch_logits(kPrefillTok, &mk, &mq4, ws.pre, a, grid_ctas(sms), stream), stream)) != DSA_OK)
+      return st;
   }
   return DSA_OK;
 }

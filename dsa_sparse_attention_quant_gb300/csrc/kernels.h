@@ -16,6 +16,9 @@ constexpr int kBlock = DSA_BLOCK_SIZE;
 constexpr int kPageBytes = DSA_PAGE_BYTES;
 constexpr int kScaleOffset = kBlock * kDim;  // 8192: the 64 fp32 scales follow the 64 K rows
 
+// Query tokens per block of the prefill segment (decode blocks hold one).
+constexpr int kPrefillTok = 4;
+
 // One query block: NTOK consecutive query tokens of one request.
 struct QBlock {
   int32_t req;  // request
@@ -142,8 +145,8 @@ struct SelectArgs {
 };
 
 // ntok_per_block = 1 (decode segment: the kernel plans its slice from the
-// request metadata in `a`, `plan` is unused) or 4 (prefill segment, `plan`
-// written by the prologue).
+// request metadata in `a`, `plan` is unused) or kPrefillTok (prefill segment,
+// `plan` written by the prologue).
 cudaError_t launch_logits(int ntok_per_block, const CUtensorMap* tmap_k, const CUtensorMap* tmap_q,
                           SegmentPlan plan, const LogitsArgs& a, int num_sms, cudaStream_t stream);
 

@@ -31,18 +31,22 @@ template <int NTOK>
 struct LogitsCfg {
   static constexpr int N = 64 * NTOK;                     // MMA N: heads x tokens
   static constexpr int kStages = NTOK == 1 ? 8 : 6;       // K-tile ring
-  // Epilogue: two teams take the tiles in turn. A decode team is one
-  // warpgroup (its scores ran no faster with more); a prefill team is two
-  // warpgroups that split a tile's four tokens, so that more warps hide the
-  // TMEM-load and FMA latency of the 64-head reduction.
-  static constexpr int kTeams = 2;
-  static constexpr int kTeamWG = NTOK == 1 ? 1 : 2;      // warpgroups per team
+  // TMEM accumulator ring: as many N-column accumulators as fit in the 512
+  // columns, at most four.
+  static constexpr int kAcc = 512 / N < 4 ? 512 / N : 4;
+  // Epilogue: teams take the tiles in turn, each team one or two warpgroups
+  // that split a tile's tokens (two tokens, 128 columns, per warpgroup), one
+  // team per accumulator. A decode team is one warpgroup and two teams suffice
+  // (their scores ran no faster with more). Prefill blocks of four tokens
+  // (two 256-column accumulators, two teams of two warpgroups) ran faster than
+  // blocks of two (four teams, each K tile read twice as often).
+  static constexpr int kTeamWG = NTOK <= 2 ? 1 : NTOK / 2;  // warpgroups per team
+  static constexpr int kTeams = NTOK == 1 ? 2 : kAcc;
   static constexpr int kEpiWG = kTeams * kTeamWG;
-  static constexpr int kTokPerWG = NTOK / kTeamWG;       // tokens of a tile one warpgroup reduces
-  static constexpr int kAcc = NTOK == 1 ? 4 : 2;          // TMEM accumulator ring
+  static constexpr int kTokPerWG = NTOK / kTeamWG;          // tokens of a tile one warpgroup reduces
   static constexpr int kEpiWarps = 4 * kEpiWG;
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
-  static constexpr uint32_t kTmemCols = N * kAcc;         // 256 or 512
+  static constexpr uint32_t kTmemCols = N * kAcc;         // 256 (decode) or 512 (prefill)
   static constexpr int kStageBytes = 17 * 1024;           // 2 x 8 KB K pages, 2 x 256 B scales, 1 KB aligned
   static constexpr int kScaleOff = 16384;
   static constexpr int kQBytes = N * kDim;
@@ -505,7 +509,7 @@ static cudaError_t launch_logits_t(const CUtensorMap* tmap_k, const CUtensorMap*
 cudaError_t launch_logits(int ntok_per_block, const CUtensorMap* tmap_k, const CUtensorMap* tmap_q,
                           SegmentPlan plan, const LogitsArgs& a, int num_sms, cudaStream_t stream) {
   if (ntok_per_block == 1) return launch_logits_t<1>(tmap_k, tmap_q, plan, a, num_sms, stream);
-  return launch_logits_t<4>(tmap_k, tmap_q, plan, a, num_sms, stream);
+  return launch_logits_t<kPrefillTok>(tmap_k, tmap_q, plan, a, num_sms, stream);
 }
 
 }  // namespace dsa

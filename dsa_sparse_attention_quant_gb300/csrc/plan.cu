@@ -128,7 +128,7 @@ __device__ void plan_batch(const PlanArgs& p, PlanSmem& S) {
   // the decode segment is planned by its score kernel; a segment without
   // requests launches no score kernel
   if (p.num_reqs > p.num_decodes)
-    plan_segment(p.qsl, p.seq_lens, p.num_decodes, p.num_reqs, 4, p.num_tokens, p.bt_stride, p.grid, p.pre, p.err,
+    plan_segment(p.qsl, p.seq_lens, p.num_decodes, p.num_reqs, kPrefillTok, p.num_tokens, p.bt_stride, p.grid, p.pre, p.err,
                  S);
 }
 
