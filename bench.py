@@ -700,9 +700,17 @@ def cpu_baseline(hb, budget_s: float):
         if dt >= budget_s / 2 or n_rows >= T:
             break
         n_rows = int(min(T, max(2 * n_rows, n_rows * budget_s / max(dt, 1e-3))))
+    reps = 1
+    if n_rows >= T and dt < budget_s / 4:  # the whole step is quick: time several passes of it
+        reps = int(min(1000, max(2, budget_s / 2 / max(dt, 1e-4))))
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            p = oracle_step(ora, hb, cache, rows)
+        dt = (time.perf_counter() - t0) / reps
     return {"value": p / dt, "unit": "pairs/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{n_rows} of {T} query rows of the same step ({p} pairs; K write of all {T} new tokens, "
-                      f"fp64 scores, full-sort top-k, conversion), {dt:.1f} s, OpenMP over rows"}
+                      f"fp64 scores, full-sort top-k, conversion), {dt:.2f} s per pass, {reps} pass(es), "
+                      f"OpenMP over rows"}
 
 
 def run_reference(args):
