@@ -97,6 +97,27 @@ def profiled_traffic(summary: str):
     return int(fields["bytes"])
 
 
+# --------------------------------------------------------------------- ranks
+
+def max_over_ranks(x: float, device) -> float:
+    """The largest value of x over the ranks of the process group (x itself on
+    one rank). The timed region of a multi-GPU run is the slowest rank's."""
+    import torch
+    import torch.distributed as dist
+
+    if not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, seconds: float) -> float:
+    """Throughput of the whole job: every rank processed its own replica of the
+    workload (weak scaling), all within the slowest rank's time."""
+    return units_per_rank * world / seconds
+
+
 def read_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -303,10 +324,7 @@ def run_ours(args):
         per_kernel = np.array([[evs[j].elapsed_time(evs[j + 1]) for j in range(launches_per_step)] for evs in kev])
         score_cols = [j for j, name in enumerate(kernels) if name.startswith("logits")]
         kernel_ms = per_kernel[:, score_cols].sum(axis=1)
-        if world > 1:
-            t = torch.tensor([elapsed_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            elapsed_ms = float(t.item())
+        elapsed_ms = max_over_ranks(elapsed_ms, dev)
 
         # end to end through the same calls from pinned host memory: H2D of the
         # step's inputs and metadata, the step, D2H of the physical ids
@@ -349,10 +367,7 @@ def run_ours(args):
             e2e_step(i)
         e1 = time.perf_counter()
         e2e_s = e1 - e0
-        if world > 1:
-            t = torch.tensor([e2e_s], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
+        e2e_s = max_over_ranks(e2e_s, dev)
     torch.cuda.synchronize()
     if dsa.check_device_error(err):
         raise SystemExit(f"device error word set: {int(err.item()):#x}")
@@ -361,8 +376,8 @@ def run_ours(args):
         dist.destroy_process_group()
         return
     ms_per_step = elapsed_ms / args.steps
-    value = pairs * world / (ms_per_step / 1e3)
-    rows_per_s = T * world / (ms_per_step / 1e3)
+    value = whole_job_rate(pairs, world, ms_per_step / 1e3)
+    rows_per_s = whole_job_rate(T, world, ms_per_step / 1e3)
     hbm_peak, bf16_burst, bf16_sustained, peak_src = read_peaks()
     kernel_avg_ms = float(np.mean(kernel_ms))
     traffic = profiled_traffic(f"logits_kernel_{args.workload}.md")
@@ -417,7 +432,7 @@ def run_ours(args):
         "roofline": roofline,
         "breakdown_us": breakdown,
         "e2e": {
-            "value": pairs * world / (e2e_s / args.steps),
+            "value": whole_job_rate(pairs, world, e2e_s / args.steps),
             "unit": "pairs/s",
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
