@@ -129,6 +129,16 @@ def permutation(seed: int, stream: int, n: int) -> np.ndarray:
     return np.argsort(random_u64(seed, stream, n), kind="stable").astype(np.int64)
 
 
+def rope_cos_sin(max_pos: int, theta: float = 10000.0) -> np.ndarray:
+    """The rotary angles as a model holds them: float32 [max_pos, 64], row p =
+    cos(p * f_i) for i < 32, then sin(p * f_i), f_i = theta^(-2i/64) (fp64,
+    rounded to fp32). Input preparation: the path receives this table."""
+    half = ROPE_DIM // 2
+    inv = theta ** (-2.0 * np.arange(half, dtype=np.float64) / ROPE_DIM)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
 def rope_neox(x: np.ndarray, positions: np.ndarray, theta: float = 10000.0) -> np.ndarray:
     """Rotary position embedding on dims ``[0, ROPE_DIM)`` of the last axis (fp64).
 

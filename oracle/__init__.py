@@ -65,6 +65,7 @@ def _bind(lib):
         "ora_slot_offsets": (None, [I64, P, P]),
         "ora_k_quant_write": (I64, [P, I64, P, P, I64]),
         "ora_q_quant": (None, [P, I64, P, P]),
+        "ora_rope": (I64, [P, I64, I64, P, P, I64, P]),
         "ora_logits_row": (None, [P, P, P, P, P, I64, P]),
         "ora_topk_row": (None, [P, I64, I32, P]),
         "ora_indexer": (I64, [P, P, P, P, I64, P, P, P, I64, I32, P, P, I64]),
@@ -147,6 +148,18 @@ class Oracle:
         scales = np.zeros(q.shape[:-1], np.float32)
         self._lib.ora_q_quant(_p(q), q.size // DIM, _p(codes), _p(scales))
         return codes, scales
+
+    def rope(self, x_bf16, positions, cos_sin, rows_per_token: int):
+        """Rotate the leading 64 dims of bf16 rows of 128 (any leading shape);
+        row r belongs to token r // rows_per_token. Returns (rotated bits, rows
+        left unrotated because their position is outside the table)."""
+        x = _c(x_bf16, np.uint16)
+        pos = _c(positions, np.int64)
+        cs = _c(cos_sin, np.float32)
+        out = np.empty_like(x)
+        bad = self._lib.ora_rope(_p(x), x.size // DIM, int(rows_per_token), _p(pos), _p(cs), int(cs.shape[0]),
+                                 _p(out))
+        return out, int(bad)
 
     def fill_cache(self, batch, cache: np.ndarray | None = None, include_new: bool = True):
         """The oracle's own cache for ``batch``: context K, then this step's K."""

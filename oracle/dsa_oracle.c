@@ -107,6 +107,50 @@ static float bf16_value(uint16_t bits) {
   return f;
 }
 
+/* fp32 -> bf16, round to nearest even (the model's tensors are bf16). */
+static uint16_t bf16_round(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x7FFFFFu)) return (uint16_t)((u >> 16) | 0x40u); /* NaN */
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+/* Rotary position embedding of the PE subspace, before the quantiser.
+ * "IndexCache：DeepSeek 稀疏注意力中的跨层索引复用", `Indexer.forward`: the first
+ * rope_dim = 64 dims of every q head and of the shared K row are rotated by
+ * `rotary_emb(positions, q_pe, k_pe)`; the other 64 dims pass through.
+ * Reading taken (the pairing is not printed): half-split pairs (i, i+32),
+ * i < 32, with the angles of position p given as an input table
+ * cos_sin[p*64 + i] = cos, cos_sin[p*64 + 32 + i] = sin;
+ *   y[i]    = x[i]*cos - x[i+32]*sin,   y[i+32] = x[i+32]*cos + x[i]*sin,
+ * each product and each sum rounded in IEEE fp32 (no fused multiply-add), the
+ * result rounded to bf16. Row r belongs to token r / rows_per_token. A row
+ * whose position is outside [0, max_pos) is copied unrotated and counted. */
+int64_t ora_rope(const uint16_t *x, int64_t rows, int64_t rows_per_token, const int64_t *positions,
+                 const float *cos_sin, int64_t max_pos, uint16_t *out) {
+  int64_t r, bad = 0;
+  for (r = 0; r < rows; ++r) {
+    const uint16_t *xr = x + r * ORA_DIM;
+    uint16_t *yr = out + r * ORA_DIM;
+    const int64_t p = positions[r / rows_per_token];
+    int i;
+    memcpy(yr, xr, ORA_DIM * sizeof(uint16_t));
+    if (p < 0 || p >= max_pos) {
+      ++bad;
+      continue;
+    }
+    for (i = 0; i < ORA_ROPE / 2; ++i) {
+      const float x1 = bf16_value(xr[i]), x2 = bf16_value(xr[i + ORA_ROPE / 2]);
+      const float c = cos_sin[p * ORA_ROPE + i], s = cos_sin[p * ORA_ROPE + ORA_ROPE / 2 + i];
+      const float a = x1 * c, b = x2 * s, d = x2 * c, e = x1 * s;
+      yr[i] = bf16_round(a - b);
+      yr[i + ORA_ROPE / 2] = bf16_round(d + e);
+    }
+  }
+  return bad;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Paged cache. [IC] `DeepseekV32IndexerBackend.get_kv_cache_shape` gives
  * (num_blocks, block_size, head_size) uint8 with one shared K head, and the

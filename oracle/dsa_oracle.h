@@ -21,6 +21,7 @@ extern "C" {
 
 #define ORA_HEADS 64
 #define ORA_DIM 128
+#define ORA_ROPE 64                               /* rotated leading dims (PE subspace) */
 #define ORA_BLOCK 64
 #define ORA_SLOT_BYTES 132                       /* 128 B FP8 K + 4 B fp32 scale */
 #define ORA_PAGE_BYTES (ORA_BLOCK * ORA_SLOT_BYTES) /* 8448 */
@@ -38,6 +39,11 @@ void ora_slot_offsets(int64_t slot, int64_t *k_byte, int64_t *scale_byte);
 int64_t ora_k_quant_write(const uint16_t *k_bf16, int64_t n, const int64_t *slot_mapping,
                           uint8_t *cache, int64_t num_blocks);
 void ora_q_quant(const uint16_t *q_bf16, int64_t rows, uint8_t *q_codes, float *q_scale);
+
+/* RoPE on the leading 64 dims (half-split pairs, fp32 steps, bf16 result);
+ * returns the number of rows left unrotated (position out of range). */
+int64_t ora_rope(const uint16_t *x, int64_t rows, int64_t rows_per_token, const int64_t *positions,
+                 const float *cos_sin, int64_t max_pos, uint16_t *out);
 
 /* indexer scores and selection */
 void ora_logits_row(const uint8_t *q_codes, const float *q_scale, const float *w,

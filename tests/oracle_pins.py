@@ -417,4 +417,62 @@ def pin_schedule(ora):
         raise AssertionError(f"schedule accepted {bad}")
 
 
+def _bf16_float(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+def pin_rope_hand_cases(ora):
+    # unit vectors in dims 0 and 32 rotated by (cos, sin) = (0.6, 0.8): the pair
+    # of dim i is dim i + 32, dim i takes x*cos - y*sin, dim i + 32 y*cos + x*sin
+    x = np.zeros((4, 128), np.uint16)
+    x[0, 0] = 0x3F80      # e_0
+    x[1, 32] = 0x3F80     # e_32
+    x[2, 5] = 0x4000      # 2 * e_5
+    x[3, 64] = 0x3F80     # e_64: outside the rotated dims
+    cs = np.zeros((2, 64), np.float32)
+    cs[:, :32] = 1.0      # position 0: the identity
+    cs[1, :32], cs[1, 32:] = 0.6, 0.8
+    out, bad = ora.rope(x, np.array([1, 1, 1, 1], np.int64), cs, 1)
+    assert bad == 0
+    bf = lambda v: int(synth.bf16_bits(np.array([v]))[0])
+    assert out[0, 0] == bf(0.6) and out[0, 32] == bf(0.8)
+    assert out[1, 0] == bf(-0.8) and out[1, 32] == bf(0.6)
+    assert out[2, 5] == bf(1.2) and out[2, 37] == bf(1.6)
+    assert np.array_equal(out[3], x[3])
+    assert np.count_nonzero(out[0]) == 2 and np.count_nonzero(out[1]) == 2
+    ident, _ = ora.rope(x, np.zeros(4, np.int64), cs, 1)
+    assert np.array_equal(ident, x)
+    # a position outside the table: copied and counted
+    same, bad = ora.rope(x[:2], np.array([2], np.int64), cs, 2)
+    assert bad == 2 and np.array_equal(same, x[:2])
+
+
+def pin_rope_error_bound(ora, n: int = 2000):
+    # against the exact rotation in fp64: each output is the exact value up to
+    # the fp32 steps (< 2^-22 relative to |x||c| + |y||s|) and one bf16 rounding
+    # (half an ulp, <= 2^-8 relative); rows share a position per token of 3 rows
+    rng = np.random.default_rng(3)
+    x = synth.bf16_bits(rng.standard_normal((n, 128)) * 4.0)
+    cs = synth.rope_cos_sin(512)
+    pos = rng.integers(0, 512, size=(n + 2) // 3).astype(np.int64)
+    out, bad = ora.rope(x, pos, cs, 3)
+    assert bad == 0
+    xf = _bf16_float(x).astype(np.float64)
+    p = pos[np.arange(n) // 3]
+    c = cs[p, :32].astype(np.float64)
+    s = cs[p, 32:].astype(np.float64)
+    x1, x2 = xf[:, :32], xf[:, 32:64]
+    y1, y2 = x1 * c - x2 * s, x2 * c + x1 * s
+    g = _bf16_float(out).astype(np.float64)
+    for got, ref, scale in ((g[:, :32], y1, np.abs(x1 * c) + np.abs(x2 * s)),
+                            (g[:, 32:64], y2, np.abs(x2 * c) + np.abs(x1 * s))):
+        tol = np.abs(ref) * 2.0 ** -8 * (1 + 2.0 ** -20) + scale * 2.0 ** -22 + 1e-30
+        assert np.all(np.abs(got - ref) <= tol)
+    assert np.array_equal(out[:, 64:], x[:, 64:])
+    # the rotation keeps each pair's length (to the rounding above)
+    r_in = np.hypot(x1, x2)
+    r_out = np.hypot(g[:, :32], g[:, 32:64])
+    assert np.all(np.abs(r_out - r_in) <= r_in * 2.0 ** -7 + 1e-30)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

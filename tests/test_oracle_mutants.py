@@ -34,6 +34,12 @@ MUTANTS = {
     "schedule_offset_off_by_one": [("int v = l - offset + 1;", "int v = l - offset;")],
     "schedule_no_char_check": [("if (pattern[l] != 'F' && pattern[l] != 'S') return -1;", "")],
     "convert_ignores_stride": [("row[id / block_size] * block_stride_rows", "row[id / block_size] * block_size")],
+    "rope_interleaved_pairs": [("x2 = bf16_value(xr[i + ORA_ROPE / 2]);", "x2 = bf16_value(xr[i ^ 1]);")],
+    "rope_sine_sign": [("yr[i] = bf16_round(a - b);", "yr[i] = bf16_round(a + b);")],
+    "rope_cos_sin_swapped": [("const float c = cos_sin[p * ORA_ROPE + i], s = cos_sin[p * ORA_ROPE + ORA_ROPE / 2 + i];",
+                              "const float s = cos_sin[p * ORA_ROPE + i], c = cos_sin[p * ORA_ROPE + ORA_ROPE / 2 + i];")],
+    "rope_token_of_row": [("const int64_t p = positions[r / rows_per_token];", "const int64_t p = positions[r % rows_per_token];")],
+    "rope_truncates": [("  u += 0x7FFFu + ((u >> 16) & 1u);\n", "")],
     "convert_counts_padding": [("        ++valid;\n", ""), ("        physical[t * topk + j] = -1;\n",
                                                         "        physical[t * topk + j] = -1;\n        ++valid;\n")],
 }
