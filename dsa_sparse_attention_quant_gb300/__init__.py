@@ -9,10 +9,12 @@ from .binding import (  # noqa: F401
     DsaError,
     check_device_error,
     indexer_k_quant_write,
+    indexer_k_rope_quant_write,
     indexer_logits,
     indexer_logits_topk,
     indexer_plan,
     indexer_q_quant_fold,
+    indexer_q_rope_quant_fold,
     indexer_topk,
     indexer_workspace_size,
     layer_stack_run,
@@ -22,4 +24,4 @@ from .binding import (  # noqa: F401
     topk_logical_to_physical,
 )
 
-__version__ = "0.1.0"
+__version__ = "0.2.0"

@@ -37,6 +37,7 @@ SYMBOLS = [
     "dsa_topk_logical_to_physical", "dsa_schedule_build",
     "dsa_layer_stack_workspace_size", "dsa_layer_stack_run",
     "dsa_indexer_logits_topk_static", "dsa_set_launch_events",
+    "dsa_indexer_k_rope_quant_write", "dsa_indexer_q_rope_quant_fold",
 ]
 STATIC_WORKSPACE_BYTES = 32 << 20
 
@@ -82,6 +83,9 @@ class DsaStackPlanC(ctypes.Structure):
         ("topk", ctypes.c_int32),
         ("softmax_scale", ctypes.c_float),
         ("block_stride_rows", ctypes.c_int32),
+        ("positions", ctypes.c_void_p),
+        ("rope_cos_sin", ctypes.c_void_p),
+        ("rope_max_pos", ctypes.c_int64),
     ]
 
 
@@ -122,6 +126,8 @@ def load(build_if_missing: bool = True):
                                                    SZ, P, P]),
             "dsa_indexer_logits_topk_static": (ctypes.c_int, [BP, P, P, P, I32, P, P, P, P, P]),
             "dsa_set_launch_events": (ctypes.c_int, [P, I32]),
+            "dsa_indexer_k_rope_quant_write": (ctypes.c_int, [P, I64, I64, P, P, I64, P, P, I64, P, P]),
+            "dsa_indexer_q_rope_quant_fold": (ctypes.c_int, [P, P, I64, P, P, I64, F32, P, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -210,6 +216,50 @@ def indexer_k_quant_write(k, slot_mapping, k_cache, dev_err=None, stream=None):
     st = load().dsa_indexer_k_quant_write(_ptr(k), n, row_stride, _ptr(slot_mapping), _ptr(k_cache),
                                           int(k_cache.shape[0]), _ptr(dev_err), _stream(stream))
     _check(st, "dsa_indexer_k_quant_write")
+
+
+def _rope_table(cos_sin):
+    _need(cos_sin, torch.float32, "cos_sin")
+    if cos_sin.dim() != 2 or cos_sin.shape[1] != 64:
+        raise DsaError("cos_sin must be [max_pos, 64] fp32")
+    return int(cos_sin.shape[0])
+
+
+def indexer_k_rope_quant_write(k, positions, cos_sin, slot_mapping, k_cache, dev_err=None, stream=None):
+    """RoPE of k's leading 64 dims (by positions and the cos/sin table), then S1."""
+    _need(slot_mapping, torch.int64, "slot_mapping")
+    _need(positions, torch.int64, "positions")
+    _need(k_cache, torch.uint8, "k_cache")
+    max_pos = _rope_table(cos_sin)
+    n = int(slot_mapping.shape[0])
+    if n == 0:
+        return
+    if k.dtype != torch.bfloat16 or not k.is_cuda or k.stride(-1) != 1:
+        raise DsaError("k must be a CUDA bf16 tensor with unit inner stride")
+    row_stride = int(k.stride(0)) if k.dim() == 2 else HEAD_DIM
+    st = load().dsa_indexer_k_rope_quant_write(_ptr(k), n, row_stride, _ptr(positions), _ptr(cos_sin), max_pos,
+                                               _ptr(slot_mapping), _ptr(k_cache), int(k_cache.shape[0]),
+                                               _ptr(dev_err), _stream(stream))
+    _check(st, "dsa_indexer_k_rope_quant_write")
+
+
+def indexer_q_rope_quant_fold(q, w, positions, cos_sin, softmax_scale: float = 0.0, q_fp8=None, q_scale=None,
+                              w_folded=None, dev_err=None, stream=None):
+    """RoPE of every q head's leading 64 dims, then S2a."""
+    _need(q, torch.bfloat16, "q")
+    _need(w, torch.float32, "w")
+    _need(positions, torch.int64, "positions")
+    max_pos = _rope_table(cos_sin)
+    T = int(q.shape[0])
+    if q_fp8 is None:
+        q_fp8 = torch.empty((T, HEADS, HEAD_DIM), dtype=torch.uint8, device=q.device)
+    if w_folded is None:
+        w_folded = torch.empty((T, HEADS), dtype=torch.float32, device=q.device)
+    st = load().dsa_indexer_q_rope_quant_fold(_ptr(q), _ptr(w), T, _ptr(positions), _ptr(cos_sin), max_pos,
+                                              float(softmax_scale), _ptr(q_fp8), _ptr(q_scale), _ptr(w_folded),
+                                              _ptr(dev_err), _stream(stream))
+    _check(st, "dsa_indexer_q_rope_quant_fold")
+    return q_fp8, q_scale, w_folded
 
 
 def indexer_q_quant_fold(q, w, softmax_scale: float = 0.0, q_fp8=None, q_scale=None, w_folded=None, stream=None):
@@ -345,10 +395,13 @@ def layer_stack_workspace_size(batch: Batch, topk: int) -> int:
 
 def layer_stack_run(batch: Batch, fs: str, layers, topk: int, slot_mapping=None, topk_buf=None, phys_buf=None,
                     valid_buf=None, consumer=None, ws=None, softmax_scale: float = 0.0, block_stride_rows: int = 0,
-                    dev_err=None, stream=None):
+                    dev_err=None, stream=None, positions=None, rope_cos_sin=None):
     """Run a stack of layers. ``layers[l]`` is None for 'S' layers, else a dict
     with tensors ``q``, ``w``, ``k_cache`` and optionally ``k_new``.
-    ``consumer(layer, producer, phys_ptr, valid_ptr)`` is called per layer."""
+    ``consumer(layer, producer, phys_ptr, valid_ptr)`` is called per layer.
+    With ``rope_cos_sin`` ([max_pos, 64] fp32) and ``positions`` (int64 [T]),
+    q and k_new arrive un-rotated and each F layer rotates them (RoPE) on the
+    way into the quantiser."""
     n = len(fs)
     arr = (DsaLayerInputsC * max(n, 1))()
     keep = []
@@ -359,7 +412,12 @@ def layer_stack_run(batch: Batch, fs: str, layers, topk: int, slot_mapping=None,
         arr[l] = DsaLayerInputsC(L["q"].data_ptr(), L["w"].data_ptr(),
                                  L["k_new"].data_ptr() if L.get("k_new") is not None else None,
                                  L["k_cache"].data_ptr())
-    plan = DsaStackPlanC(n, fs.encode(), arr, int(topk), float(softmax_scale), int(block_stride_rows))
+    max_pos = 0
+    if rope_cos_sin is not None:
+        max_pos = _rope_table(rope_cos_sin)
+        _need(positions, torch.int64, "positions")
+    plan = DsaStackPlanC(n, fs.encode(), arr, int(topk), float(softmax_scale), int(block_stride_rows),
+                         _ptr(positions) if rope_cos_sin is not None else None, _ptr(rope_cos_sin), max_pos)
     dev = torch.device("cuda", torch.cuda.current_device())
     T = batch.num_tokens
     if topk_buf is None:

@@ -264,7 +264,7 @@ const char* dsa_status_string(int status) {
   }
 }
 
-int dsa_version(void) { return 100; }
+int dsa_version(void) { return 200; }
 
 int dsa_check_device_error(const int32_t* dev_err, uint32_t* out, dsa_stream_t stream) {
   if (dev_err == nullptr) return DSA_EINVAL;
@@ -284,8 +284,8 @@ int dsa_indexer_k_quant_write(const void* k, int64_t n_tokens, int64_t k_row_str
   int sms;
   int st = device_sms(&sms);
   if (st != DSA_OK) return st;
-  return from_cuda(launch_k_quant_write(k, n_tokens, k_row_stride, slot_mapping, k_cache, num_blocks, dev_err,
-                                        stream));
+  return from_cuda(launch_k_quant_write(k, n_tokens, k_row_stride, slot_mapping, k_cache, num_blocks, RopeArgs{},
+                                        dev_err, stream));
 }
 
 int dsa_indexer_q_quant_fold(const void* q, const float* w, int64_t n_tokens, float softmax_scale, uint8_t* q_fp8,
@@ -297,7 +297,39 @@ int dsa_indexer_q_quant_fold(const void* q, const float* w, int64_t n_tokens, fl
   int st = device_sms(&sms);
   if (st != DSA_OK) return st;
   if (!(softmax_scale > 0.0f)) softmax_scale = 0.08838834764831845f;  // 128^-1/2
-  return from_cuda(launch_q_quant_fold(q, w, n_tokens, softmax_scale, q_fp8, q_scale, w_folded, stream));
+  return from_cuda(launch_q_quant_fold(q, w, n_tokens, softmax_scale, q_fp8, q_scale, w_folded, RopeArgs{}, nullptr,
+                                       stream));
+}
+
+int dsa_indexer_k_rope_quant_write(const void* k, int64_t n_tokens, int64_t k_row_stride, const int64_t* positions,
+                                   const float* cos_sin, int64_t max_pos, const int64_t* slot_mapping,
+                                   uint8_t* k_cache, int64_t num_blocks, int32_t* dev_err, dsa_stream_t stream) {
+  if (n_tokens < 0 || num_blocks < 1 || k_row_stride < kDim || k_row_stride % 8 != 0 || max_pos < 1) return DSA_EINVAL;
+  if (n_tokens == 0) return DSA_OK;
+  if (!k || !slot_mapping || !k_cache || !positions || !cos_sin || !aligned16(k) || !aligned16(k_cache) ||
+      !aligned16(cos_sin))
+    return DSA_EINVAL;
+  int sms;
+  int st = device_sms(&sms);
+  if (st != DSA_OK) return st;
+  return from_cuda(launch_k_quant_write(k, n_tokens, k_row_stride, slot_mapping, k_cache, num_blocks,
+                                        RopeArgs{positions, cos_sin, max_pos}, dev_err, stream));
+}
+
+int dsa_indexer_q_rope_quant_fold(const void* q, const float* w, int64_t n_tokens, const int64_t* positions,
+                                  const float* cos_sin, int64_t max_pos, float softmax_scale, uint8_t* q_fp8,
+                                  float* q_scale, float* w_folded, int32_t* dev_err, dsa_stream_t stream) {
+  if (n_tokens < 0 || max_pos < 1) return DSA_EINVAL;
+  if (n_tokens == 0) return DSA_OK;
+  if (!q || !w || !q_fp8 || !w_folded || !positions || !cos_sin || !aligned16(q) || !aligned16(q_fp8) ||
+      !aligned16(cos_sin))
+    return DSA_EINVAL;
+  int sms;
+  int st = device_sms(&sms);
+  if (st != DSA_OK) return st;
+  if (!(softmax_scale > 0.0f)) softmax_scale = 0.08838834764831845f;  // 128^-1/2
+  return from_cuda(launch_q_quant_fold(q, w, n_tokens, softmax_scale, q_fp8, q_scale, w_folded,
+                                       RopeArgs{positions, cos_sin, max_pos}, dev_err, stream));
 }
 
 size_t dsa_indexer_workspace_size(const DsaBatch* batch, int32_t topk) {
@@ -448,6 +480,9 @@ int dsa_layer_stack_run(const DsaStackPlan* plan, const DsaBatch* batch, const i
     return DSA_EINVAL;
   if (!topk_ok(plan->topk)) return DSA_EINVAL;
   if (plan->n_layers > 0 && plan->fs[0] != 'F') return DSA_EINVAL;
+  if (plan->rope_cos_sin != nullptr &&
+      (plan->positions == nullptr || plan->rope_max_pos < 1 || !aligned16(plan->rope_cos_sin)))
+    return DSA_EINVAL;
   for (int32_t l = 0; l < plan->n_layers; ++l) {
     const char c = plan->fs[l];
     if (c != 'F' && c != 'S') return DSA_EINVAL;
@@ -483,6 +518,7 @@ int dsa_layer_stack_run(const DsaStackPlan* plan, const DsaBatch* batch, const i
         pa.q = static_cast<const __nv_bfloat16*>(L.q);
         pa.w = L.w;
         pa.softmax_scale = softmax_scale;
+        pa.rope = RopeArgs{plan->positions, plan->rope_cos_sin, plan->rope_max_pos};
         pa.q_fp8 = q8;
         pa.w_folded = wf;
         pa.plan = pa.plan && !planned;

@@ -107,6 +107,48 @@ __device__ __forceinline__ uint32_t quant_row_lane(uint2 raw, float* scale_out) 
   return e4m3x4(f0.x * inv, f0.y * inv, f1.x * inv, f1.y * inv);
 }
 
+// RoPE of the leading 64 dims of one 128-value bf16 row held by a warp (lane
+// i: values 4i..4i+3): dim i < 32 pairs with dim i + 32, which sits on lane
+// i/4 + 8. y[i] = x[i]*c - x[i+32]*s, y[i+32] = x[i+32]*c + x[i]*s, each
+// product and sum rounded in fp32 (no contraction), the result rounded to
+// bf16. cs: the position's row of the cos/sin table (64 floats, 16-byte
+// aligned: cos of the 32 pair angles, then their sin). All lanes must call.
+__device__ __forceinline__ uint2 rope_row_lane(uint2 raw, const float* cs) {
+  const int lane = threadIdx.x & 31;
+  const uint2 other = make_uint2(__shfl_xor_sync(0xffffffffu, raw.x, 8), __shfl_xor_sync(0xffffffffu, raw.y, 8));
+  if (lane >= 16) return raw;
+  const int i0 = 4 * (lane & 7);
+  const float4 c = __ldg(reinterpret_cast<const float4*>(cs + i0));
+  const float4 s = __ldg(reinterpret_cast<const float4*>(cs + 32 + i0));
+  const float2 x01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+  const float2 x23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+  const float2 y01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&other.x));
+  const float2 y23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&other.y));
+  const float x[4] = {x01.x, x01.y, x23.x, x23.y}, y[4] = {y01.x, y01.y, y23.x, y23.y};
+  const float cc[4] = {c.x, c.y, c.z, c.w}, ss[4] = {s.x, s.y, s.z, s.w};
+  float r[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    // lanes 0-7 hold x[i] (partner x[i+32]); lanes 8-15 hold x[i+32] (partner x[i])
+    const float a = __fmul_rn(x[u], cc[u]), b = __fmul_rn(y[u], ss[u]);
+    r[u] = lane < 8 ? __fsub_rn(a, b) : __fadd_rn(a, b);
+  }
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(r[0], r[1]), hi = __floats2bfloat162_rn(r[2], r[3]);
+  return make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+}
+
+// The row of the cos/sin table for a position, or nullptr (no rotation:
+// table absent, or the position out of range, which is flagged).
+__device__ __forceinline__ const float* rope_row(const RopeArgs& r, int64_t token, int32_t* err, int lane) {
+  if (r.cos_sin == nullptr) return nullptr;
+  const int64_t p = __ldg(r.positions + token);
+  if (p < 0 || p >= r.max_pos) {
+    if (lane == 0) flag_error(err, DSA_DEVERR_POS_RANGE);
+    return nullptr;
+  }
+  return r.cos_sin + p * kRope;
+}
+
 // ---------------------------------------------------------------------------
 // Shared-memory addresses and mbarriers.
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

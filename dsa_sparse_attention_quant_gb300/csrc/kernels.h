@@ -15,6 +15,14 @@ constexpr int kDim = DSA_HEAD_DIM;
 constexpr int kBlock = DSA_BLOCK_SIZE;
 constexpr int kPageBytes = DSA_PAGE_BYTES;
 constexpr int kScaleOffset = kBlock * kDim;  // 8192: the 64 fp32 scales follow the 64 K rows
+constexpr int kRope = 64;                    // rotated leading dims of q and K rows
+
+// RoPE fused into the quantiser: cos_sin == nullptr means the rows arrive rotated.
+struct RopeArgs {
+  const int64_t* positions;  // [tokens]
+  const float* cos_sin;      // [max_pos, 64]: cos of the 32 pair angles, then sin
+  int64_t max_pos;
+};
 
 // Query tokens per block of the prefill segment (decode blocks hold one).
 constexpr int kPrefillTok = 4;
@@ -47,9 +55,11 @@ struct SegmentPlan {
 };
 
 cudaError_t launch_k_quant_write(const void* k, int64_t n, int64_t row_stride, const int64_t* slot_mapping,
-                                 uint8_t* cache, int64_t num_blocks, int32_t* err, cudaStream_t stream);
+                                 uint8_t* cache, int64_t num_blocks, const RopeArgs& rope, int32_t* err,
+                                 cudaStream_t stream);
 cudaError_t launch_q_quant_fold(const void* q, const float* w, int64_t n_tokens, float softmax_scale,
-                                uint8_t* q_fp8, float* q_scale, float* w_folded, cudaStream_t stream);
+                                uint8_t* q_fp8, float* q_scale, float* w_folded, const RopeArgs& rope,
+                                int32_t* err, cudaStream_t stream);
 cudaError_t launch_convert(const int32_t* logical, int64_t n_tokens, int topk, const int32_t* req_id,
                            const int32_t* block_table, int64_t bt_stride, int stride_rows, int32_t* physical,
                            int32_t* valid_counts, int32_t* err, cudaStream_t stream);
@@ -78,6 +88,7 @@ struct PrologueArgs {
   uint8_t* k_cache;
   int64_t num_blocks;
   int n_tokens;
+  RopeArgs rope;            // RoPE of q and k_new rows before the quantiser (optional)
   bool plan;
   PlanArgs p;
   uint32_t* hist;      // zeroed here for the score kernel: [hist_rows][kHistBins]

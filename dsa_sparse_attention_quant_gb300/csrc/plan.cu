@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(kPrologueThreads, 6) prologue_kernel(PrologueA
   const int64_t z_rows = a.hist != nullptr ? a.hist_rows : 0;
   // jobs: groups of 4 q rows (their loads are issued together), then K rows, then zeroing
   constexpr int kGroup = 4;
+  static_assert(kHeads % kGroup == 0, "a group of q rows belongs to one token");
   const int64_t q_groups = (q_rows + kGroup - 1) / kGroup;
   const int64_t jobs = q_groups + k_rows + z_rows;
   for (int64_t j = static_cast<int64_t>(blockIdx.x - first) * (kPrologueThreads / 32) + (threadIdx.x >> 5); j < jobs;
@@ -172,6 +173,13 @@ __global__ void __launch_bounds__(kPrologueThreads, 6) prologue_kernel(PrologueA
         const int64_t r = r0 + u;
         raw[u] = r < q_rows ? __ldg(reinterpret_cast<const uint2*>(a.q + r * kDim) + lane) : make_uint2(0, 0);
         wv[u] = (lane == 0 && r < q_rows) ? __ldg(a.w + r) : 0.0f;
+      }
+      if (a.rope.cos_sin != nullptr) {  // the group's rows are heads of one token (64 % kGroup == 0)
+        const float* cs = rope_row(a.rope, r0 / kHeads, a.err, lane);
+        if (cs != nullptr) {
+#pragma unroll
+          for (int u = 0; u < kGroup; ++u) raw[u] = rope_row_lane(raw[u], cs);
+        }
       }
 #pragma unroll
       for (int u = 0; u < kGroup; ++u) {
@@ -190,7 +198,11 @@ __global__ void __launch_bounds__(kPrologueThreads, 6) prologue_kernel(PrologueA
         if (lane == 0) flag_error(a.err, DSA_DEVERR_SLOT_RANGE);
         continue;
       }
-      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(a.k_new + t * kDim) + lane);
+      uint2 raw = __ldg(reinterpret_cast<const uint2*>(a.k_new + t * kDim) + lane);
+      if (a.rope.cos_sin != nullptr) {
+        const float* cs = rope_row(a.rope, t, a.err, lane);
+        if (cs != nullptr) raw = rope_row_lane(raw, cs);
+      }
       float s;
       const uint32_t codes = quant_row_lane(raw, &s);
       uint8_t* page = a.k_cache + (slot / kBlock) * kPageBytes;

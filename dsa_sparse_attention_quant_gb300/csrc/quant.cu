@@ -5,7 +5,9 @@
 // the `SparseAttnIndexer` body calls `indexer_k_quant_and_cache(k, kv_cache,
 // slot_mapping, quant_block_size, scale_fmt)`, and `Indexer.forward` quantises
 // q per 128-value group with ue8m0 scales and folds q_scale, softmax_scale and
-// n_head^-0.5 into the head weights. One warp handles one 128-value row: each
+// n_head^-0.5 into the head weights. With a cos/sin table, the rows are first
+// rotated on their leading 64 dims (RoPE, as `Indexer.forward` applies
+// `rotary_emb` before quantising). One warp handles one 128-value row: each
 // lane loads 8 bytes (4 bf16), the warp reduces amax with shuffles, and the
 // 32 lanes store 128 contiguous code bytes — fully coalesced, one pass over
 // HBM in each direction.
@@ -18,7 +20,7 @@ __global__ void __launch_bounds__(256) k_quant_write_kernel(const __nv_bfloat16*
                                                             int64_t row_stride,
                                                             const int64_t* __restrict__ slot_mapping,
                                                             uint8_t* __restrict__ cache, int64_t num_blocks,
-                                                            int32_t* err) {
+                                                            RopeArgs rope, int32_t* err) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   for (int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < n; t += warps) {
@@ -28,7 +30,11 @@ __global__ void __launch_bounds__(256) k_quant_write_kernel(const __nv_bfloat16*
       if (lane == 0) flag_error(err, DSA_DEVERR_SLOT_RANGE);
       continue;
     }
-    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(k + t * row_stride) + lane);
+    uint2 raw = __ldg(reinterpret_cast<const uint2*>(k + t * row_stride) + lane);
+    if (rope.cos_sin != nullptr) {
+      const float* cs = rope_row(rope, t, err, lane);  // warp-uniform
+      if (cs != nullptr) raw = rope_row_lane(raw, cs);
+    }
     float s;
     const uint32_t codes = quant_row_lane(raw, &s);
     uint8_t* page = cache + (slot / kBlock) * kPageBytes;
@@ -42,11 +48,16 @@ __global__ void __launch_bounds__(256) q_quant_fold_kernel(const __nv_bfloat16* 
                                                            const float* __restrict__ w, int64_t rows,
                                                            float softmax_scale, uint8_t* __restrict__ q_fp8,
                                                            float* __restrict__ q_scale,
-                                                           float* __restrict__ w_folded) {
+                                                           float* __restrict__ w_folded, RopeArgs rope,
+                                                           int32_t* err) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   for (int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
-    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(q + r * kDim) + lane);
+    uint2 raw = __ldg(reinterpret_cast<const uint2*>(q + r * kDim) + lane);
+    if (rope.cos_sin != nullptr) {
+      const float* cs = rope_row(rope, r / kHeads, err, lane);  // warp-uniform
+      if (cs != nullptr) raw = rope_row_lane(raw, cs);
+    }
     float s;
     const uint32_t codes = quant_row_lane(raw, &s);
     reinterpret_cast<uint32_t*>(q_fp8 + r * kDim)[lane] = codes;
@@ -114,19 +125,23 @@ static int grid_for_rows(int64_t rows, int warps_per_block) {
 }
 
 cudaError_t launch_k_quant_write(const void* k, int64_t n, int64_t row_stride, const int64_t* slot_mapping,
-                                 uint8_t* cache, int64_t num_blocks, int32_t* err, cudaStream_t stream) {
+                                 uint8_t* cache, int64_t num_blocks, const RopeArgs& rope, int32_t* err,
+                                 cudaStream_t stream) {
   if (n <= 0) return cudaSuccess;
   k_quant_write_kernel<<<grid_for_rows(n, 8), 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(k), n,
-                                                                row_stride, slot_mapping, cache, num_blocks, err);
+                                                                row_stride, slot_mapping, cache, num_blocks, rope,
+                                                                err);
   return cudaGetLastError();
 }
 
 cudaError_t launch_q_quant_fold(const void* q, const float* w, int64_t n_tokens, float softmax_scale,
-                                uint8_t* q_fp8, float* q_scale, float* w_folded, cudaStream_t stream) {
+                                uint8_t* q_fp8, float* q_scale, float* w_folded, const RopeArgs& rope, int32_t* err,
+                                cudaStream_t stream) {
   const int64_t rows = n_tokens * kHeads;
   if (rows <= 0) return cudaSuccess;
   q_quant_fold_kernel<<<grid_for_rows(rows, 8), 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(q), w, rows,
-                                                                  softmax_scale, q_fp8, q_scale, w_folded);
+                                                                  softmax_scale, q_fp8, q_scale, w_folded, rope,
+                                                                  err);
   return cudaGetLastError();
 }
 

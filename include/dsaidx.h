@@ -68,6 +68,7 @@ typedef struct CUstream_st *dsa_stream_t; /* same type as cudaStream_t */
 #define DSA_DEVERR_ID_RANGE 4u    /* top-k id past its request's block-table row */
 #define DSA_DEVERR_TIMEOUT 8u     /* a pipeline wait gave up (about 1 s); kernel returned early */
 #define DSA_DEVERR_SEQ_RANGE 16u  /* seq_len < q_len, or seq_len beyond the block-table row */
+#define DSA_DEVERR_POS_RANGE 32u  /* a RoPE position outside [0, max_pos): the row is left unrotated */
 
 #define DSA_HEADS 64
 #define DSA_HEAD_DIM 128
@@ -124,6 +125,29 @@ typedef struct DsaBatch {
 DSA_API int dsa_indexer_k_quant_write(const void *k, int64_t n_tokens, int64_t k_row_stride,
                               const int64_t *slot_mapping, uint8_t *k_cache,
                               int64_t num_blocks, int32_t *dev_err, dsa_stream_t stream);
+
+/* ------------------------------- RoPE fused into S1 and S2a (next row) */
+/* [IC] `Indexer.forward` rotates the leading qk_rope_head_dim = 64 dims of
+ * every q head and of the shared K row, `rotary_emb(positions, q_pe, k_pe)`,
+ * before the quantisation. These calls take un-rotated bf16 rows and rotate
+ * them on the way into the quantiser: half-split pairs (i, i+32), i < 32,
+ *   y[i] = x[i]*cos - x[i+32]*sin,  y[i+32] = x[i+32]*cos + x[i]*sin,
+ * each product and sum rounded in fp32 (no fused multiply-add), the result
+ * rounded to bf16 (the model's tensors are bf16), dims 64..127 unchanged.
+ *   positions  device int64 [n_tokens]: the token's position
+ *   cos_sin    device fp32 [max_pos, 64], 16-byte aligned: row p holds
+ *              cos(p*f_i) for i < 32, then sin(p*f_i)
+ * A position outside [0, max_pos) leaves the row unrotated and flags
+ * DSA_DEVERR_POS_RANGE. Everything else as dsa_indexer_k_quant_write and
+ * dsa_indexer_q_quant_fold (q rows of token t all take positions[t]). */
+DSA_API int dsa_indexer_k_rope_quant_write(const void *k, int64_t n_tokens, int64_t k_row_stride,
+                                   const int64_t *positions, const float *cos_sin, int64_t max_pos,
+                                   const int64_t *slot_mapping, uint8_t *k_cache,
+                                   int64_t num_blocks, int32_t *dev_err, dsa_stream_t stream);
+DSA_API int dsa_indexer_q_rope_quant_fold(const void *q, const float *w, int64_t n_tokens,
+                                  const int64_t *positions, const float *cos_sin, int64_t max_pos,
+                                  float softmax_scale, uint8_t *q_fp8, float *q_scale,
+                                  float *w_folded, int32_t *dev_err, dsa_stream_t stream);
 
 /* --------------------------------------- S2a: q quant + weight folding */
 /* [IC] `Indexer.forward`: q viewed as rows of 128 is quantised per row with a
@@ -284,6 +308,11 @@ typedef struct DsaStackPlan {
   int32_t topk;
   float softmax_scale;            /* <= 0 selects 128^-0.5 */
   int32_t block_stride_rows;      /* for the conversion; <= 0 selects 64 */
+  /* RoPE fused into the per-layer prologue (see dsa_indexer_q_rope_quant_fold):
+   * rope_cos_sin = NULL means q and k_new arrive already rotated. */
+  const int64_t *positions;       /* device int64 [T] */
+  const float *rope_cos_sin;      /* device fp32 [rope_max_pos, 64] or NULL */
+  int64_t rope_max_pos;
 } DsaStackPlan;
 
 DSA_API size_t dsa_layer_stack_workspace_size(const DsaBatch *batch, int32_t topk);

@@ -28,7 +28,7 @@ def test_library_exports_every_declared_symbol():
     lib = binding.load()
     for name in declared_symbols():
         assert hasattr(lib, name), name
-    assert lib.dsa_version() == 100
+    assert lib.dsa_version() == 200
     assert lib.dsa_status_string(0) == b"ok"
     assert b"invalid" in lib.dsa_status_string(1)
 
@@ -100,3 +100,20 @@ def test_ue8m0_exponent_rule_equals_division_for_every_bf16_amax():
     r = (a / np.float32(448.0)).astype(np.float32).view(np.uint32)
     up = np.where((r & 0x7FFFFF) != 0, (r & 0x7F800000) + 0x800000, r).astype(np.uint32)
     assert np.array_equal(rule.view(np.uint32), up)
+
+
+def test_rope_entry_points_reject_bad_arguments_on_the_host():
+    lib = binding.load()
+    P = ctypes.c_void_p
+    fake = P(4096)  # never dereferenced: every call below fails its host checks first
+    k_write = lib.dsa_indexer_k_rope_quant_write
+    # no cos/sin table, no positions, empty table, misaligned table
+    assert k_write(fake, 4, 128, fake, None, 16, fake, fake, 8, None, None) == binding.DSA_EINVAL
+    assert k_write(fake, 4, 128, None, fake, 16, fake, fake, 8, None, None) == binding.DSA_EINVAL
+    assert k_write(fake, 4, 128, fake, fake, 0, fake, fake, 8, None, None) == binding.DSA_EINVAL
+    assert k_write(fake, 4, 128, fake, P(4100), 16, fake, fake, 8, None, None) == binding.DSA_EINVAL
+    assert k_write(fake, 0, 128, fake, fake, 16, fake, fake, 8, None, None) == binding.DSA_OK
+    q_fold = lib.dsa_indexer_q_rope_quant_fold
+    assert q_fold(fake, fake, 4, fake, None, 16, 0.0, fake, None, fake, None, None) == binding.DSA_EINVAL
+    assert q_fold(fake, fake, 4, fake, fake, 0, 0.0, fake, None, fake, None, None) == binding.DSA_EINVAL
+    assert q_fold(fake, fake, 0, fake, fake, 16, 0.0, fake, None, fake, None, None) == binding.DSA_OK
