@@ -251,12 +251,17 @@ def run_ours(args):
         (["select"] if has_dec else []) + (["topk"] if has_pre else [])
     launches_per_step = len(kernels)
 
+    # --rope: q and the new K rows arrive un-rotated and the layer's prologue
+    # applies RoPE (positions + cos/sin table) before quantising them
+    positions = torch.from_numpy(hb.positions).to(dev) if args.rope else None
+    rope_cs = torch.from_numpy(synth.rope_cos_sin(int(hb.seq_lens.max()) + 1)).to(dev) if args.rope else None
+
     def step(i, ev=None):
         # S4: the IndexCache runner over this one-layer stack ('F'); one C-ABI call
         if ev is not None:
             dsa.binding.set_launch_events(ev)
         dsa.layer_stack_run(batch, fs, layers[i % n_rep], k, slot_mapping=slots, topk_buf=topk, phys_buf=phys,
-                            valid_buf=valid, ws=ws, dev_err=err)
+                            valid_buf=valid, ws=ws, dev_err=err, positions=positions, rope_cos_sin=rope_cs)
         if ev is not None:
             dsa.binding.set_launch_events(())
 
@@ -338,6 +343,8 @@ def run_ours(args):
             "bt": torch.from_numpy(hb.block_table.astype(np.int32)).pin_memory(),
             "req": torch.from_numpy(hb.req_id_per_token.astype(np.int32)).pin_memory(),
         }
+        if args.rope:
+            host["pos"] = torch.from_numpy(hb.positions).pin_memory()
         out_phys = torch.empty((T, k), dtype=torch.int32).pin_memory()
         out_valid = torch.empty(T, dtype=torch.int32).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in host.values())
@@ -353,6 +360,8 @@ def run_ours(args):
             batch.seq_lens.copy_(host["seq"], non_blocking=True)
             batch.block_table.copy_(host["bt"], non_blocking=True)
             batch.req_id_per_token.copy_(host["req"], non_blocking=True)
+            if args.rope:
+                positions.copy_(host["pos"], non_blocking=True)
             step(i)
             out_phys.copy_(phys, non_blocking=True)
             out_valid.copy_(valid, non_blocking=True)
@@ -428,6 +437,7 @@ def run_ours(args):
             "l2": f"inputs larger than L2: {n_rep} rotating input replicas, "
                   f"{n_rep * per_replica / 1e6:.0f} MB > 2x 129 MB",
             "parallelism": f"replica per GPU x{world}" if world > 1 else "1 GPU",
+            "rope": "q and new K rotated (RoPE) in the layer prologue" if args.rope else "inputs arrive rotated",
         },
         "roofline": roofline,
         "breakdown_us": breakdown,
@@ -782,6 +792,8 @@ def main():
     ap.add_argument("--clock-window", type=float, default=1.0, help="seconds of untimed steps while sampling clocks")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rope", action="store_true",
+                    help="q and new K arrive un-rotated; the layer prologue applies RoPE before quantising")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
