@@ -331,41 +331,58 @@ def run_ours(args):
         kernel_ms = per_kernel[:, score_cols].sum(axis=1)
         elapsed_ms = max_over_ranks(elapsed_ms, dev)
 
-        # end to end through the same calls from pinned host memory: H2D of the
-        # step's inputs and metadata, the step, D2H of the physical ids
-        host = {
-            "q": torch.from_numpy(hb.q.view(np.int16)).pin_memory(),
-            "w": torch.from_numpy(hb.w).pin_memory(),
-            "k_new": torch.from_numpy(hb.k_new.view(np.int16)).pin_memory(),
-            "slots": torch.from_numpy(hb.slot_mapping).pin_memory(),
-            "qsl": torch.from_numpy(hb.query_start_loc.astype(np.int32)).pin_memory(),
-            "seq": torch.from_numpy(hb.seq_lens.astype(np.int32)).pin_memory(),
-            "bt": torch.from_numpy(hb.block_table.astype(np.int32)).pin_memory(),
-            "req": torch.from_numpy(hb.req_id_per_token.astype(np.int32)).pin_memory(),
-        }
+        # End to end through the public API from pinned host memory. Every step
+        # uploads its inputs (q, w, new K, slots, the batch metadata, positions
+        # with --rope) packed in one pinned buffer with one copy, runs the layer
+        # runner (a prepared dsa.LayerStack on views of that upload), and reads
+        # the physical ids and valid counts back with one copy.
+        parts = [("q", hb.q), ("w", hb.w), ("k_new", hb.k_new), ("slots", hb.slot_mapping),
+                 ("qsl", hb.query_start_loc.astype(np.int32)), ("seq", hb.seq_lens.astype(np.int32)),
+                 ("bt", hb.block_table.astype(np.int32)), ("req", hb.req_id_per_token.astype(np.int32))]
         if args.rope:
-            host["pos"] = torch.from_numpy(hb.positions).pin_memory()
-        out_phys = torch.empty((T, k), dtype=torch.int32).pin_memory()
-        out_valid = torch.empty(T, dtype=torch.int32).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = out_phys.numel() * 4 + out_valid.numel() * 4
+            parts.append(("pos", hb.positions.astype(np.int64)))
+        offs, total = {}, 0
+        for name, arr in parts:
+            offs[name] = (total, np.ascontiguousarray(arr))
+            total += (arr.nbytes + 255) // 256 * 256
+        host_in = torch.empty(max(total, 256), dtype=torch.uint8).pin_memory()
+        hv = host_in.numpy()
+        for name, (o, arr) in offs.items():
+            hv[o:o + arr.nbytes] = arr.reshape(-1).view(np.uint8)
+        out_bytes = (T * k * 4 + 255) // 256 * 256 + T * 4
+        host_out = torch.empty(max(out_bytes, 256), dtype=torch.uint8).pin_memory()
+
+        def view(buf, name, dtype, shape):
+            o, arr = offs[name]
+            return buf[o:o + arr.nbytes].view(dtype).view(shape)
+
+        stacks, dev_in = [], []
+        dev_out = torch.empty(max(out_bytes, 256), dtype=torch.uint8, device=dev)
+        phys_e = dev_out[:T * k * 4].view(torch.int32).view(T, k)
+        voff = (T * k * 4 + 255) // 256 * 256
+        valid_e = dev_out[voff:voff + T * 4].view(torch.int32)
+        for r in reps:
+            d = torch.empty(max(total, 256), dtype=torch.uint8, device=dev)
+            d.copy_(host_in)
+            be = dsa.Batch(view(d, "qsl", torch.int32, (-1,)), view(d, "seq", torch.int32, (-1,)),
+                           view(d, "bt", torch.int32, tuple(hb.block_table.shape)), view(d, "req", torch.int32, (-1,)),
+                           hb.num_decodes, hb.num_blocks, batch.max_seq_len, batch.num_decode_tokens)
+            le = [dict(q=view(d, "q", torch.bfloat16, (T, 64, 128)), w=view(d, "w", torch.float32, (T, 64)),
+                       k_new=view(d, "k_new", torch.bfloat16, (T, 128)), k_cache=r.k_cache)]
+            stacks.append(dsa.LayerStack(be, fs, le, k, slot_mapping=view(d, "slots", torch.int64, (-1,)),
+                                         topk_buf=topk, phys_buf=phys_e, valid_buf=valid_e, ws=ws, dev_err=err,
+                                         positions=view(d, "pos", torch.int64, (-1,)) if args.rope else None,
+                                         rope_cos_sin=rope_cs))
+            dev_in.append(d)
+        h2d, d2h = host_in.numel(), host_out.numel()  # the bytes each step copies
+        cur = torch.cuda.current_stream()
 
         def e2e_step(i):
-            r = reps[i % n_rep]
-            r.q.view(torch.int16).copy_(host["q"], non_blocking=True)
-            r.w.copy_(host["w"], non_blocking=True)
-            r.k_new.view(torch.int16).copy_(host["k_new"], non_blocking=True)
-            slots.copy_(host["slots"], non_blocking=True)
-            batch.query_start_loc.copy_(host["qsl"], non_blocking=True)
-            batch.seq_lens.copy_(host["seq"], non_blocking=True)
-            batch.block_table.copy_(host["bt"], non_blocking=True)
-            batch.req_id_per_token.copy_(host["req"], non_blocking=True)
-            if args.rope:
-                positions.copy_(host["pos"], non_blocking=True)
-            step(i)
-            out_phys.copy_(phys, non_blocking=True)
-            out_valid.copy_(valid, non_blocking=True)
-            torch.cuda.current_stream().synchronize()
+            j = i % n_rep
+            dev_in[j].copy_(host_in, non_blocking=True)
+            stacks[j].run(cur)
+            host_out.copy_(dev_out, non_blocking=True)
+            cur.synchronize()
 
         for i in range(args.warmup):
             e2e_step(i)

@@ -7,6 +7,7 @@ seeded synthetic inputs.
 from .binding import (  # noqa: F401
     Batch,
     DsaError,
+    LayerStack,
     check_device_error,
     indexer_k_quant_write,
     indexer_k_rope_quant_write,

@@ -393,46 +393,63 @@ def layer_stack_workspace_size(batch: Batch, topk: int) -> int:
     return int(load().dsa_layer_stack_workspace_size(ctypes.byref(batch.c), int(topk)))
 
 
+class LayerStack:
+    """A prepared ``dsa_layer_stack_run``: the C plan, the per-layer input table,
+    the output buffers and the workspace are built once; ``run()`` issues the
+    call again on the same tensors (whose contents may change between runs).
+    ``layers[l]`` is None for 'S' layers, else a dict with tensors ``q``, ``w``,
+    ``k_cache`` and optionally ``k_new``. ``consumer(layer, producer, phys_ptr,
+    valid_ptr)`` is called per layer. With ``rope_cos_sin`` ([max_pos, 64]
+    fp32) and ``positions`` (int64 [T]), q and k_new arrive un-rotated and each
+    F layer rotates them (RoPE) on the way into the quantiser."""
+
+    def __init__(self, batch: Batch, fs: str, layers, topk: int, slot_mapping=None, topk_buf=None, phys_buf=None,
+                 valid_buf=None, consumer=None, ws=None, softmax_scale: float = 0.0, block_stride_rows: int = 0,
+                 dev_err=None, positions=None, rope_cos_sin=None):
+        n = len(fs)
+        self._arr = (DsaLayerInputsC * max(n, 1))()
+        self._keep = [batch, slot_mapping, dev_err, positions, rope_cos_sin]
+        for l, L in enumerate(layers):
+            if L is None:
+                continue
+            self._keep.append(L)
+            self._arr[l] = DsaLayerInputsC(L["q"].data_ptr(), L["w"].data_ptr(),
+                                           L["k_new"].data_ptr() if L.get("k_new") is not None else None,
+                                           L["k_cache"].data_ptr())
+        max_pos = 0
+        if rope_cos_sin is not None:
+            max_pos = _rope_table(rope_cos_sin)
+            _need(positions, torch.int64, "positions")
+        self._fs = fs.encode()
+        self._plan = DsaStackPlanC(n, self._fs, self._arr, int(topk), float(softmax_scale), int(block_stride_rows),
+                                   _ptr(positions) if rope_cos_sin is not None else None, _ptr(rope_cos_sin),
+                                   max_pos)
+        dev = torch.device("cuda", torch.cuda.current_device())
+        T = batch.num_tokens
+        self.topk_buf = topk_buf if topk_buf is not None else torch.empty((T, int(topk)), dtype=torch.int32,
+                                                                          device=dev)
+        self.phys_buf = phys_buf if phys_buf is not None else torch.empty((T, int(topk)), dtype=torch.int32,
+                                                                          device=dev)
+        self.valid_buf = valid_buf if valid_buf is not None else torch.empty(T, dtype=torch.int32, device=dev)
+        self.ws = _workspace(layer_stack_workspace_size(batch, topk), dev, ws)
+        if consumer is not None:
+            self._cb = CONSUMER_FN(lambda l, p, ph, va, u: consumer(int(l), int(p), ph, va))
+        else:
+            self._cb = CONSUMER_FN()
+        self._fn = load().dsa_layer_stack_run
+        self._args = (ctypes.byref(self._plan), ctypes.byref(batch.c), _ptr(slot_mapping), _ptr(self.topk_buf),
+                      _ptr(self.phys_buf), _ptr(self.valid_buf), self._cb, None, _ptr(self.ws), self.ws.numel(),
+                      _ptr(dev_err))
+
+    def run(self, stream=None):
+        st = self._fn(*self._args, _stream(stream))
+        _check(st, "dsa_layer_stack_run")
+        return self.topk_buf, self.phys_buf, self.valid_buf
+
+
 def layer_stack_run(batch: Batch, fs: str, layers, topk: int, slot_mapping=None, topk_buf=None, phys_buf=None,
                     valid_buf=None, consumer=None, ws=None, softmax_scale: float = 0.0, block_stride_rows: int = 0,
                     dev_err=None, stream=None, positions=None, rope_cos_sin=None):
-    """Run a stack of layers. ``layers[l]`` is None for 'S' layers, else a dict
-    with tensors ``q``, ``w``, ``k_cache`` and optionally ``k_new``.
-    ``consumer(layer, producer, phys_ptr, valid_ptr)`` is called per layer.
-    With ``rope_cos_sin`` ([max_pos, 64] fp32) and ``positions`` (int64 [T]),
-    q and k_new arrive un-rotated and each F layer rotates them (RoPE) on the
-    way into the quantiser."""
-    n = len(fs)
-    arr = (DsaLayerInputsC * max(n, 1))()
-    keep = []
-    for l, L in enumerate(layers):
-        if L is None:
-            continue
-        keep.append(L)
-        arr[l] = DsaLayerInputsC(L["q"].data_ptr(), L["w"].data_ptr(),
-                                 L["k_new"].data_ptr() if L.get("k_new") is not None else None,
-                                 L["k_cache"].data_ptr())
-    max_pos = 0
-    if rope_cos_sin is not None:
-        max_pos = _rope_table(rope_cos_sin)
-        _need(positions, torch.int64, "positions")
-    plan = DsaStackPlanC(n, fs.encode(), arr, int(topk), float(softmax_scale), int(block_stride_rows),
-                         _ptr(positions) if rope_cos_sin is not None else None, _ptr(rope_cos_sin), max_pos)
-    dev = torch.device("cuda", torch.cuda.current_device())
-    T = batch.num_tokens
-    if topk_buf is None:
-        topk_buf = torch.empty((T, int(topk)), dtype=torch.int32, device=dev)
-    if phys_buf is None:
-        phys_buf = torch.empty((T, int(topk)), dtype=torch.int32, device=dev)
-    if valid_buf is None:
-        valid_buf = torch.empty(T, dtype=torch.int32, device=dev)
-    ws = _workspace(layer_stack_workspace_size(batch, topk), dev, ws)
-    if consumer is not None:
-        cb = CONSUMER_FN(lambda l, p, ph, va, u: consumer(int(l), int(p), ph, va))
-    else:
-        cb = CONSUMER_FN()
-    st = load().dsa_layer_stack_run(ctypes.byref(plan), ctypes.byref(batch.c), _ptr(slot_mapping), _ptr(topk_buf),
-                                    _ptr(phys_buf), _ptr(valid_buf), cb, None, _ptr(ws), ws.numel(),
-                                    _ptr(dev_err), _stream(stream))
-    _check(st, "dsa_layer_stack_run")
-    return topk_buf, phys_buf, valid_buf
+    """Run a stack of layers once (see ``LayerStack`` for the arguments)."""
+    return LayerStack(batch, fs, layers, topk, slot_mapping, topk_buf, phys_buf, valid_buf, consumer, ws,
+                      softmax_scale, block_stride_rows, dev_err, positions, rope_cos_sin).run(stream)
