@@ -1,0 +1,61 @@
+"""The layer runner captured once in a CUDA graph and replayed on new inputs.
+
+The runner allocates nothing, never synchronises and reads nothing back, and
+every kernel parameter (tensor maps included) is captured by value, so a graph
+of one call replays on the same buffers whatever they hold. Here the call is
+captured on one step's inputs, the buffers are then overwritten with another
+step's (same shapes and metadata, other q, w, K), and the replay's top-k must
+match the oracle on the new inputs."""
+import numpy as np
+import pytest
+import torch
+
+import dsa_sparse_attention_quant_gb300 as dsa
+import oracle
+from dsa_sparse_attention_quant_gb300 import synth
+from oracle import compare
+from tests.gpu_harness import DEV, bf16_tensor
+
+pytestmark = pytest.mark.gpu
+
+
+def test_captured_layer_run_replays_on_new_inputs():
+    shape = ([900, 2500, 64], [(700, 500)])
+    first = synth.make_batch(41, *shape, 256, table_seed=40)
+    second = synth.make_batch(42, *shape, 256, table_seed=40)  # same metadata and pages, other values
+    assert np.array_equal(first.block_table, second.block_table)
+    batch = dsa.Batch.from_host(first, DEV)
+    q, w, kn = bf16_tensor(first.q), torch.from_numpy(first.w).to(DEV), bf16_tensor(first.k_new)
+    slots = torch.from_numpy(first.slot_mapping).to(DEV)
+    cache = torch.zeros((first.num_blocks, 8448), dtype=torch.uint8, device=DEV)
+    ctx_slots = torch.from_numpy(first.ctx_slots).to(DEV)
+    dsa.indexer_k_quant_write(bf16_tensor(first.ctx_k), ctx_slots, cache)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    stack = dsa.LayerStack(batch, "F", [dict(q=q, w=w, k_new=kn, k_cache=cache)], first.topk, slot_mapping=slots,
+                           dev_err=err)
+    stack.run()  # first call on the device outside the capture
+    torch.cuda.synchronize()
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        stack.run()
+    torch.cuda.current_stream().wait_stream(side)
+
+    # the second step's values into the same buffers, then replay
+    q.copy_(bf16_tensor(second.q))
+    w.copy_(torch.from_numpy(second.w).to(DEV))
+    kn.copy_(bf16_tensor(second.k_new))
+    cache.zero_()
+    dsa.indexer_k_quant_write(bf16_tensor(second.ctx_k), ctx_slots, cache)
+    stack.topk_buf.fill_(-7)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref_cache = oracle.fill_cache(second)
+    assert np.array_equal(cache.cpu().numpy(), ref_cache), "the replay's K write differs"
+    rows = np.arange(second.num_tokens)
+    _, scores = oracle.indexer(second, ref_cache, rows=rows, with_scores=True)
+    fails = compare.check_topk(stack.topk_buf.cpu().numpy(), scores, second.positions + 1, second.topk)
+    assert not fails, f"top-k mismatches in {len(fails)} rows, first {fails[0]}"
