@@ -66,6 +66,7 @@ def _bind(lib):
         "ora_k_quant_write": (I64, [P, I64, P, P, I64]),
         "ora_q_quant": (None, [P, I64, P, P]),
         "ora_rope": (I64, [P, I64, I64, P, P, I64, P]),
+        "ora_gather_rows": (I64, [P, I64, I64, I64, P, I64, I32, P]),
         "ora_logits_row": (None, [P, P, P, P, P, I64, P]),
         "ora_topk_row": (None, [P, I64, I32, P]),
         "ora_indexer": (I64, [P, P, P, P, I64, P, P, P, I64, I32, P, P, I64]),
@@ -159,6 +160,17 @@ class Oracle:
         out = np.empty_like(x)
         bad = self._lib.ora_rope(_p(x), x.size // DIM, int(rows_per_token), _p(pos), _p(cs), int(cs.shape[0]),
                                  _p(out))
+        return out, int(bad)
+
+    def gather_rows(self, rows: np.ndarray, physical, row_bytes: int):
+        """out[t, j] = the first row_bytes bytes of rows[physical[t, j]] (uint8 [R, stride]),
+        zeros for -1 or an out-of-range id; returns (out, out-of-range count)."""
+        assert rows.dtype == np.uint8 and rows.ndim == 2 and rows.flags["C_CONTIGUOUS"]
+        ph = _c(physical, np.int32)
+        T, k = ph.shape
+        out = np.full((T, k, row_bytes), 0xA5, np.uint8)  # a row the gather skipped would show
+        bad = self._lib.ora_gather_rows(_p(rows), rows.shape[0], int(row_bytes), rows.shape[1], _p(ph), T, k,
+                                        _p(out))
         return out, int(bad)
 
     def fill_cache(self, batch, cache: np.ndarray | None = None, include_new: bool = True):

@@ -373,3 +373,31 @@ int ora_schedule(int n_layers, int use_index_cache, int freq, int offset,
   }
   return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* The consumer's gather (next row 4): "IndexCache：DeepSeek 稀疏注意力中的跨层
+ * 索引复用" — the sparse MLA of every layer of a group reads, for each query
+ * token, the KV rows of the k selected keys; "vllm.v1.attention.backends.mla.
+ * index_group" converts the ids to physical slots for exactly that read. The
+ * row format is not on the pages, so the gather is by bytes: out[t][j] = the
+ * row_bytes bytes of physical row physical[t][j] (rows row_stride bytes
+ * apart), zeros where the id is -1; an id >= num_rows (or < -1) also gives
+ * zeros and is counted. Returns that count. */
+int64_t ora_gather_rows(const uint8_t *rows, int64_t num_rows, int64_t row_bytes, int64_t row_stride,
+                        const int32_t *physical, int64_t n_tokens, int topk, uint8_t *out) {
+  int64_t t, bad = 0;
+  int j;
+  for (t = 0; t < n_tokens; ++t) {
+    for (j = 0; j < topk; ++j) {
+      const int32_t id = physical[t * topk + j];
+      uint8_t *dst = out + (t * topk + j) * row_bytes;
+      if (id >= 0 && id < num_rows) {
+        memcpy(dst, rows + (int64_t)id * row_stride, (size_t)row_bytes);
+      } else {
+        memset(dst, 0, (size_t)row_bytes);
+        if (id != -1) ++bad;
+      }
+    }
+  }
+  return bad;
+}

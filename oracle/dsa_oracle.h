@@ -64,6 +64,10 @@ void ora_convert(const int32_t *logical, int64_t n_tokens, int topk,
 int ora_schedule(int n_layers, int use_index_cache, int freq, int offset,
                  const char *pattern, char *fs_out, int32_t *producer_out);
 
+/* The consumer's gather by physical row (bytes); returns out-of-range ids. */
+int64_t ora_gather_rows(const uint8_t *rows, int64_t num_rows, int64_t row_bytes, int64_t row_stride,
+                        const int32_t *physical, int64_t n_tokens, int topk, uint8_t *out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -475,4 +475,17 @@ def pin_rope_error_bound(ora, n: int = 2000):
     assert np.all(np.abs(r_out - r_in) <= r_in * 2.0 ** -7 + 1e-30)
 
 
+def pin_gather_rows_vs_library(ora):
+    # numpy's take along the row axis, zero rows for -1 and out-of-range ids
+    rng = np.random.default_rng(5)
+    rows = rng.integers(0, 256, size=(300, 160), dtype=np.uint8)
+    phys = rng.integers(-1, 300, size=(7, 33)).astype(np.int32)
+    phys[2, 3], phys[4, 0] = 300, -5  # out of range: zeros, counted
+    out, bad = ora.gather_rows(rows, phys, 144)
+    ok = (phys >= 0) & (phys < 300)
+    ref = np.zeros((7, 33, 144), np.uint8)
+    ref[ok] = np.take(rows[:, :144], phys[ok], axis=0)
+    assert bad == 2 and np.array_equal(out, ref)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

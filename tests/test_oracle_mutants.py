@@ -40,6 +40,8 @@ MUTANTS = {
                               "const float s = cos_sin[p * ORA_ROPE + i], c = cos_sin[p * ORA_ROPE + ORA_ROPE / 2 + i];")],
     "rope_token_of_row": [("const int64_t p = positions[r / rows_per_token];", "const int64_t p = positions[r % rows_per_token];")],
     "rope_truncates": [("  u += 0x7FFFu + ((u >> 16) & 1u);\n", "")],
+    "gather_row_stride_ignored": [("rows + (int64_t)id * row_stride", "rows + (int64_t)id * row_bytes")],
+    "gather_keeps_stale_rows": [("        memset(dst, 0, (size_t)row_bytes);\n", "")],
     "convert_counts_padding": [("        ++valid;\n", ""), ("        physical[t * topk + j] = -1;\n",
                                                         "        physical[t * topk + j] = -1;\n        ++valid;\n")],
 }
