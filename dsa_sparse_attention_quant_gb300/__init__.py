@@ -9,6 +9,7 @@ from .binding import (  # noqa: F401
     DsaError,
     LayerStack,
     check_device_error,
+    gather_rows,
     indexer_k_quant_write,
     indexer_k_rope_quant_write,
     indexer_logits,

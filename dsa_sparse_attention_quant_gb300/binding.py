@@ -37,7 +37,7 @@ SYMBOLS = [
     "dsa_topk_logical_to_physical", "dsa_schedule_build",
     "dsa_layer_stack_workspace_size", "dsa_layer_stack_run",
     "dsa_indexer_logits_topk_static", "dsa_set_launch_events",
-    "dsa_indexer_k_rope_quant_write", "dsa_indexer_q_rope_quant_fold",
+    "dsa_indexer_k_rope_quant_write", "dsa_indexer_q_rope_quant_fold", "dsa_gather_rows",
 ]
 STATIC_WORKSPACE_BYTES = 32 << 20
 
@@ -128,6 +128,7 @@ def load(build_if_missing: bool = True):
             "dsa_set_launch_events": (ctypes.c_int, [P, I32]),
             "dsa_indexer_k_rope_quant_write": (ctypes.c_int, [P, I64, I64, P, P, I64, P, P, I64, P, P]),
             "dsa_indexer_q_rope_quant_fold": (ctypes.c_int, [P, P, I64, P, P, I64, F32, P, P, P, P, P]),
+            "dsa_gather_rows": (ctypes.c_int, [P, I64, I64, I64, P, I64, I32, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -216,6 +217,20 @@ def indexer_k_quant_write(k, slot_mapping, k_cache, dev_err=None, stream=None):
     st = load().dsa_indexer_k_quant_write(_ptr(k), n, row_stride, _ptr(slot_mapping), _ptr(k_cache),
                                           int(k_cache.shape[0]), _ptr(dev_err), _stream(stream))
     _check(st, "dsa_indexer_k_quant_write")
+
+
+def gather_rows(rows, physical, row_bytes: int, out=None, dev_err=None, stream=None):
+    """The consumer's gather: out[t, j] = the first row_bytes bytes of
+    rows[physical[t, j]] (uint8 [R, stride]); zero rows for -1."""
+    _need(rows, torch.uint8, "rows")
+    _need(physical, torch.int32, "physical")
+    T, k = physical.shape
+    if out is None:
+        out = torch.empty((T, k, int(row_bytes)), dtype=torch.uint8, device=physical.device)
+    st = load().dsa_gather_rows(_ptr(rows), int(rows.shape[0]), int(row_bytes), int(rows.stride(0)),
+                                _ptr(physical), T, k, _ptr(out), _ptr(dev_err), _stream(stream))
+    _check(st, "dsa_gather_rows")
+    return out
 
 
 def _rope_table(cos_sin):

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libdsaidx.so")
-SOURCES = ["api.cu", "quant.cu", "plan.cu", "logits.cu", "topk.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "quant.cu", "plan.cu", "logits.cu", "topk.cu", "noalloc.cu", "gather.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "kernels.h")] + [os.path.join(ROOT, "include", "dsaidx.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

@@ -301,6 +301,21 @@ int dsa_indexer_q_quant_fold(const void* q, const float* w, int64_t n_tokens, fl
                                        stream));
 }
 
+int dsa_gather_rows(const uint8_t* rows, int64_t num_rows, int64_t row_bytes, int64_t row_stride,
+                    const int32_t* physical, int64_t n_tokens, int32_t topk, uint8_t* out, int32_t* dev_err,
+                    dsa_stream_t stream) {
+  if (num_rows < 0 || row_bytes <= 0 || row_bytes % 16 != 0 || row_stride < row_bytes || row_stride % 16 != 0 ||
+      n_tokens < 0 || topk < 1)
+    return DSA_EINVAL;
+  if (n_tokens == 0) return DSA_OK;
+  if (!physical || !out || !aligned16(out) || (num_rows > 0 && (!rows || !aligned16(rows)))) return DSA_EINVAL;
+  int sms;
+  int st = device_sms(&sms);
+  if (st != DSA_OK) return st;
+  return from_cuda(launch_gather_rows(rows, num_rows, row_bytes, row_stride, physical, n_tokens * topk, out, sms,
+                                      dev_err, stream));
+}
+
 int dsa_indexer_k_rope_quant_write(const void* k, int64_t n_tokens, int64_t k_row_stride, const int64_t* positions,
                                    const float* cos_sin, int64_t max_pos, const int64_t* slot_mapping,
                                    uint8_t* k_cache, int64_t num_blocks, int32_t* dev_err, dsa_stream_t stream) {

@@ -172,4 +172,10 @@ cudaError_t launch_topk(const float* logits, int64_t ld, const int32_t* qsl, con
 // chunk; the last CTA of a row resolves its boundary bin.
 cudaError_t launch_select(const SelectArgs& a, const TopkPhys* phys, int num_sms, cudaStream_t stream);
 
+// The consumer's gather: out[i] = row physical[i] (row_bytes, a multiple of
+// 16, from rows row_stride bytes apart), zeros for -1 or out of range.
+cudaError_t launch_gather_rows(const uint8_t* rows, int64_t num_rows, int64_t row_bytes, int64_t row_stride,
+                               const int32_t* physical, int64_t n_ids, uint8_t* out, int num_sms, int32_t* err,
+                               cudaStream_t stream);
+
 }  // namespace dsa

@@ -278,6 +278,23 @@ DSA_API int dsa_schedule_build(int32_t n_layers, int32_t use_index_cache, int32_
                        int32_t offset, const char *pattern, char *fs_out,
                        int32_t *producer_out);
 
+/* ------------------------------- the consumer's gather (next row 4) */
+/* [IC]: the sparse MLA of each layer reads, per query token, the KV rows of the
+ * selected keys; [IG] `_convert_once` gives it physical slots for that read.
+ * The row format is not on the pages, so this copies bytes:
+ *   out[t][j] = rows[physical[t][j] * row_stride .. + row_bytes)
+ * and zeros where the id is -1 (rows shorter than k keep -1 in the tail).
+ *   rows        device uint8, num_rows rows row_stride bytes apart, 16-byte aligned
+ *   row_bytes   bytes per row copied: > 0, a multiple of 16, <= row_stride
+ *   row_stride  a multiple of 16
+ *   physical    device int32 [n_tokens, topk] (dsa_topk_logical_to_physical,
+ *               or phys_buf of the layer runner)
+ *   out         device uint8 [n_tokens, topk, row_bytes], 16-byte aligned, written
+ * An id outside [-1, num_rows) gives a zero row and flags DSA_DEVERR_ID_RANGE. */
+DSA_API int dsa_gather_rows(const uint8_t *rows, int64_t num_rows, int64_t row_bytes, int64_t row_stride,
+                            const int32_t *physical, int64_t n_tokens, int32_t topk, uint8_t *out,
+                            int32_t *dev_err, dsa_stream_t stream);
+
 /* ------------------------------------------- the layer-schedule runner */
 /* One decoding step over a stack of DSA layers with IndexCache: [IC] F/S
  * layer forward and [IG] `SparseMLAIndexGroup` (one group = an F layer and
