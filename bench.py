@@ -710,6 +710,56 @@ def run_stack(args):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------------- gather
+
+GATHER_DESC = ("gather64x2048: the consumer's read of the selected rows — 64 decode tokens x 2048 physical "
+               "slots each, 656-byte rows (an FP8 MLA KV row size) from a 2,097,152-row paged cache "
+               "(1.38 GB), ids drawn uniformly (seeded)")
+
+
+def run_gather(args):
+    """Times dsa_gather_rows on its own: value = gathered rows per second."""
+    import torch
+
+    import dsa_sparse_attention_quant_gb300 as dsa
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    R, T, k, rb = 64 * 32768, 64, 2048, 656
+    g = torch.Generator(device=dev)
+    g.manual_seed(6000)
+    rows = torch.randint(0, 256, (R, rb), dtype=torch.uint8, device=dev, generator=g)
+    n_sets = 4  # rotating id sets
+    phys = [torch.randint(0, R, (T, k), dtype=torch.int32, device=dev, generator=g) for _ in range(n_sets)]
+    out = torch.empty((T, k, rb), dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    for i in range(args.warmup):
+        dsa.gather_rows(rows, phys[i % n_sets], rb, out=out, dev_err=err)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        a.record()
+        for i in range(args.steps):
+            dsa.gather_rows(rows, phys[i % n_sets], rb, out=out, dev_err=err)
+        b.record()
+        torch.cuda.synchronize()
+    if dsa.check_device_error(err):
+        raise SystemExit(f"device error word set: {int(err.item()):#x}")
+    ms = a.elapsed_time(b) / args.steps
+    moved = 2 * T * k * rb + T * k * 4
+    hbm_peak, _, _, peak_src = read_peaks()
+    gbs = moved / (ms / 1e3) / 1e9
+    print(json.dumps({
+        "metric": "gathered KV rows/s (the consumer's read of the selected rows)", "value": T * k / (ms / 1e3),
+        "unit": "rows/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": GATHER_DESC, "l2": "inputs larger than L2 (1.38 GB of rows, 4 rotating id sets)"},
+        "roofline": {"bound": "hbm", "kernel": "dsa::gather_rows_kernel", "achieved": gbs, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": gbs / hbm_peak, "traffic": None, "algorithmic_bytes_per_launch": moved,
+                     "avg_launch_ms": ms, "peak_source": f"{peak_src}: MEASURED_PEAKS.json hbm_gbs"},
+        "gpu_launches": args.steps, "clocks": clocks.summary(),
+    }), flush=True)
+
+
 # --------------------------------------------------------------------- oracle
 
 def oracle_state(hb):
@@ -818,6 +868,8 @@ def main():
         run_reference(args)
     elif args.workload == "stack61":
         run_stack(args)
+    elif args.workload == "gather64x2048":
+        run_gather(args)
     else:
         run_ours(args)
 
