@@ -232,7 +232,7 @@ int run_logits(const DsaBatch* b, const uint8_t* q_fp8, const float* w_folded, c
 
 // Top-k of every row from scores built with the decode rows' histograms:
 // the decode rows by the multi-CTA select (chunks of each row in parallel,
-// round 1 from the histograms), the others by one CTA per row.
+// pass 1 from the histograms), the others by one CTA per row.
 int run_topk(const DsaBatch* b, const IndexerWs& ws, int64_t ld, int32_t topk, int32_t* out, const TopkPhys* phys,
              int sms, cudaStream_t stream) {
   SelectArgs sa{ws.logits, ld, b->query_start_loc, b->seq_lens, b->req_id_per_token, b->num_reqs,

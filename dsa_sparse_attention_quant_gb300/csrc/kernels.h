@@ -162,7 +162,7 @@ cudaError_t launch_logits(int ntok_per_block, const CUtensorMap* tmap_k, const C
                           SegmentPlan plan, const LogitsArgs& a, int num_sms, cudaStream_t stream);
 
 // Rows [row_begin, n_tokens): one CTA per row. Rows t < hist_rows take their
-// first radix round from hist (the score kernel's histograms; may be nullptr).
+// first radix pass from hist (the score kernel's histograms; may be nullptr).
 cudaError_t launch_topk(const float* logits, int64_t ld, const int32_t* qsl, const int32_t* seq_lens,
                         const int32_t* req_id, int num_reqs, int row_begin, int n_tokens, int topk, int32_t* out,
                         const TopkPhys* phys, const uint32_t* hist, int hist_rows, cudaStream_t stream);

@@ -18,7 +18,7 @@
 //  * Warp roles: warp 0 issues TMA (K pages, K scales, q block, w' block),
 //    warp 1 issues the MMAs, the remaining warps read TMEM and apply
 //    ReLU, the w' reduction and the K scale, and store fp32 scores.
-//  * Decode rows also get their score histogram (round 1 of the top-k radix
+//  * Decode rows also get their score histogram (pass 1 of the top-k radix
 //    select), so the top-k never scans a decode row to find its boundary bin.
 //  * Every wait is bounded in time (DSA_DEVERR_TIMEOUT, then an orderly exit).
 #include "common.cuh"
@@ -57,7 +57,7 @@ struct LogitsCfg {
   static constexpr int kNumBars = 2 * kStages + 4 + 2 * kAcc + 1 + kEpiWG;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffMeta = kOffMisc + 16;  // 2 QMeta (2 x 24 B), the slice (4 ints), scan scratch (33 ints)
-  // decode: one score histogram per epilogue warpgroup (first radix round of the top-k)
+  // decode: one score histogram per epilogue warpgroup (first radix pass of the top-k)
   static constexpr int kHistBytes = NTOK == 1 ? kEpiWG * kHistBins * 4 : 0;
   static constexpr int kOffHist = (kOffMeta + 2 * 24 + 4 * 4 + 33 * 4 + 127) / 128 * 128;
   static constexpr int kSmemBytes = kOffHist + kHistBytes + 1024;  // + slack to align the base to 1024

@@ -1,6 +1,6 @@
 // select.cuh — exact per-row top-k by radix select over order-preserving
 // 32-bit keys of fp32 scores (a > b iff key(a) > key(b)), shared by the top-k
-// kernels and the decode score kernel's tail (sm_103a).
+// kernels: the per-row top-k and the multi-CTA decode select (sm_103a).
 //
 // The top-k op of "IndexCache：DeepSeek 稀疏注意力中的跨层索引复用" (atomage.cn)
 // fills a row of the shared `topk_indices_buffer` with the ids of the
@@ -9,10 +9,10 @@
 // physical slots, block_table[req][id/64] * block_stride_rows + id%64. Ids are
 // emitted in no particular order.
 //
-// Round 1 bins the keys by their top 11 bits; the bin holding the k-th
+// Pass 1 bins the keys by their top 11 bits; the bin holding the k-th
 // largest key (the boundary bin) is found by a block-wide scan from the top.
 // Every key above that bin is taken in one pass while the bin's keys are
-// gathered; two more rounds (11 and 10 bits) on the gathered keys find the
+// gathered; two more passes (11 and 10 bits) on the gathered keys find the
 // k-th key exactly, and the keys above it plus as many equal keys as are
 // still needed are taken. The ids are collected in shared memory and written
 // out (with their physical slots) in one coalesced pass.
@@ -23,7 +23,7 @@
 
 namespace dsa {
 
-constexpr int kSelBins = kHistBins;  // 2048: round-1 bins = the score kernel's histograms
+constexpr int kSelBins = kHistBins;  // 2048: pass-1 bins = the score kernel's histograms
 constexpr int kCandCap = 4096;       // most boundary-bin keys ever gathered in shared memory
 constexpr int kMaxTopk = 4096;       // largest k the library accepts
 
@@ -138,10 +138,10 @@ __device__ void write_ids(const uint32_t* oid, int topk, const RowOut& o, bool* 
   }
 }
 
-// Rounds 2 and 3 on the boundary bin b1's keys cand_key(0..m) (ids cand_id),
+// Passes 2 and 3 on the boundary bin b1's keys cand_key(0..m) (ids cand_id),
 // of which `need` are still to be taken after the n_up keys above the bin;
 // the keys above the k-th and as many ties as needed go to put(position, id)
-// at positions n_up, n_up + 1, ... (below topk). hist holds round 1 of the
+// at positions n_up, n_up + 1, ... (below topk). hist holds pass 1 of the
 // row on entry and is reused.
 template <int NT, typename CandKey, typename CandId, typename Put>
 __device__ void resolve_boundary(CandKey cand_key, CandId cand_id, uint32_t m, uint32_t b1, uint32_t need,
@@ -199,7 +199,7 @@ __device__ void resolve_boundary(CandKey cand_key, CandId cand_id, uint32_t m, u
 // written through o. Warp w owns a contiguous chunk of the row: it counts,
 // a scan over the warps gives each its offsets, and it places its keys in
 // order, so the reads stay coalesced. hist (shared, kSelBins) holds the
-// keys' round-1 histogram on entry; ckey / cidx (shared, cap each) take
+// keys' pass-1 histogram on entry; ckey / cidx (shared, cap each) take
 // the boundary bin's keys; oid (shared, topk) collects the ids.
 template <int NT, typename KeyAt>
 __device__ void select_row(KeyAt key_at, int n, uint32_t* hist, uint32_t* ckey, uint32_t* cidx, uint32_t* oid,

@@ -12,10 +12,10 @@
 // Both kernels are exact radix selects (select.cuh); ids are emitted in no
 // particular order.
 //  * topk_kernel: one 256-thread CTA per row, shared memory sized to the row
-//    (several rows run per SM). Round 1 comes from the histogram the score
+//    (several rows run per SM). Pass 1 comes from the histogram the score
 //    kernel built when there is one, else from the row. Rows that fit are
 //    staged once in shared memory; longer rows are re-read from L2.
-//  * select_kernel: decode rows, whose round-1 histogram the score kernel
+//  * select_kernel: decode rows, whose pass-1 histogram the score kernel
 //    accumulated. Several CTAs per row place the keys above the boundary bin
 //    and collect the boundary bin's keys; the last CTA of the row to finish
 //    resolves the boundary bin on those candidates only.
@@ -195,7 +195,7 @@ cudaError_t launch_topk(const float* logits, int64_t ld, const int32_t* qsl, con
 
 // ---------------------------------------------------------------------------
 // Multi-CTA select for decode rows: CTA (c, t) takes scores [c*chunk,
-// (c+1)*chunk) of row t. Round 1 is the score kernel's histogram of the row,
+// (c+1)*chunk) of row t. Pass 1 is the score kernel's histogram of the row,
 // so every chunk knows the boundary bin at once: it places its keys above the
 // bin (one global reservation per CTA) and its boundary-bin keys (as
 // candidates in global memory); the row's last CTA resolves the candidates.
@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(SelectArgs a, Ph
       __syncthreads();
     }
     auto cand_at = [&](uint32_t j) -> uint2 { return staged ? cands[j] : __ldcg(crow + j); };
-    // hist still holds the row's round 1: 1 <= need <= m
+    // hist still holds the row's pass 1: 1 <= need <= m
     resolve_boundary<kSelectThreads>([&](uint32_t j) -> uint32_t { return cand_at(j).x; },
                                      [&](uint32_t j) -> uint32_t { return cand_at(j).y; }, m, b1,
                                      static_cast<uint32_t>(a.topk) - above, above, hist,
