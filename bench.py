@@ -66,18 +66,23 @@ STACK_DESC = ("stack61: 61 DSA layers, IndexCache freq=4 (skip = max(l-1,0)%4 !=
               "with freq=1 (all 61 layers run the indexer)")
 
 
-def kernel_source_sha() -> str:
+LOGITS_SOURCES = ("logits.cu", "common.cuh")
+GATHER_SOURCES = ("gather.cu", "common.cuh")
+
+
+def kernel_source_sha(sources=LOGITS_SOURCES) -> str:
+    """First 16 hex digits of the sha256 of the named csrc/ files, in order."""
     import hashlib
 
     csrc = os.path.join(ROOT, "dsa_sparse_attention_quant_gb300", "csrc")
     h = hashlib.sha256()
-    for name in ("logits.cu", "common.cuh"):
+    for name in sources:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(summary: str):
+def profiled_traffic(summary: str, sources=LOGITS_SOURCES):
     """DRAM bytes per launch from an ncu summary in profiles/, or None when the
     summary is missing or was taken on a different kernel source."""
     path = os.path.join(ROOT, "profiles", summary)
@@ -92,7 +97,7 @@ def profiled_traffic(summary: str):
             fields["sha"] = line.split(":", 1)[1].strip()
         elif line.startswith("dram_bytes_per_launch"):
             fields["bytes"] = line.split("|")[-1].strip()
-    if fields.get("sha") != kernel_source_sha() or "bytes" not in fields:
+    if fields.get("sha") != kernel_source_sha(sources) or "bytes" not in fields:
         return None
     return int(fields["bytes"])
 
@@ -754,7 +759,9 @@ def run_gather(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
         "config": {"workload": GATHER_DESC, "l2": "inputs larger than L2 (1.38 GB of rows, 4 rotating id sets)"},
         "roofline": {"bound": "hbm", "kernel": "dsa::gather_rows_kernel", "achieved": gbs, "peak": hbm_peak,
-                     "unit": "GB/s", "frac": gbs / hbm_peak, "traffic": None, "algorithmic_bytes_per_launch": moved,
+                     "unit": "GB/s", "frac": gbs / hbm_peak,
+                     "traffic": profiled_traffic("gather_rows_kernel_gather64x2048.md", GATHER_SOURCES),
+                     "algorithmic_bytes_per_launch": moved,
                      "avg_launch_ms": ms, "peak_source": f"{peak_src}: MEASURED_PEAKS.json hbm_gbs"},
         "gpu_launches": args.steps, "clocks": clocks.summary(),
     }), flush=True)
