@@ -29,7 +29,9 @@ _lock = threading.Lock()
 HEADS = 64
 DIM = 128
 BLOCK = 64
-PAGE_BYTES = 64 * 132
+PAGE_BYTES = 64 * 132      # FP8 cache page: 64 x 128 B E4M3 K, then 64 fp32 scales
+FP4_PAGE_BYTES = 64 * 68   # FP4 cache page: 64 x 64 B E2M1 K (two per byte), then 64 fp32 scales
+FMT = {"fp8": 0, "fp4": 1}
 GCC_FLAGS = ["-O2", "-std=gnu11", "-fPIC", "-shared", "-fopenmp",
              "-ffp-contract=off", "-fno-fast-math"]
 
@@ -63,11 +65,19 @@ def _bind(lib):
         "ora_ue8m0_scale": (ctypes.c_float, [ctypes.c_float]),
         "ora_quant_group": (None, [P, I32, P, P]),
         "ora_slot_offsets": (None, [I64, P, P]),
+        "ora_slot_offsets_fmt": (None, [I64, I32, P, P]),
         "ora_k_quant_write": (I64, [P, I64, P, P, I64]),
+        "ora_k_quant_write_fmt": (I64, [P, I64, P, P, I64, I32]),
+        "ora_e2m1_value": (ctypes.c_double, [ctypes.c_uint8]),
+        "ora_e2m1_encode": (ctypes.c_uint8, [ctypes.c_float]),
+        "ora_ue8m0_scale_e2m1": (ctypes.c_float, [ctypes.c_float]),
+        "ora_quant_group_e2m1": (None, [P, I32, P, P]),
         "ora_q_quant": (None, [P, I64, P, P]),
         "ora_rope": (I64, [P, I64, I64, P, P, I64, P]),
         "ora_gather_rows": (I64, [P, I64, I64, I64, P, I64, I32, P]),
         "ora_logits_row": (None, [P, P, P, P, P, I64, P]),
+        "ora_logits_row_fmt": (None, [P, P, P, P, I32, P, I64, P]),
+        "ora_indexer_fmt": (I64, [P, P, P, I32, P, I64, P, P, P, I64, I32, P, P, I64]),
         "ora_topk_row": (None, [P, I64, I32, P]),
         "ora_indexer": (I64, [P, P, P, P, I64, P, P, P, I64, I32, P, P, I64]),
         "ora_convert": (None, [P, I64, I32, P, P, I64, I32, I32, P, P]),
@@ -89,6 +99,16 @@ def _p(a):
 
 def _c(a, dtype) -> np.ndarray:
     return np.ascontiguousarray(a, dtype=dtype)
+
+
+def cache_format(cache: np.ndarray) -> int:
+    """0 for an FP8 cache (pages of 8448 B), 1 for an FP4 cache (pages of 4352 B)."""
+    assert cache.dtype == np.uint8 and cache.ndim == 2 and cache.flags["C_CONTIGUOUS"]
+    if cache.shape[1] == PAGE_BYTES:
+        return 0
+    if cache.shape[1] == FP4_PAGE_BYTES:
+        return 1
+    raise ValueError(f"cache pages of {cache.shape[1]} B are neither FP8 ({PAGE_BYTES}) nor FP4 ({FP4_PAGE_BYTES})")
 
 
 class Oracle:
@@ -121,26 +141,46 @@ class Oracle:
         self._lib.ora_quant_group(_p(x), int(x.shape[0]), _p(codes), _p(s))
         return codes, float(s[0])
 
+    # -- E2M1 (the FP4 cache's element) --------------------------------------
+    def e2m1_value(self, code: int) -> float:
+        return float(self._lib.ora_e2m1_value(int(code)))
+
+    def e2m1_encode(self, v: float) -> int:
+        return int(self._lib.ora_e2m1_encode(float(v)))
+
+    def ue8m0_scale_e2m1(self, amax: float) -> float:
+        return float(self._lib.ora_ue8m0_scale_e2m1(float(amax)))
+
+    def quant_group_e2m1(self, x):
+        """Quantise one group of fp32 values to packed E2M1; returns (bytes uint8, scale)."""
+        x = _c(x, np.float32)
+        assert x.shape[0] % 2 == 0
+        packed = np.zeros(x.shape[0] // 2, np.uint8)
+        s = np.zeros(1, np.float32)
+        self._lib.ora_quant_group_e2m1(_p(x), int(x.shape[0]), _p(packed), _p(s))
+        return packed, float(s[0])
+
     # -- paged cache --------------------------------------------------------
-    def slot_offsets(self, slot: int):
+    def slot_offsets(self, slot: int, fmt: str = "fp8"):
         kb = np.zeros(1, np.int64)
         sb = np.zeros(1, np.int64)
-        self._lib.ora_slot_offsets(int(slot), _p(kb), _p(sb))
+        self._lib.ora_slot_offsets_fmt(int(slot), FMT[fmt], _p(kb), _p(sb))
         return int(kb[0]), int(sb[0])
 
     @staticmethod
-    def new_cache(num_blocks: int) -> np.ndarray:
-        return np.zeros((num_blocks, PAGE_BYTES), np.uint8)
+    def new_cache(num_blocks: int, fmt: str = "fp8") -> np.ndarray:
+        return np.zeros((num_blocks, FP4_PAGE_BYTES if fmt == "fp4" else PAGE_BYTES), np.uint8)
 
     def k_quant_write(self, k_bf16, slot_mapping, cache: np.ndarray) -> int:
-        """Quantise bf16 K rows into ``cache`` (uint8 [num_blocks, 8448]) in place.
+        """Quantise bf16 K rows into ``cache`` in place: uint8 [num_blocks, 8448]
+        (FP8) or [num_blocks, 4352] (FP4), told apart by the page size.
 
         Returns the number of tokens whose slot was beyond the cache."""
         k = _c(k_bf16, np.uint16)
         sm = _c(slot_mapping, np.int64)
-        assert cache.dtype == np.uint8 and cache.flags["C_CONTIGUOUS"]
-        return int(self._lib.ora_k_quant_write(_p(k), int(sm.shape[0]), _p(sm), _p(cache),
-                                               int(cache.shape[0])))
+        fmt = cache_format(cache)
+        return int(self._lib.ora_k_quant_write_fmt(_p(k), int(sm.shape[0]), _p(sm), _p(cache),
+                                                   int(cache.shape[0]), fmt))
 
     def q_quant(self, q_bf16):
         """Quantise q rows of 128 (any leading shape); returns (codes, scales)."""
@@ -173,10 +213,10 @@ class Oracle:
                                         _p(out))
         return out, int(bad)
 
-    def fill_cache(self, batch, cache: np.ndarray | None = None, include_new: bool = True):
+    def fill_cache(self, batch, cache: np.ndarray | None = None, include_new: bool = True, fmt: str = "fp8"):
         """The oracle's own cache for ``batch``: context K, then this step's K."""
         if cache is None:
-            cache = self.new_cache(batch.num_blocks)
+            cache = self.new_cache(batch.num_blocks, fmt)
         self.k_quant_write(batch.ctx_k, batch.ctx_slots, cache)
         if include_new:
             self.k_quant_write(batch.k_new, batch.slot_mapping, cache)
@@ -185,9 +225,9 @@ class Oracle:
     # -- scores and selection -----------------------------------------------
     def logits_row(self, q_codes, q_scale, w, cache, bt_row, n_keys: int) -> np.ndarray:
         out = np.zeros(max(int(n_keys), 1), np.float64)
-        self._lib.ora_logits_row(
+        self._lib.ora_logits_row_fmt(
             _p(_c(q_codes, np.uint8)), _p(_c(q_scale, np.float32)), _p(_c(w, np.float32)),
-            _p(cache), _p(_c(bt_row, np.int32)), int(n_keys), _p(out))
+            _p(cache), cache_format(cache), _p(_c(bt_row, np.int32)), int(n_keys), _p(out))
         return out[: int(n_keys)]
 
     def topk_row(self, scores, k: int) -> np.ndarray:
@@ -213,8 +253,8 @@ class Oracle:
         ld = int(pos[rows].max() + 1) if (with_scores and n) else 0
         scores = np.zeros((max(n, 1), max(ld, 1)), np.float64) if with_scores else None
         bt = _c(batch.block_table, np.int32)
-        rc = self._lib.ora_indexer(
-            _p(_c(batch.q, np.uint16)), _p(_c(batch.w, np.float32)), _p(cache),
+        rc = self._lib.ora_indexer_fmt(
+            _p(_c(batch.q, np.uint16)), _p(_c(batch.w, np.float32)), _p(cache), cache_format(cache),
             _p(bt), int(bt.shape[1]), _p(_c(batch.req_id_per_token, np.int32)), _p(pos),
             _p(rows), n, k, _p(topk), _p(scores), ld)
         if rc != 0:

@@ -14,6 +14,8 @@
  *   [IG] "vllm.v1.attention.backends.mla.index_group" API page (docs.vllm.ai):
  *        `SparseMLAIndexGroup._convert_once` and the group builder.
  *   [OCP] OCP 8-bit Floating Point Specification (OFP8), E4M3 encoding.
+ *   [MX]  OCP Microscaling Formats (MX) Specification v1.0, the FP4 (E2M1)
+ *         element type.
  *
  * Where the pages leave a step open, the reading taken is stated at the
  * function. Arithmetic is fp64 on dequantised values; the two places where
@@ -77,16 +79,18 @@ uint8_t ora_e4m3_encode(float v) {
  * K + 4 bytes FP32 scale" per token, so the group is the whole 128-dim row.
  * Reading taken: scale = amax/448 (fp32), with amax floored at 1e-10, rounded
  * UP to a power of two (ue8m0 = exponent only), so |x/scale| <= 448.          */
-float ora_ue8m0_scale(float amax) {
+static float ue8m0_of(float amax, float qmax) {
   float r;
   int e;
   double m;
   if (!(amax >= 1e-10f)) amax = 1e-10f;
-  r = amax / 448.0f;             /* IEEE fp32 division */
+  r = amax / qmax;               /* IEEE fp32 division */
   m = frexp((double)r, &e);      /* r = m * 2^e, m in [0.5, 1) */
   if (m == 0.5) return r;        /* already a power of two */
   return (float)ldexp(1.0, e);   /* next power of two above r */
 }
+
+float ora_ue8m0_scale(float amax) { return ue8m0_of(amax, 448.0f); }
 
 void ora_quant_group(const float *x, int n, uint8_t *codes, float *scale) {
   float amax = 0.0f, s;
@@ -97,6 +101,69 @@ void ora_quant_group(const float *x, int n, uint8_t *codes, float *scale) {
   }
   s = ora_ue8m0_scale(amax);
   for (i = 0; i < n; ++i) codes[i] = ora_e4m3_encode(x[i] / s); /* fp32 division */
+  *scale = s;
+}
+
+/* ------------------------------------------------------------------------ */
+/* FP4 indexer cache. [IC] hands `sparse_attn_indexer` a `use_fp4_cache` flag
+ * beside `quant_block_size` and `scale_fmt`; the pages print nothing more of
+ * the format. Reading taken: the element type is [MX]'s E2M1, and the
+ * quantiser is the FP8 cache's with E2M1 in place of E4M3 — one ue8m0 scale
+ * per token's 128 values, amax/6 (6 = E2M1's largest magnitude) rounded up to
+ * a power of two, codes rounded to nearest-even and saturated. q stays FP8.
+ *
+ * E2M1 per [MX]: 1 sign bit, 2 exponent bits with bias 1, 1 mantissa bit.
+ * Exponent field 0 holds the subnormal m * 0.5; there is no infinity or NaN,
+ * so the magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4 and 6. Codes are 0..15.      */
+
+double ora_e2m1_value(uint8_t code) {
+  int sign = (code >> 3) & 1;
+  int e = (code >> 1) & 3;
+  int m = code & 1;
+  double mag = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+  return sign ? -mag : mag;
+}
+
+/* Nearest E2M1 value to v, ties to the even code; magnitudes beyond 6 become
+ * 6 (saturating). The sign of zero is kept. NaN never reaches the quantiser
+ * (finite bf16 inputs, |x/scale| <= 6); it is mapped to +6. */
+uint8_t ora_e2m1_encode(float v) {
+  uint8_t sign;
+  double a, quantum, steps;
+  int e;
+  if (isnan(v)) return 0x7;
+  sign = signbit(v) ? 0x8 : 0x0;
+  a = fabs((double)v);
+  if (a >= 6.0) return sign | 0x7;
+  if (!(a > 0.0)) return sign;
+  e = ilogb(a);
+  if (e < 0) e = 0;               /* the subnormal 0.5 shares the spacing of [1, 2) */
+  quantum = ldexp(1.0, e - 1);    /* 2 steps per binade */
+  steps = nearbyint(a / quantum); /* exact quotient; default mode rounds half to even */
+  if (steps == 0.0) return sign;
+  if (steps < 2.0) return sign | 0x1; /* only when e == 0: the subnormal 0.5 */
+  if (steps == 4.0) {                 /* rounded up into the next binade */
+    e += 1;
+    steps = 2.0;
+  }
+  return sign | (uint8_t)(((e + 1) << 1) | ((int)steps - 2));
+}
+
+float ora_ue8m0_scale_e2m1(float amax) { return ue8m0_of(amax, 6.0f); }
+
+/* One group to packed E2M1: element 2i in the low nibble of byte i, element
+ * 2i+1 in the high nibble (reading taken: the lower index in the lower bits,
+ * as in little-endian packing). n is even. */
+void ora_quant_group_e2m1(const float *x, int n, uint8_t *packed, float *scale) {
+  float amax = 0.0f, s;
+  int i;
+  for (i = 0; i < n; ++i) {
+    float a = fabsf(x[i]);
+    if (a > amax) amax = a;
+  }
+  s = ora_ue8m0_scale_e2m1(amax);
+  for (i = 0; i < n; i += 2)
+    packed[i / 2] = (uint8_t)(ora_e2m1_encode(x[i] / s) | (ora_e2m1_encode(x[i + 1] / s) << 4));
   *scale = s;
 }
 
@@ -158,9 +225,17 @@ int64_t ora_rope(const uint16_t *x, int64_t rows, int64_t rows_per_token, const 
  * Reading taken for the order inside a 64-slot page (8448 B): the 64 K rows
  * of 128 B first, then the 64 fp32 scales.                                  */
 void ora_slot_offsets(int64_t slot, int64_t *k_byte, int64_t *scale_byte) {
+  ora_slot_offsets_fmt(slot, ORA_FMT_FP8, k_byte, scale_byte);
+}
+
+/* The FP4 page (reading taken, as for FP8): the 64 rows of 64 code bytes,
+ * then the 64 fp32 scales — 4352 B. */
+void ora_slot_offsets_fmt(int64_t slot, int fmt, int64_t *k_byte, int64_t *scale_byte) {
   int64_t page = slot / ORA_BLOCK, off = slot % ORA_BLOCK;
-  *k_byte = page * ORA_PAGE_BYTES + off * ORA_DIM;
-  *scale_byte = page * ORA_PAGE_BYTES + ORA_BLOCK * ORA_DIM + off * 4;
+  int64_t row = (fmt == ORA_FMT_FP4) ? ORA_DIM / 2 : ORA_DIM;
+  int64_t page_bytes = (fmt == ORA_FMT_FP4) ? ORA_FP4_PAGE_BYTES : ORA_PAGE_BYTES;
+  *k_byte = page * page_bytes + off * row;
+  *scale_byte = page * page_bytes + ORA_BLOCK * row + off * 4;
 }
 
 /* [IC] `SparseAttnIndexer` body: `indexer_k_quant_and_cache(k, kv_cache,
@@ -169,6 +244,12 @@ void ora_slot_offsets(int64_t slot, int64_t *k_byte, int64_t *scale_byte) {
  * tokens whose slot lies outside the cache (also skipped). */
 int64_t ora_k_quant_write(const uint16_t *k_bf16, int64_t n, const int64_t *slot_mapping,
                           uint8_t *cache, int64_t num_blocks) {
+  return ora_k_quant_write_fmt(k_bf16, n, slot_mapping, cache, num_blocks, ORA_FMT_FP8);
+}
+
+/* The same write into an FP8 (fmt 0) or FP4 (fmt 1) cache. */
+int64_t ora_k_quant_write_fmt(const uint16_t *k_bf16, int64_t n, const int64_t *slot_mapping,
+                              uint8_t *cache, int64_t num_blocks, int fmt) {
   int64_t i, bad = 0;
   for (i = 0; i < n; ++i) {
     float x[ORA_DIM], s;
@@ -182,9 +263,12 @@ int64_t ora_k_quant_write(const uint16_t *k_bf16, int64_t n, const int64_t *slot
       continue;
     }
     for (d = 0; d < ORA_DIM; ++d) x[d] = bf16_value(k_bf16[i * ORA_DIM + d]);
-    ora_quant_group(x, ORA_DIM, codes, &s);
-    ora_slot_offsets(slot, &kb, &sb);
-    memcpy(cache + kb, codes, ORA_DIM);
+    if (fmt == ORA_FMT_FP4)
+      ora_quant_group_e2m1(x, ORA_DIM, codes, &s);
+    else
+      ora_quant_group(x, ORA_DIM, codes, &s);
+    ora_slot_offsets_fmt(slot, fmt, &kb, &sb);
+    memcpy(cache + kb, codes, (fmt == ORA_FMT_FP4) ? ORA_DIM / 2 : ORA_DIM);
     memcpy(cache + sb, &s, 4);
   }
   return bad;
@@ -219,6 +303,14 @@ void ora_q_quant(const uint16_t *q_bf16, int64_t rows, uint8_t *q_codes, float *
 void ora_logits_row(const uint8_t *q_codes, const float *q_scale, const float *w,
                     const uint8_t *cache, const int32_t *bt_row, int64_t n_keys,
                     double *out) {
+  ora_logits_row_fmt(q_codes, q_scale, w, cache, ORA_FMT_FP8, bt_row, n_keys, out);
+}
+
+/* The same score over an FP8 (fmt 0) or FP4 (fmt 1) K cache; only the
+ * dequantisation of k[s] differs. */
+void ora_logits_row_fmt(const uint8_t *q_codes, const float *q_scale, const float *w,
+                        const uint8_t *cache, int fmt, const int32_t *bt_row, int64_t n_keys,
+                        double *out) {
   static const double softmax_scale = 0.08838834764831845; /* 1/sqrt(128) */
   static const double head_norm = 0.125;                   /* 1/sqrt(64) */
   double qd[ORA_HEADS][ORA_DIM], kd[ORA_DIM];
@@ -232,9 +324,13 @@ void ora_logits_row(const uint8_t *q_codes, const float *q_scale, const float *w
     int64_t kb, sb;
     float ks;
     double total = 0.0;
-    ora_slot_offsets(slot, &kb, &sb);
+    ora_slot_offsets_fmt(slot, fmt, &kb, &sb);
     memcpy(&ks, cache + sb, 4);
-    for (d = 0; d < ORA_DIM; ++d) kd[d] = ora_e4m3_value(cache[kb + d]) * (double)ks;
+    for (d = 0; d < ORA_DIM; ++d) {
+      double v = (fmt == ORA_FMT_FP4) ? ora_e2m1_value((uint8_t)((cache[kb + d / 2] >> (4 * (d & 1))) & 15))
+                                      : ora_e4m3_value(cache[kb + d]);
+      kd[d] = v * (double)ks;
+    }
     for (h = 0; h < ORA_HEADS; ++h) {
       double dot = 0.0;
       for (d = 0; d < ORA_DIM; ++d) dot += qd[h][d] * kd[d];
@@ -278,6 +374,15 @@ int64_t ora_indexer(const uint16_t *q_bf16, const float *w, const uint8_t *cache
                     const int32_t *req_id_per_token, const int64_t *positions,
                     const int64_t *rows, int64_t n_rows, int topk,
                     int32_t *topk_out, double *scores_out, int64_t scores_ld) {
+  return ora_indexer_fmt(q_bf16, w, cache, ORA_FMT_FP8, block_table, bt_stride, req_id_per_token, positions,
+                         rows, n_rows, topk, topk_out, scores_out, scores_ld);
+}
+
+int64_t ora_indexer_fmt(const uint16_t *q_bf16, const float *w, const uint8_t *cache, int fmt,
+                        const int32_t *block_table, int64_t bt_stride,
+                        const int32_t *req_id_per_token, const int64_t *positions,
+                        const int64_t *rows, int64_t n_rows, int topk,
+                        int32_t *topk_out, double *scores_out, int64_t scores_ld) {
   int64_t i, err = 0;
   for (i = 0; i < n_rows; ++i)
     if (scores_out && positions[rows[i]] + 1 > scores_ld) err = -1;
@@ -291,8 +396,8 @@ int64_t ora_indexer(const uint16_t *q_bf16, const float *w, const uint8_t *cache
     double *sc = scores_out ? scores_out + i * scores_ld
                             : (double *)malloc(sizeof(double) * (size_t)n);
     ora_q_quant(q_bf16 + t * ORA_HEADS * ORA_DIM, ORA_HEADS, qc, qs);
-    ora_logits_row(qc, qs, w + t * ORA_HEADS, cache,
-                   block_table + (int64_t)req_id_per_token[t] * bt_stride, n, sc);
+    ora_logits_row_fmt(qc, qs, w + t * ORA_HEADS, cache, fmt,
+                       block_table + (int64_t)req_id_per_token[t] * bt_stride, n, sc);
     ora_topk_row(sc, n, topk, topk_out + i * topk);
     if (!scores_out) free(sc);
   }

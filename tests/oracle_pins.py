@@ -10,7 +10,8 @@ Sources: the web pages "IndexCacheï¼šDeepSeek ç¨€ç–æ³¨æ„åŠ›ä¸­çš„è·¨å±‚ç´¢å¼•å
 (atomage.cn; its `Indexer`, FP8 indexer-cache, `SparseAttnIndexer` and layer
 schedule snippets), "PR #37735 å®Œæ•´æŠ¥å‘Š" (prhub.com.cn; å…³é”®æºç ç‰‡æ®µ and
 é£Žé™©ä¸Žå½±å“), the vLLM API page "vllm.v1.attention.backends.mla.index_group"
-(`_convert_once`), and the OCP 8-bit floating point specification.
+(`_convert_once`), the OCP 8-bit floating point specification, and the OCP
+Microscaling Formats (MX) specification (the E2M1 element of the FP4 cache).
 """
 from __future__ import annotations
 
@@ -322,6 +323,158 @@ def pin_indexer_block_table_invariance(ora):
     s1 = ora.indexer(b1, ora.fill_cache(b1), with_scores=True)[1]
     s2 = ora.indexer(b2, ora.fill_cache(b2), with_scores=True)[1]
     assert np.array_equal(s1, s2)
+
+
+# ----------------------------------------------------------------- FP4 cache
+
+E2M1_MAGNITUDES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]  # codes 0..7 (OCP MX, FP4 E2M1)
+
+
+def _e2m1_brute(v: float) -> int:
+    """Nearest E2M1 code by enumeration: smallest distance, then the even code;
+    magnitudes past 6 saturate. The test's own rule, not the oracle's."""
+    sign = 0x8 if math.copysign(1.0, v) < 0 else 0
+    a = min(abs(v), 6.0)
+    best = min(range(8), key=lambda c: (abs(E2M1_MAGNITUDES[c] - a), c & 1))
+    return sign | best
+
+
+def pin_e2m1_golden(ora):
+    for value, code, *_ in read_golden("e2m1_codes.txt"):
+        got = ora.e2m1_encode(float(np.float32(float(value))))
+        assert got == int(code, 16), (value, hex(got), code)
+    for c in range(16):
+        want = (-1.0 if c & 8 else 1.0) * E2M1_MAGNITUDES[c & 7]
+        got = ora.e2m1_value(c)
+        assert got == want and math.copysign(1.0, got) == (-1.0 if c & 8 else 1.0), (c, got)
+
+
+def pin_e2m1_brute_force(ora, n: int = 3000):
+    grid = np.arange(-8 * 64, 8 * 64 + 1) / 64.0  # every multiple of 1/64 in [-8, 8]: all halfway points
+    rnd = (synth.normal(91, 1, n) * np.exp2(synth.uniform01(91, 2, n) * 8 - 4)).astype(np.float32)
+    for v in np.concatenate([grid.astype(np.float32), rnd]):
+        assert ora.e2m1_encode(float(v)) == _e2m1_brute(float(v)), float(v)
+
+
+def pin_ue8m0_e2m1(ora, n: int = 3000):
+    cases = [
+        (6.0, 1.0),           # 6/6 = 1: kept
+        (1.0, 0.25),          # 1/6 in (2^-3, 2^-2]
+        (3.0, 0.5),           # 3/6 = 2^-1 exactly
+        (3.015625, 1.0),      # next bf16 above 3: rounds up
+        (12.0, 2.0),
+        (0.0, 2.0 ** -35),    # amax floored at 1e-10: 1e-10/6 in (2^-36, 2^-35]
+    ]
+    for amax, want in cases:
+        assert ora.ue8m0_scale_e2m1(amax) == want, (amax, ora.ue8m0_scale_e2m1(amax), want)
+    u = synth.uniform01(92, 1, n)
+    for a in np.exp2(u * 60.0 - 30.0).astype(np.float32):
+        s = ora.ue8m0_scale_e2m1(float(a))
+        assert math.frexp(s)[0] == 0.5, "scale must be a power of two"
+        assert 3.0 < float(a) / s <= 6.0, "scale must be the smallest power of two that fits"
+
+
+def pin_quant_group_e2m1_vs_brute_force(ora, n_groups: int = 24):
+    x = synth.bf16_to_f32(bf16(synth.normal(93, 1, n_groups * 128))).reshape(n_groups, 128)
+    x[2] *= 1e-12
+    x[3] = 0.0
+    for g in range(n_groups):
+        packed, s = ora.quant_group_e2m1(x[g])
+        assert packed.shape == (64,)
+        assert s == ora.ue8m0_scale_e2m1(float(np.abs(x[g]).max()))
+        codes = [_e2m1_brute(float(np.float32(v) / np.float32(s))) for v in x[g]]
+        assert list(packed & 15) == codes[0::2] and list(packed >> 4) == codes[1::2]
+        deq = np.array([(-1.0 if c & 8 else 1.0) * E2M1_MAGNITUDES[c & 7] for c in codes]) * s
+        assert np.all(np.abs(deq - x[g]) <= 0.25 * np.abs(x[g]) + 0.25 * s)
+
+
+def pin_fp4_slot_layout(ora):
+    # 68 bytes per slot (64 bytes of E2M1 pairs + one fp32 scale), 64 slots per page = 4352
+    # bytes; inside a page the 64 K rows come first, then the 64 scales.
+    assert ora.slot_offsets(0, "fp4") == (0, 4096)
+    assert ora.slot_offsets(1, "fp4") == (64, 4100)
+    assert ora.slot_offsets(63, "fp4") == (63 * 64, 4096 + 63 * 4)
+    assert ora.slot_offsets(64, "fp4") == (4352, 4352 + 4096)
+    assert ora.slot_offsets(65, "fp4") == (4416, 8452)
+
+
+def pin_fp4_k_quant_write_worked(ora):
+    cache = ora.new_cache(2, "fp4")
+    assert cache.shape == (2, 4352)
+    k = np.zeros((4, 128), np.float64)
+    k[0, 0], k[0, 1], k[0, 3] = 1.0, -0.5, 3.0   # amax 3 -> scale 0.5: codes 0x4, 0xA, 0x0, 0x7
+    k[1, 5] = -2.0                                # padding token: must not be written
+    k[2, 126], k[2, 127] = 1.0, -12.0             # amax 12 -> scale 2: 0.5 -> 0x1, -6 -> 0xF
+    k[3, 0] = 1.0                                 # slot past the cache: skipped and counted
+    slots = np.array([5, -1, 70, 128], np.int64)
+    assert ora.k_quant_write(bf16(k), slots, cache) == 1
+    flat = cache.reshape(-1)
+    want = np.zeros_like(flat)
+    want[5 * 64 + 0] = 0xA4   # dims 0 (low nibble) and 1 (high nibble)
+    want[5 * 64 + 1] = 0x70   # dims 2 and 3
+    want[4096 + 5 * 4: 4096 + 5 * 4 + 4] = np.frombuffer(np.float32(0.5).tobytes(), np.uint8)
+    want[4352 + 6 * 64 + 63] = 0xF1
+    want[4352 + 4096 + 6 * 4: 4352 + 4096 + 6 * 4 + 4] = np.frombuffer(np.float32(2.0).tobytes(), np.uint8)
+    assert np.array_equal(flat, want)
+
+
+def pin_fp4_scores_equal_fp8_on_shared_values(ora):
+    """Keys whose values both caches hold exactly (E2M1 magnitudes times a
+    power of two, with 6 * 2^j the row's amax) dequantise identically from the
+    FP4 and the FP8 cache, so every score and every top-k row of the indexer
+    agree exactly between the two: the FP4 decode is tied to the pinned FP8
+    path."""
+    b = synth.make_batch(94, [150, 1], [(90, 20)], 16)
+    u = synth.uniform01(94, 7, (b.ctx_k.shape[0] + b.k_new.shape[0]) * 128)
+    mags = np.array(E2M1_MAGNITUDES)[(u * 8).astype(int) % 8]
+    sign = np.where(synth.uniform01(94, 8, u.size) < 0.5, -1.0, 1.0)
+    vals = (mags * sign).reshape(-1, 128)
+    vals[:, 5] = 6.0                                     # amax 6 * 2^j in every row
+    j = (np.arange(vals.shape[0]) % 5 - 2).astype(np.float64)
+    vals *= np.exp2(j)[:, None]
+    n_ctx = b.ctx_k.shape[0]
+    b.ctx_k = bf16(vals[:n_ctx])
+    b.k_new = bf16(vals[n_ctx:])
+    c8 = ora.fill_cache(b)
+    c4 = ora.fill_cache(b, fmt="fp4")
+    t8, s8 = ora.indexer(b, c8, with_scores=True)
+    t4, s4 = ora.indexer(b, c4, with_scores=True)
+    assert np.array_equal(s8, s4) and np.array_equal(t8, t4)
+    assert np.abs(s8).max() > 0
+    # and a single row through logits_row on both caches
+    qc, qs = ora.q_quant(b.q[0])
+    bt = b.block_table[b.req_id_per_token[0]]
+    n = int(b.positions[0]) + 1
+    assert np.array_equal(ora.logits_row(qc, qs, b.w[0], c8, bt, n), ora.logits_row(qc, qs, b.w[0], c4, bt, n))
+
+
+def pin_fp4_scores_vs_library(ora):
+    """The FP4 cache's codes unpacked by the test (low nibble first) and
+    decoded by table; the score is then a float64 matmul of dequantised
+    values (ReLU per head, weighted sum over heads)."""
+    n_keys = 130
+    Q = synth.normal(95, 1, 64 * 128).reshape(64, 128)
+    K = synth.normal(95, 2, n_keys * 128).reshape(n_keys, 128)
+    K[::4] *= 7.0
+    w = synth.normal(95, 3, 64).astype(np.float32)
+    bt = np.array([2, 0, 1], np.int32)
+    pos = np.arange(n_keys)
+    slots = bt[pos // 64].astype(np.int64) * 64 + pos % 64
+    cache = ora.new_cache(3, "fp4")
+    assert ora.k_quant_write(bf16(K), slots, cache) == 0
+    qc, qs = ora.q_quant(bf16(Q))
+    got = ora.logits_row(qc, qs, w, cache, bt, n_keys)
+    flat = cache.reshape(-1)
+    table = np.array([(-1.0 if c & 8 else 1.0) * E2M1_MAGNITUDES[c & 7] for c in range(16)])
+    kd = np.zeros((n_keys, 128))
+    for i, s in enumerate(slots):
+        row = flat[(s // 64) * 4352 + (s % 64) * 64:][:64]
+        codes = np.stack([row & 15, row >> 4], axis=1).reshape(-1)
+        ks = np.frombuffer(flat[(s // 64) * 4352 + 4096 + (s % 64) * 4:][:4].tobytes(), np.float32)[0]
+        kd[i] = table[codes] * np.float64(ks)
+    qd = torch_e4m3_value(qc) * qs.astype(np.float64)[:, None]
+    want = SOFTMAX_SCALE * HEAD_NORM * (np.maximum(qd @ kd.T, 0.0).T @ w.astype(np.float64))
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-300)
 
 
 # ----------------------------------------------------------------- top-k

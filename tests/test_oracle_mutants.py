@@ -21,9 +21,9 @@ MUTANTS = {
     "reversed_k_dims": [("dot += qd[h][d] * kd[d];", "dot += qd[h][d] * kd[ORA_DIM - 1 - d];")],
     "causal_excludes_self": [("int64_t n = positions[t] + 1;", "int64_t n = positions[t] > 0 ? positions[t] : 1;")],
     "ignore_page_index": [("(int64_t)bt_row[s / ORA_BLOCK] * ORA_BLOCK", "(int64_t)bt_row[0] * ORA_BLOCK")],
-    "interleaved_slots": [("*k_byte = page * ORA_PAGE_BYTES + off * ORA_DIM;", "*k_byte = slot * ORA_SLOT_BYTES;"),
-                          ("*scale_byte = page * ORA_PAGE_BYTES + ORA_BLOCK * ORA_DIM + off * 4;",
-                           "*scale_byte = slot * ORA_SLOT_BYTES + ORA_DIM;")],
+    "interleaved_slots": [("*k_byte = page * page_bytes + off * row;", "*k_byte = slot * (row + 4);"),
+                          ("*scale_byte = page * page_bytes + ORA_BLOCK * row + off * 4;",
+                           "*scale_byte = slot * (row + 4) + row;")],
     "scale_rounds_down": [("return (float)ldexp(1.0, e);", "return (float)ldexp(1.0, e - 1);")],
     "no_amax_floor": [("if (!(amax >= 1e-10f)) amax = 1e-10f;", "")],
     "ties_away_from_zero": [("q = nearbyint(a / quantum);", "q = round(a / quantum);")],
@@ -42,6 +42,17 @@ MUTANTS = {
     "rope_truncates": [("  u += 0x7FFFu + ((u >> 16) & 1u);\n", "")],
     "gather_row_stride_ignored": [("rows + (int64_t)id * row_stride", "rows + (int64_t)id * row_bytes")],
     "gather_keeps_stale_rows": [("        memset(dst, 0, (size_t)row_bytes);\n", "")],
+    "e2m1_ties_away_from_zero": [("steps = nearbyint(a / quantum);", "steps = round(a / quantum);")],
+    "e2m1_no_saturation": [("if (a >= 6.0) return sign | 0x7;", "")],
+    "e2m1_subnormal_dropped": [("if (steps < 2.0) return sign | 0x1;", "if (steps < 2.0) return sign;")],
+    "e2m1_exponent_bias_2": [("ldexp(1.0 + 0.5 * m, e - 1)", "ldexp(1.0 + 0.5 * m, e - 2)")],
+    "e2m1_scale_uses_fp8_max": [("return ue8m0_of(amax, 6.0f);", "return ue8m0_of(amax, 448.0f);")],
+    "fp4_nibbles_swapped": [("(ora_e2m1_encode(x[i] / s) | (ora_e2m1_encode(x[i + 1] / s) << 4))",
+                             "(ora_e2m1_encode(x[i + 1] / s) | (ora_e2m1_encode(x[i] / s) << 4))")],
+    "fp4_decode_high_nibble_first": [("(4 * (d & 1))", "(4 * (1 - (d & 1)))")],
+    "fp4_fp8_page_size": [("int64_t page_bytes = (fmt == ORA_FMT_FP4) ? ORA_FP4_PAGE_BYTES : ORA_PAGE_BYTES;",
+                           "int64_t page_bytes = ORA_PAGE_BYTES;")],
+    "fp4_row_read_as_fp8": [("double v = (fmt == ORA_FMT_FP4) ?", "double v = 0 ?")],
     "convert_counts_padding": [("        ++valid;\n", ""), ("        physical[t * topk + j] = -1;\n",
                                                         "        physical[t * topk + j] = -1;\n        ++valid;\n")],
 }
