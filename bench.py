@@ -203,8 +203,8 @@ class ClockSampler:
 class Replica:
     """One independent copy of a step's device inputs (K cache, q, w, new K)."""
 
-    def __init__(self, hb, dsa, torch, dev, ctx_k, ctx_slots):
-        self.k_cache = torch.zeros((hb.num_blocks, 8448), dtype=torch.uint8, device=dev)
+    def __init__(self, hb, dsa, torch, dev, ctx_k, ctx_slots, kcache="fp8"):
+        self.k_cache = dsa.new_k_cache(hb.num_blocks, kcache, device=dev)
         dsa.indexer_k_quant_write(ctx_k, ctx_slots, self.k_cache)
         self.q = torch.from_numpy(hb.q.view(np.int16)).view(torch.bfloat16).to(dev)
         self.w = torch.from_numpy(hb.w).to(dev)
@@ -233,12 +233,14 @@ def run_ours(args):
     slots = torch.from_numpy(hb.slot_mapping).to(dev)
     fs, _ = dsa.schedule_build(1, True, 4)
 
-    cache_bytes = hb.num_blocks * 8448
+    fp4 = args.kcache == "fp4"
+    slot_bytes = 68 if fp4 else 132
+    cache_bytes = hb.num_blocks * 64 * slot_bytes
     per_replica = cache_bytes + hb.q.nbytes + hb.w.nbytes + hb.k_new.nbytes
     n_rep = args.replicas or max(1, min(16, math.ceil(2 * L2_BYTES / per_replica)))
     ctx_k = torch.from_numpy(hb.ctx_k.view(np.int16)).view(torch.bfloat16).to(dev)
     ctx_slots = torch.from_numpy(hb.ctx_slots).to(dev)
-    reps = [Replica(hb, dsa, torch, dev, ctx_k, ctx_slots) for _ in range(n_rep)]
+    reps = [Replica(hb, dsa, torch, dev, ctx_k, ctx_slots, args.kcache) for _ in range(n_rep)]
     del ctx_k, ctx_slots
 
     ws = torch.empty(dsa.layer_stack_workspace_size(batch, k), dtype=torch.uint8, device=dev)
@@ -411,14 +413,16 @@ def run_ours(args):
     rows_per_s = whole_job_rate(T, world, ms_per_step / 1e3)
     hbm_peak, bf16_burst, bf16_sustained, peak_src = read_peaks()
     kernel_avg_ms = float(np.mean(kernel_ms))
-    traffic = profiled_traffic(f"logits_kernel_{args.workload}.md")
+    traffic = profiled_traffic(f"logits_kernel_{args.workload}{'_fp4' if fp4 else ''}.md")
     breakdown = {name: float(per_kernel[:, j].mean() * 1e3) for j, name in enumerate(kernels)}
     if not has_pre:
-        # decode: the 132-byte K slots stream from HBM once per pair
-        algo_bytes = pairs * (132 + 4) + T * (64 * 128 + 64 * 4)
+        # decode: the K slots (132 B FP8, 68 B FP4) stream from HBM once per pair,
+        # each pair's fp32 score is written once; q codes and w' once per token
+        algo_bytes = pairs * (slot_bytes + 4) + T * (64 * 128 + 64 * 4)
         achieved = algo_bytes / (kernel_avg_ms / 1e3) / 1e9
         roofline = {
-            "bound": "hbm", "kernel": "dsa::logits_kernel<1> (decode scores, tcgen05 FP8)",
+            "bound": "hbm",
+            "kernel": f"dsa::logits_kernel<1> (decode scores, tcgen05 {'E2M1 K x E4M3 q' if fp4 else 'FP8'})",
             "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
             "traffic": traffic, "algorithmic_bytes_per_launch": algo_bytes,
             "peak_source": f"{peak_src}: MEASURED_PEAKS.json hbm_gbs (copy bandwidth)",
@@ -429,10 +433,12 @@ def run_ours(args):
         achieved = flops / (kernel_avg_ms / 1e3) / 1e12
         peak = 2.0 * bf16_sustained  # FP8 = 2 x bf16 (nominal 4.5 / 2.25 PFLOP/s); sustained: long step
         roofline = {
-            "bound": "tensor", "kernel": "dsa::logits_kernel (scores, tcgen05 FP8)",
+            "bound": "tensor",
+            "kernel": f"dsa::logits_kernel (scores, tcgen05 {'kind::f8f6f4 E2M1 K x E4M3 q' if fp4 else 'FP8'})",
             "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
             "traffic": traffic, "algorithmic_flops_per_launch": flops,
-            "peak_source": f"{peak_src}: 2 x MEASURED_PEAKS.json bf16_tflops_sustained (FP8 = 2 x bf16 nominal)",
+            "peak_source": f"{peak_src}: 2 x MEASURED_PEAKS.json bf16_tflops_sustained (FP8 = 2 x bf16 nominal; "
+                           "kind::f8f6f4 runs E2M1 operands at the FP8 rate)",
         }
     roofline["avg_launch_ms"] = kernel_avg_ms
     roofline["timing"] = ("CUDA events recorded on the launching stream around every launch of the score kernel, "
@@ -449,10 +455,12 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "fp8_e4m3 x fp8_e4m3 -> fp32",
+        "dtype": "fp4_e2m1 (K) x fp8_e4m3 (q) -> fp32" if fp4 else "fp8_e4m3 x fp8_e4m3 -> fp32",
         "data": "synthetic (seeded normals, bf16-rounded)",
         "config": {
             "workload": desc,
+            "k_cache": ("FP4: E2M1 codes + ue8m0 fp32 scale per token, 68 B/slot (the reading of use_fp4_cache)"
+                        if fp4 else "FP8: E4M3 codes + ue8m0 fp32 scale per token, 132 B/slot"),
             "query_tokens": T,
             "pairs_per_step": pairs,
             "topk": k,
@@ -475,7 +483,7 @@ def run_ours(args):
         "wall_s_timed_region": wall1 - wall0,
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(hb, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(hb, args.cpu_seconds, args.kcache)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -483,7 +491,7 @@ def run_ours(args):
 
 # --------------------------------------------------------------------- stack61
 
-def stack_inputs(meta, n_layers, dev, dsa, torch):
+def stack_inputs(meta, n_layers, dev, dsa, torch, kcache="fp8"):
     """Per-layer q, w, new K and K cache of the stack, drawn on the device.
 
     Layer l draws from torch's CUDA generator seeded with 5000 + l (N(0,1),
@@ -497,7 +505,7 @@ def stack_inputs(meta, n_layers, dev, dsa, torch):
     for l in range(n_layers):
         g = torch.Generator(device=dev)
         g.manual_seed(5000 + l)
-        cache = torch.zeros((meta.num_blocks, 8448), dtype=torch.uint8, device=dev)
+        cache = dsa.new_k_cache(meta.num_blocks, kcache, device=dev)
         for c0 in range(0, n_ctx, 1 << 20):
             c1 = min(n_ctx, c0 + (1 << 20))
             k = torch.randn((c1 - c0, 128), generator=g, device=dev).to(torch.bfloat16)
@@ -544,7 +552,7 @@ def run_stack(args):
     fs4, _ = dsa.schedule_build(STACK_LAYERS, True, STACK_FREQ)
     fs1, _ = dsa.schedule_build(STACK_LAYERS, True, 1)
     n_f = fs4.count("F")
-    layers = stack_inputs(meta, STACK_LAYERS, dev, dsa, torch)
+    layers = stack_inputs(meta, STACK_LAYERS, dev, dsa, torch, args.kcache)
     l4 = [layers[l] if fs4[l] == "F" else None for l in range(STACK_LAYERS)]
     ws = torch.empty(dsa.layer_stack_workspace_size(batch, k), dtype=torch.uint8, device=dev)
     topk = torch.empty((T, k), dtype=torch.int32, device=dev)
@@ -663,7 +671,8 @@ def run_stack(args):
     pre_pairs = layer_pairs - dec_pairs
     hbm_peak, bf16_burst, bf16_sustained, peak_src = read_peaks()
     ms = {name: float(per_kernel[:, j].mean()) for j, name in enumerate(kernels)}
-    dec_bytes = dec_pairs * (132 + 4) + n_dec * (64 * 128 + 64 * 4)
+    slot_bytes = 68 if args.kcache == "fp4" else 132
+    dec_bytes = dec_pairs * (slot_bytes + 4) + n_dec * (64 * 128 + 64 * 4)
     dec_gbs = dec_bytes / (ms["logits<1>"] / 1e3) / 1e9
     pre_tflops = pre_pairs * 64 * 128 * 2 / (ms["logits<4>"] / 1e3) / 1e12
     fp8_peak = 2.0 * bf16_sustained
@@ -691,7 +700,7 @@ def run_stack(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "fp8_e4m3 x fp8_e4m3 -> fp32",
+        "dtype": "fp4_e2m1 (K) x fp8_e4m3 (q) -> fp32" if args.kcache == "fp4" else "fp8_e4m3 x fp8_e4m3 -> fp32",
         "data": "synthetic (seeded normals, bf16-rounded; per-layer tensors from torch's seeded CUDA generator)",
         "config": {
             "workload": STACK_DESC,
@@ -699,7 +708,9 @@ def run_stack(args):
             "query_tokens_per_layer": T, "pairs_per_step": pairs, "topk": k,
             "freq1_ms_per_step": ms1,
             "freq4_speedup_vs_freq1": ms1 / ms4,
-            "l2": f"inputs larger than L2: every F layer reads its own {meta.num_blocks * 8448 / 1e6:.0f} MB K cache",
+            "k_cache": args.kcache,
+            "l2": f"inputs larger than L2: every F layer reads its own "
+                  f"{meta.num_blocks * 64 * slot_bytes / 1e6:.0f} MB K cache",
             "parallelism": "1 GPU",
         },
         "roofline": roofline,
@@ -711,7 +722,7 @@ def run_stack(args):
         "wall_s_timed_region": wall1 - wall0,
     }
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(stack_host_batch(meta, dev, torch), args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(stack_host_batch(meta, dev, torch), args.cpu_seconds, args.kcache)
     print(json.dumps(line), flush=True)
 
 
@@ -769,10 +780,10 @@ def run_gather(args):
 
 # --------------------------------------------------------------------- oracle
 
-def oracle_state(hb):
+def oracle_state(hb, kcache="fp8"):
     import oracle
 
-    cache = oracle.new_cache(hb.num_blocks)
+    cache = oracle.new_cache(hb.num_blocks, kcache)
     oracle.k_quant_write(hb.ctx_k, hb.ctx_slots, cache)  # the cache state before the step
     return oracle, cache
 
@@ -786,8 +797,8 @@ def oracle_step(ora, hb, cache, rows):
     return int((hb.positions[rows] + 1).sum())
 
 
-def cpu_baseline(hb, budget_s: float):
-    ora, cache = oracle_state(hb)
+def cpu_baseline(hb, budget_s: float, kcache: str = "fp8"):
+    ora, cache = oracle_state(hb, kcache)
     T = hb.num_tokens
     # size the sample: grow the row count until one pass takes about the budget
     n_rows, dt, p = 1, 0.0, 0
@@ -817,7 +828,7 @@ def run_reference(args):
     if rank != 0:
         return
     hb, desc = workload(args.workload)
-    ora, cache = oracle_state(hb)
+    ora, cache = oracle_state(hb, args.kcache)
     T = hb.num_tokens
     t0 = time.perf_counter()
     oracle_step(ora, hb, cache, np.arange(1, dtype=np.int64))
@@ -847,7 +858,8 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded normals, bf16-rounded)",
-        "config": {"workload": desc, "query_tokens": T, "pairs_per_step": hb.num_pairs(), "topk": hb.topk},
+        "config": {"workload": desc, "query_tokens": T, "pairs_per_step": hb.num_pairs(), "topk": hb.topk,
+                   "k_cache": args.kcache},
         "cpu_baseline": {"value": value, "unit": "pairs/s", "cores": os.cpu_count(), "kind": "oracle",
                          "sample": f"{n_rows} of {T} query rows per step"},
         "e2e": {"value": value, "unit": "pairs/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -866,6 +878,8 @@ def main():
     ap.add_argument("--clock-window", type=float, default=1.0, help="seconds of untimed steps while sampling clocks")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kcache", choices=["fp8", "fp4"], default="fp8",
+                    help="indexer K cache: FP8 (132 B/slot) or FP4 E2M1 (68 B/slot)")
     ap.add_argument("--rope", action="store_true",
                     help="q and new K arrive un-rotated; the layer prologue applies RoPE before quantising")
     args = ap.parse_args()

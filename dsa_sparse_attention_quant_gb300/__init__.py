@@ -8,6 +8,7 @@ from .binding import (  # noqa: F401
     Batch,
     DsaError,
     LayerStack,
+    cache_format,
     check_device_error,
     gather_rows,
     indexer_k_quant_write,
@@ -22,8 +23,9 @@ from .binding import (  # noqa: F401
     layer_stack_run,
     layer_stack_workspace_size,
     load,
+    new_k_cache,
     schedule_build,
     topk_logical_to_physical,
 )
 
-__version__ = "0.2.0"
+__version__ = "0.3.0"

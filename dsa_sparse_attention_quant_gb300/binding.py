@@ -9,6 +9,7 @@ raise; there is no fallback path.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import threading
 
@@ -28,6 +29,7 @@ DEVERR = {
     16: "seq_len inconsistent",
 }
 HEADS, HEAD_DIM, BLOCK_SIZE, PAGE_BYTES = 64, 128, 64, 8448
+FP4_PAGE_BYTES = 4352  # 64 slots x (64 E2M1 code bytes + 4 scale bytes)
 
 SYMBOLS = [
     "dsa_status_string", "dsa_version", "dsa_check_device_error",
@@ -38,6 +40,7 @@ SYMBOLS = [
     "dsa_layer_stack_workspace_size", "dsa_layer_stack_run",
     "dsa_indexer_logits_topk_static", "dsa_set_launch_events",
     "dsa_indexer_k_rope_quant_write", "dsa_indexer_q_rope_quant_fold", "dsa_gather_rows",
+    "dsa_indexer_k_quant_write_fp4",
 ]
 STATIC_WORKSPACE_BYTES = 32 << 20
 
@@ -59,6 +62,7 @@ class DsaBatchC(ctypes.Structure):
         ("seq_lens", ctypes.c_void_p),
         ("block_table", ctypes.c_void_p),
         ("req_id_per_token", ctypes.c_void_p),
+        ("k_cache_format", ctypes.c_int32),
     ]
 
 
@@ -127,6 +131,7 @@ def load(build_if_missing: bool = True):
             "dsa_indexer_logits_topk_static": (ctypes.c_int, [BP, P, P, P, I32, P, P, P, P, P]),
             "dsa_set_launch_events": (ctypes.c_int, [P, I32]),
             "dsa_indexer_k_rope_quant_write": (ctypes.c_int, [P, I64, I64, P, P, I64, P, P, I64, P, P]),
+            "dsa_indexer_k_quant_write_fp4": (ctypes.c_int, [P, I64, I64, P, P, I64, P, P, I64, P, P]),
             "dsa_indexer_q_rope_quant_fold": (ctypes.c_int, [P, P, I64, P, P, I64, F32, P, P, P, P, P]),
             "dsa_gather_rows": (ctypes.c_int, [P, I64, I64, I64, P, I64, I32, P, P, P]),
         }
@@ -203,17 +208,57 @@ class Batch:
                    int(hb.query_start_loc[hb.num_decodes]) if hb.num_reqs else 0)
 
 
+# ---------------------------------------------------------------- K caches
+
+def new_k_cache(num_blocks: int, fmt: str = "fp8", device=None):
+    """A zeroed indexer K cache of ``num_blocks`` pages: FP8 (8448-byte pages) or
+    FP4 (4352-byte pages of E2M1 codes)."""
+    if fmt not in ("fp8", "fp4"):
+        raise DsaError("fmt must be 'fp8' or 'fp4'")
+    page = FP4_PAGE_BYTES if fmt == "fp4" else PAGE_BYTES
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    return torch.zeros((int(num_blocks), page), dtype=torch.uint8, device=dev)
+
+
+def cache_format(k_cache) -> int:
+    """DSA_KCACHE_FP8 (0) or DSA_KCACHE_FP4 (1), from the page size of a
+    [num_blocks, page_bytes] (or [num_blocks, ...]) uint8 K cache."""
+    if k_cache.dtype != torch.uint8:
+        raise DsaError(f"k_cache must be torch.uint8, got {k_cache.dtype}")
+    if k_cache.dim() < 2:
+        raise DsaError("k_cache must be [num_blocks, page bytes] (or [num_blocks, 64, slot bytes])")
+    page = math.prod(int(d) for d in k_cache.shape[1:])
+    if page == PAGE_BYTES:
+        return 0
+    if page == FP4_PAGE_BYTES:
+        return 1
+    raise DsaError(f"k_cache pages of {page} bytes are neither FP8 ({PAGE_BYTES}) nor FP4 ({FP4_PAGE_BYTES})")
+
+
+def _bind_format(batch, k_cache):
+    batch.c.k_cache_format = cache_format(k_cache)
+
+
 # ---------------------------------------------------------------- entry points
 
 def indexer_k_quant_write(k, slot_mapping, k_cache, dev_err=None, stream=None):
+    """S1: quantise bf16 K rows into the cache at their slots, FP8 or FP4 by the
+    cache's page size."""
     _need(slot_mapping, torch.int64, "slot_mapping")
     _need(k_cache, torch.uint8, "k_cache")
+    fp4 = cache_format(k_cache) == 1
     n = int(slot_mapping.shape[0])
     if n == 0:
         return
     if k.dtype != torch.bfloat16 or not k.is_cuda or k.stride(-1) != 1:
         raise DsaError("k must be a CUDA bf16 tensor with unit inner stride")
     row_stride = int(k.stride(0)) if k.dim() == 2 else HEAD_DIM
+    if fp4:
+        st = load().dsa_indexer_k_quant_write_fp4(_ptr(k), n, row_stride, None, None, 0, _ptr(slot_mapping),
+                                                  _ptr(k_cache), int(k_cache.shape[0]), _ptr(dev_err),
+                                                  _stream(stream))
+        _check(st, "dsa_indexer_k_quant_write_fp4")
+        return
     st = load().dsa_indexer_k_quant_write(_ptr(k), n, row_stride, _ptr(slot_mapping), _ptr(k_cache),
                                           int(k_cache.shape[0]), _ptr(dev_err), _stream(stream))
     _check(st, "dsa_indexer_k_quant_write")
@@ -245,6 +290,7 @@ def indexer_k_rope_quant_write(k, positions, cos_sin, slot_mapping, k_cache, dev
     _need(slot_mapping, torch.int64, "slot_mapping")
     _need(positions, torch.int64, "positions")
     _need(k_cache, torch.uint8, "k_cache")
+    fp4 = cache_format(k_cache) == 1
     max_pos = _rope_table(cos_sin)
     n = int(slot_mapping.shape[0])
     if n == 0:
@@ -252,10 +298,10 @@ def indexer_k_rope_quant_write(k, positions, cos_sin, slot_mapping, k_cache, dev
     if k.dtype != torch.bfloat16 or not k.is_cuda or k.stride(-1) != 1:
         raise DsaError("k must be a CUDA bf16 tensor with unit inner stride")
     row_stride = int(k.stride(0)) if k.dim() == 2 else HEAD_DIM
-    st = load().dsa_indexer_k_rope_quant_write(_ptr(k), n, row_stride, _ptr(positions), _ptr(cos_sin), max_pos,
-                                               _ptr(slot_mapping), _ptr(k_cache), int(k_cache.shape[0]),
-                                               _ptr(dev_err), _stream(stream))
-    _check(st, "dsa_indexer_k_rope_quant_write")
+    fn = load().dsa_indexer_k_quant_write_fp4 if fp4 else load().dsa_indexer_k_rope_quant_write
+    st = fn(_ptr(k), n, row_stride, _ptr(positions), _ptr(cos_sin), max_pos, _ptr(slot_mapping), _ptr(k_cache),
+            int(k_cache.shape[0]), _ptr(dev_err), _stream(stream))
+    _check(st, "dsa_indexer_k_quant_write_fp4" if fp4 else "dsa_indexer_k_rope_quant_write")
 
 
 def indexer_q_rope_quant_fold(q, w, positions, cos_sin, softmax_scale: float = 0.0, q_fp8=None, q_scale=None,
@@ -308,6 +354,7 @@ def indexer_logits_topk(batch: Batch, q_fp8, w_folded, k_cache, topk: int, topk_
         topk_out = torch.empty((batch.num_tokens, int(topk)), dtype=torch.int32, device=dev)
     nbytes = indexer_workspace_size(batch, topk)
     ws = _workspace(nbytes, dev, ws)
+    _bind_format(batch, k_cache)
     st = load().dsa_indexer_logits_topk(ctypes.byref(batch.c), _ptr(q_fp8), _ptr(w_folded), _ptr(k_cache),
                                         int(topk), _ptr(topk_out), _ptr(ws), ws.numel(), _ptr(k_new),
                                         _ptr(slot_mapping), _ptr(dev_err), _stream(stream))
@@ -321,6 +368,7 @@ def indexer_logits_topk_static(batch: Batch, q_fp8, w_folded, k_cache, topk: int
     allocate device memory. ``topk_out`` must be passed; the scratch is the
     library's own static device array (DSA_STATIC_WORKSPACE_BYTES), shared by
     all calls, so calls must not overlap on the GPU."""
+    _bind_format(batch, k_cache)
     st = load().dsa_indexer_logits_topk_static(ctypes.byref(batch.c), _ptr(q_fp8), _ptr(w_folded), _ptr(k_cache),
                                                int(topk), _ptr(topk_out), _ptr(k_new), _ptr(slot_mapping),
                                                _ptr(dev_err), _stream(stream))
@@ -345,6 +393,7 @@ def indexer_logits(batch: Batch, q_fp8, w_folded, k_cache, logits=None, ws=None,
         logits = torch.full((batch.num_tokens, ld), float("nan"), dtype=torch.float32, device=dev)
     if ws is None:
         ws = indexer_plan(batch, dev_err=dev_err, stream=stream)
+    _bind_format(batch, k_cache)
     st = load().dsa_indexer_logits(ctypes.byref(batch.c), _ptr(q_fp8), _ptr(w_folded), _ptr(k_cache),
                                    _ptr(logits), int(logits.stride(0)), _ptr(ws), ws.numel(), _ptr(dev_err),
                                    _stream(stream))
@@ -424,6 +473,11 @@ class LayerStack:
         n = len(fs)
         self._arr = (DsaLayerInputsC * max(n, 1))()
         self._keep = [batch, slot_mapping, dev_err, positions, rope_cos_sin]
+        fmts = {cache_format(L["k_cache"]) for L in layers if L is not None}
+        if len(fmts) > 1:
+            raise DsaError("all layers' K caches must have one format")
+        if fmts:
+            batch.c.k_cache_format = fmts.pop()
         for l, L in enumerate(layers):
             if L is None:
                 continue

@@ -66,20 +66,25 @@ int tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
   return DSA_OK;
 }
 
-// K cache as a 3-D byte tensor {128 K bytes, 64 slots, num_blocks pages}: one
-// box is the 64 K rows of one page, landed with the 128-byte swizzle.
-int make_kcache_map(CUtensorMap* m, const uint8_t* cache, int64_t num_blocks) {
+// K cache as a 3-D tensor {128 K values, 64 slots, num_blocks pages}: one box
+// is the 64 K rows of one page, landed with the 128-byte swizzle. FP8 pages
+// are read as bytes; FP4 pages with the packed 4-bit type, which lands each
+// 64-byte row as 128 bytes (8 code bytes, then an 8-byte gap, per 16 bytes),
+// the layout the MMA reads E2M1 operands in. That type wants a 32-byte
+// aligned base and strides (64 and 4352 are).
+int make_kcache_map(CUtensorMap* m, const uint8_t* cache, int64_t num_blocks, bool fp4) {
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   int st = tensor_map_encoder(&enc);
   if (st != DSA_OK) return st;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(kBlock),
                         static_cast<cuuint64_t>(num_blocks)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(kPageBytes)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(fp4 ? kDim / 2 : kDim),
+                           static_cast<cuuint64_t>(fp4 ? kFp4PageBytes : kPageBytes)};
   cuuint32_t box[3] = {static_cast<cuuint32_t>(kDim), static_cast<cuuint32_t>(kBlock), 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(cache), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(m, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+                   const_cast<uint8_t*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DSA_OK : DSA_ECUDA;
 }
 
@@ -110,7 +115,15 @@ int check_batch(const DsaBatch* b) {
     return DSA_EINVAL;
   if (b->num_tokens > 0 && b->req_id_per_token == nullptr) return DSA_EINVAL;
   if (static_cast<int64_t>(b->num_tokens) * kHeads > (int64_t{1} << 31) - 1) return DSA_EINVAL;
+  if (b->k_cache_format != DSA_KCACHE_FP8 && b->k_cache_format != DSA_KCACHE_FP4) return DSA_EINVAL;
   return DSA_OK;
+}
+
+bool kcache_fp4(const DsaBatch* b) { return b->k_cache_format == DSA_KCACHE_FP4; }
+
+// The K cache base: 16-byte aligned, 32 for FP4 pages (the packed TMA type).
+bool kcache_aligned(const DsaBatch* b, const void* k_cache) {
+  return k_cache != nullptr && reinterpret_cast<uintptr_t>(k_cache) % (kcache_fp4(b) ? 32 : 16) == 0;
 }
 
 int64_t logits_ld(const DsaBatch* b) {
@@ -176,6 +189,7 @@ PrologueArgs plan_only(const DsaBatch* b, const IndexerWs& ws, int sms, const vo
   pa.slot_mapping = slot_mapping;
   pa.k_cache = k_cache;
   pa.num_blocks = b->num_blocks;
+  pa.k_fp4 = kcache_fp4(b);
   pa.n_tokens = b->num_tokens;
   pa.plan = b->num_reqs > b->num_decodes;
   pa.p = plan_args(b, ws, sms, dev_err);
@@ -213,18 +227,19 @@ int run_logits(const DsaBatch* b, const uint8_t* q_fp8, const float* w_folded, c
   int st = device_sms(&sms);
   if (st != DSA_OK) return st;
   CUtensorMap mk, mq1, mq4;
-  if ((st = make_kcache_map(&mk, k_cache, b->num_blocks)) != DSA_OK) return st;
+  const bool fp4 = kcache_fp4(b);
+  if ((st = make_kcache_map(&mk, k_cache, b->num_blocks, fp4)) != DSA_OK) return st;
   LogitsArgs a{w_folded,          k_cache,    b->block_table,   b->bt_stride,   b->num_blocks,
                logits,            ld,         hist ? ws.hist : nullptr,          hist ? ws.hist_rows : 0,
                b->query_start_loc, b->seq_lens, b->req_id_per_token, b->num_decodes, b->num_decode_tokens,
                dev_err};
   if (b->num_decodes > 0) {
     if ((st = make_q_map(&mq1, q_fp8, b->num_tokens, kHeads)) != DSA_OK) return st;
-    if ((st = launched(launch_logits(1, &mk, &mq1, SegmentPlan{}, a, grid_ctas(sms), stream), stream)) != DSA_OK) return st;
+    if ((st = launched(launch_logits(1, fp4, &mk, &mq1, SegmentPlan{}, a, grid_ctas(sms), stream), stream)) != DSA_OK) return st;
   }
   if (b->num_reqs > b->num_decodes) {
     if ((st = make_q_map(&mq4, q_fp8, b->num_tokens, kPrefillTok * kHeads)) != DSA_OK) return st;
-    if ((st = launched(launch_logits(kPrefillTok, &mk, &mq4, ws.pre, a, grid_ctas(sms), stream), stream)) != DSA_OK)
+    if ((st = launched(launch_logits(kPrefillTok, fp4, &mk, &mq4, ws.pre, a, grid_ctas(sms), stream), stream)) != DSA_OK)
       return st;
   }
   return DSA_OK;
@@ -264,7 +279,7 @@ const char* dsa_status_string(int status) {
   }
 }
 
-int dsa_version(void) { return 200; }
+int dsa_version(void) { return 300; }
 
 int dsa_check_device_error(const int32_t* dev_err, uint32_t* out, dsa_stream_t stream) {
   if (dev_err == nullptr) return DSA_EINVAL;
@@ -284,7 +299,23 @@ int dsa_indexer_k_quant_write(const void* k, int64_t n_tokens, int64_t k_row_str
   int sms;
   int st = device_sms(&sms);
   if (st != DSA_OK) return st;
-  return from_cuda(launch_k_quant_write(k, n_tokens, k_row_stride, slot_mapping, k_cache, num_blocks, RopeArgs{},
+  return from_cuda(launch_k_quant_write(k, n_tokens, k_row_stride, slot_mapping, k_cache, num_blocks, false,
+                                        RopeArgs{}, dev_err, stream));
+}
+
+int dsa_indexer_k_quant_write_fp4(const void* k, int64_t n_tokens, int64_t k_row_stride, const int64_t* positions,
+                                  const float* cos_sin, int64_t max_pos, const int64_t* slot_mapping,
+                                  uint8_t* k_cache, int64_t num_blocks, int32_t* dev_err, dsa_stream_t stream) {
+  if (n_tokens < 0 || num_blocks < 1 || k_row_stride < kDim || k_row_stride % 8 != 0) return DSA_EINVAL;
+  if (cos_sin != nullptr && (max_pos < 1 || !positions || !aligned16(cos_sin))) return DSA_EINVAL;
+  if (n_tokens == 0) return DSA_OK;
+  if (!k || !slot_mapping || !k_cache || !aligned16(k) || reinterpret_cast<uintptr_t>(k_cache) % 32 != 0)
+    return DSA_EINVAL;
+  int sms;
+  int st = device_sms(&sms);
+  if (st != DSA_OK) return st;
+  const RopeArgs rope = cos_sin ? RopeArgs{positions, cos_sin, max_pos} : RopeArgs{};
+  return from_cuda(launch_k_quant_write(k, n_tokens, k_row_stride, slot_mapping, k_cache, num_blocks, true, rope,
                                         dev_err, stream));
 }
 
@@ -327,7 +358,7 @@ int dsa_indexer_k_rope_quant_write(const void* k, int64_t n_tokens, int64_t k_ro
   int sms;
   int st = device_sms(&sms);
   if (st != DSA_OK) return st;
-  return from_cuda(launch_k_quant_write(k, n_tokens, k_row_stride, slot_mapping, k_cache, num_blocks,
+  return from_cuda(launch_k_quant_write(k, n_tokens, k_row_stride, slot_mapping, k_cache, num_blocks, false,
                                         RopeArgs{positions, cos_sin, max_pos}, dev_err, stream));
 }
 
@@ -381,7 +412,7 @@ int dsa_indexer_logits(const DsaBatch* batch, const uint8_t* q_fp8, const float*
   if (st != DSA_OK) return st;
   if (batch->num_tokens == 0) return DSA_OK;
   if (!q_fp8 || !w_folded || !k_cache || !logits || !ws || logits_ld < batch->max_seq_len) return DSA_EINVAL;
-  if (!aligned16(q_fp8) || !aligned16(w_folded) || !aligned16(k_cache) || !aligned16(ws)) return DSA_EINVAL;
+  if (!aligned16(q_fp8) || !aligned16(w_folded) || !kcache_aligned(batch, k_cache) || !aligned16(ws)) return DSA_EINVAL;
   IndexerWs w = carve(batch, ws);
   if (ws_bytes < w.bytes) return DSA_ENOSPACE;
   return run_logits(batch, q_fp8, w_folded, k_cache, logits, logits_ld, w, false, dev_err, stream);
@@ -412,7 +443,7 @@ int dsa_indexer_logits_topk(const DsaBatch* batch, const uint8_t* q_fp8, const f
   if ((k_new == nullptr) != (slot_mapping == nullptr)) return DSA_EINVAL;
   if (batch->num_tokens == 0) return DSA_OK;
   if (!q_fp8 || !w_folded || !k_cache || !topk_out || !ws) return DSA_EINVAL;
-  if (!aligned16(q_fp8) || !aligned16(w_folded) || !aligned16(k_cache) || !aligned16(ws) || !aligned16(topk_out))
+  if (!aligned16(q_fp8) || !aligned16(w_folded) || !kcache_aligned(batch, k_cache) || !aligned16(ws) || !aligned16(topk_out))
     return DSA_EINVAL;
   IndexerWs w = carve(batch, ws);
   if (ws_bytes < w.bytes) return DSA_ENOSPACE;
@@ -503,7 +534,7 @@ int dsa_layer_stack_run(const DsaStackPlan* plan, const DsaBatch* batch, const i
     if (c != 'F' && c != 'S') return DSA_EINVAL;
     if (c == 'F' && batch->num_tokens > 0) {
       const DsaLayerInputs& L = plan->layers[l];
-      if (!L.q || !L.w || !L.k_cache || !aligned16(L.q) || !aligned16(L.k_cache)) return DSA_EINVAL;
+      if (!L.q || !L.w || !L.k_cache || !aligned16(L.q) || !kcache_aligned(batch, L.k_cache)) return DSA_EINVAL;
       if (L.k_new != nullptr && (slot_mapping == nullptr || !aligned16(L.k_new))) return DSA_EINVAL;
     }
   }

@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -73,6 +74,20 @@ __device__ __forceinline__ float ue8m0_scale(float amax) {
   return __uint_as_float((be - 8u + ((u & 0x7FFFFFu) > 0x600000u ? 1u : 0u)) << 23);
 }
 
+// The FP4 cache's scale: the smallest power of two 2^e >= RN(amax/6). With
+// amax = m*2^E (1 <= m < 2) and 6 = 1.5*2^2 that is e = E - 2, plus one when
+// m > 1.5. RN cannot move the quotient across the power of two: for m <= 1.5
+// amax/6 <= 2^(E-2) exactly, and for m >= 1.5 + 2^-23 the quotient is at
+// least 2^(E-2) (1 + 2^-23/1.5), which rounds to 2^(E-2) (1 + 2^-23). The
+// floor 1e-10 = 1.718*2^-34 gives 2^-35.
+__device__ __forceinline__ float ue8m0_scale_e2m1(float amax) {
+  amax = fmaxf(amax, 1e-10f);
+  const uint32_t u = __float_as_uint(amax);
+  const uint32_t be = u >> 23;
+  if (be == 255u) return __uint_as_float(0x7F800000u);  // amax = +inf
+  return __uint_as_float((be - 2u + ((u & 0x7FFFFFu) > 0x400000u ? 1u : 0u)) << 23);
+}
+
 // 2^-e for a normal power of two s = 2^e (|e| <= 126).
 __device__ __forceinline__ float pow2_reciprocal(float s) {
   uint32_t e = __float_as_uint(s) >> 23;
@@ -105,6 +120,46 @@ __device__ __forceinline__ uint32_t quant_row_lane(uint2 raw, float* scale_out) 
   float inv = pow2_reciprocal(s);
   *scale_out = s;
   return e4m3x4(f0.x * inv, f0.y * inv, f1.x * inv, f1.y * inv);
+}
+
+// Four fp32 values -> four E2M1 codes (nearest-even, saturating), first value
+// in the lowest nibble.
+__device__ __forceinline__ uint32_t e2m1x4(float a, float b, float c, float d) {
+  const __nv_fp4x2_storage_t lo = __nv_cvt_float2_to_fp4x2(make_float2(a, b), __NV_E2M1, cudaRoundNearest);
+  const __nv_fp4x2_storage_t hi = __nv_cvt_float2_to_fp4x2(make_float2(c, d), __NV_E2M1, cudaRoundNearest);
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 8);
+}
+
+// quant_row_lane for the FP4 cache: the 4 E2M1 codes of this lane (16 bits).
+__device__ __forceinline__ uint32_t quant_row_lane_e2m1(uint2 raw, float* scale_out) {
+  const float2 f0 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&raw.x));
+  const float2 f1 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&raw.y));
+  float amax = fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y)));
+  amax = warp_max(amax);
+  const float s = ue8m0_scale_e2m1(amax);
+  const float inv = pow2_reciprocal(s);
+  *scale_out = s;
+  return e2m1x4(f0.x * inv, f0.y * inv, f1.x * inv, f1.y * inv);
+}
+
+// S1's store: quantise the K row a warp holds (lane i: values 4i..4i+3) and
+// write it at `slot` of an FP8 cache (8448-byte pages: 128 code bytes per
+// row) or an FP4 cache (4352-byte pages: 64 code bytes per row), the fp32
+// scale after the page's 64 rows.
+__device__ __forceinline__ void quant_store_k_row(uint8_t* cache, int64_t slot, uint2 raw, bool fp4, int lane) {
+  const int off = static_cast<int>(slot % kBlock);
+  float s;
+  if (fp4) {
+    const uint32_t codes = quant_row_lane_e2m1(raw, &s);
+    uint8_t* page = cache + (slot / kBlock) * kFp4PageBytes;
+    reinterpret_cast<uint16_t*>(page + off * (kDim / 2))[lane] = static_cast<uint16_t>(codes);
+    if (lane == 0) *reinterpret_cast<float*>(page + kFp4ScaleOffset + off * 4) = s;
+  } else {
+    const uint32_t codes = quant_row_lane(raw, &s);
+    uint8_t* page = cache + (slot / kBlock) * kPageBytes;
+    reinterpret_cast<uint32_t*>(page + off * kDim)[lane] = codes;
+    if (lane == 0) *reinterpret_cast<float*>(page + kScaleOffset + off * 4) = s;
+  }
 }
 
 // RoPE of the leading 64 dims of one 128-value bf16 row held by a warp (lane
@@ -275,11 +330,14 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor of tcgen05.mma.kind::f8f6f4: E4M3 x E4M3 -> fp32,
-// both operands K-major, M x N tile.
-__host__ __device__ constexpr uint32_t f8_idesc(int M, int N) {
+// Instruction descriptor of tcgen05.mma.kind::f8f6f4 -> fp32, both operands
+// K-major, M x N tile. B is E4M3; A is E4M3 (format 0) or, with a_e2m1, E2M1
+// (format 5), which the MMA reads from shared memory with each 16-byte chunk
+// holding 16 codes in its first 8 bytes (the image a TMA load of the
+// 16U4_ALIGN16B type lands); the K step stays 32 elements = 32 bytes.
+__host__ __device__ constexpr uint32_t f8_idesc(int M, int N, bool a_e2m1 = false) {
   return (1u << 4)                                  // D format: fp32
-         | (0u << 7) | (0u << 10)                   // A, B format: E4M3
+         | ((a_e2m1 ? 5u : 0u) << 7) | (0u << 10)   // A format, B format: E4M3
          | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
 }

@@ -15,6 +15,8 @@ constexpr int kDim = DSA_HEAD_DIM;
 constexpr int kBlock = DSA_BLOCK_SIZE;
 constexpr int kPageBytes = DSA_PAGE_BYTES;
 constexpr int kScaleOffset = kBlock * kDim;  // 8192: the 64 fp32 scales follow the 64 K rows
+constexpr int kFp4PageBytes = DSA_FP4_PAGE_BYTES;      // FP4 cache: 64 rows of 64 E2M1 bytes, then the scales
+constexpr int kFp4ScaleOffset = kBlock * kDim / 2;     // 4096
 constexpr int kRope = 64;                    // rotated leading dims of q and K rows
 
 // RoPE fused into the quantiser: cos_sin == nullptr means the rows arrive rotated.
@@ -54,8 +56,9 @@ struct SegmentPlan {
   int32_t max_qb;       // capacity of qb / tile_start
 };
 
+// fp4: the cache has FP4 pages (E2M1 codes) instead of FP8 pages.
 cudaError_t launch_k_quant_write(const void* k, int64_t n, int64_t row_stride, const int64_t* slot_mapping,
-                                 uint8_t* cache, int64_t num_blocks, const RopeArgs& rope, int32_t* err,
+                                 uint8_t* cache, int64_t num_blocks, bool fp4, const RopeArgs& rope, int32_t* err,
                                  cudaStream_t stream);
 cudaError_t launch_q_quant_fold(const void* q, const float* w, int64_t n_tokens, float softmax_scale,
                                 uint8_t* q_fp8, float* q_scale, float* w_folded, const RopeArgs& rope,
@@ -87,6 +90,7 @@ struct PrologueArgs {
   const int64_t* slot_mapping;    // [T]
   uint8_t* k_cache;
   int64_t num_blocks;
+  bool k_fp4;               // k_cache has FP4 pages
   int n_tokens;
   RopeArgs rope;            // RoPE of q and k_new rows before the quantiser (optional)
   bool plan;
@@ -157,8 +161,9 @@ struct SelectArgs {
 
 // ntok_per_block = 1 (decode segment: the kernel plans its slice from the
 // request metadata in `a`, `plan` is unused) or kPrefillTok (prefill segment,
-// `plan` written by the prologue).
-cudaError_t launch_logits(int ntok_per_block, const CUtensorMap* tmap_k, const CUtensorMap* tmap_q,
+// `plan` written by the prologue). fp4: the K cache has FP4 pages and tmap_k
+// describes them (make_kcache_map with fp4).
+cudaError_t launch_logits(int ntok_per_block, bool fp4, const CUtensorMap* tmap_k, const CUtensorMap* tmap_q,
                           SegmentPlan plan, const LogitsArgs& a, int num_sms, cudaStream_t stream);
 
 // Rows [row_begin, n_tokens): one CTA per row. Rows t < hist_rows take their

@@ -27,7 +27,13 @@
 namespace dsa {
 
 // ------------------------------------------------------------------ logits
-template <int NTOK>
+// FP4: the K cache holds E2M1 codes (4352-byte pages). The TMA box of a page
+// is then read with the packed 4-bit type, which lands each row as 128 bytes
+// in shared memory (8 code bytes and an 8-byte gap per 16-byte chunk, the
+// same 128-byte swizzle) and completes 4096 transaction bytes — the global
+// bytes it read. The MMA, the epilogue and the shared-memory layout are the
+// FP8 cache's.
+template <int NTOK, bool FP4>
 struct LogitsCfg {
   static constexpr int N = 64 * NTOK;                     // MMA N: heads x tokens
   static constexpr int kStages = NTOK == 1 ? 8 : 6;       // K-tile ring
@@ -61,7 +67,10 @@ struct LogitsCfg {
   static constexpr int kHistBytes = NTOK == 1 ? kEpiWG * kHistBins * 4 : 0;
   static constexpr int kOffHist = (kOffMeta + 2 * 24 + 4 * 4 + 33 * 4 + 127) / 128 * 128;
   static constexpr int kSmemBytes = kOffHist + kHistBytes + 1024;  // + slack to align the base to 1024
-  static constexpr uint32_t kIdesc = f8_idesc(128, N);
+  static constexpr uint32_t kIdesc = f8_idesc(128, N, FP4);
+  static constexpr int64_t kPage = FP4 ? kFp4PageBytes : kPageBytes;     // bytes per K-cache page
+  static constexpr int64_t kPageScales = FP4 ? kFp4ScaleOffset : kScaleOffset;
+  static constexpr uint32_t kPageTx = (FP4 ? 4096 : 8192) + 256;          // TMA + scale bytes per page
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation must be a power of two");
 };
@@ -159,11 +168,11 @@ __device__ void decode_slice(const LogitsArgs& a, int* slice, int* scan) {
   __syncthreads();
 }
 
-template <int NTOK>
-__global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
+template <int NTOK, bool FP4>
+__global__ void __launch_bounds__(LogitsCfg<NTOK, FP4>::kThreads, 1)
     logits_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
                   SegmentPlan plan, LogitsArgs a) {
-  using C = LogitsCfg<NTOK>;
+  using C = LogitsCfg<NTOK, FP4>;
   constexpr int S = C::kStages;
   constexpr int A = C::kAcc;
   extern __shared__ uint8_t smem_raw[];
@@ -245,16 +254,14 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
     const bool v0 = id0 >= 0 && id0 < a.num_blocks;
     const bool v1 = in1 && id1 >= 0 && id1 < a.num_blocks;
     if (!v0 || (in1 && !v1)) flag_error(a.err, DSA_DEVERR_BLOCK_RANGE);
-    mbar_arrive_expect_tx(&full[stage], (v0 ? 8192 + 256 : 0) + (v1 ? 8192 + 256 : 0));
+    mbar_arrive_expect_tx(&full[stage], (v0 ? C::kPageTx : 0) + (v1 ? C::kPageTx : 0));
     if (v0) {
       tma_load_3d(st, &tmap_k, &full[stage], 0, 0, id0);
-      bulk_load(st + C::kScaleOff, a.k_cache + static_cast<int64_t>(id0) * kPageBytes + kScaleOffset, 256,
-                &full[stage]);
+      bulk_load(st + C::kScaleOff, a.k_cache + id0 * C::kPage + C::kPageScales, 256, &full[stage]);
     }
     if (v1) {
       tma_load_3d(st + 8192, &tmap_k, &full[stage], 0, 0, id1);
-      bulk_load(st + C::kScaleOff + 256, a.k_cache + static_cast<int64_t>(id1) * kPageBytes + kScaleOffset, 256,
-                &full[stage]);
+      bulk_load(st + C::kScaleOff + 256, a.k_cache + id1 * C::kPage + C::kPageScales, 256, &full[stage]);
     }
   };
 
@@ -491,25 +498,28 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK>::kThreads, 1)
   }
 }
 
-template <int NTOK>
+template <int NTOK, bool FP4>
 static cudaError_t launch_logits_t(const CUtensorMap* tmap_k, const CUtensorMap* tmap_q, SegmentPlan plan,
                                    const LogitsArgs& a, int num_sms, cudaStream_t stream) {
-  using C = LogitsCfg<NTOK>;
+  using C = LogitsCfg<NTOK, FP4>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(logits_kernel<NTOK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(logits_kernel<NTOK, FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_pdl(logits_kernel<NTOK>, dim3(num_sms), dim3(C::kThreads), C::kSmemBytes, stream, *tmap_k, *tmap_q,
-                    plan, a);
+  return launch_pdl(logits_kernel<NTOK, FP4>, dim3(num_sms), dim3(C::kThreads), C::kSmemBytes, stream, *tmap_k,
+                    *tmap_q, plan, a);
 }
 
-cudaError_t launch_logits(int ntok_per_block, const CUtensorMap* tmap_k, const CUtensorMap* tmap_q,
+cudaError_t launch_logits(int ntok_per_block, bool fp4, const CUtensorMap* tmap_k, const CUtensorMap* tmap_q,
                           SegmentPlan plan, const LogitsArgs& a, int num_sms, cudaStream_t stream) {
-  if (ntok_per_block == 1) return launch_logits_t<1>(tmap_k, tmap_q, plan, a, num_sms, stream);
-  return launch_logits_t<kPrefillTok>(tmap_k, tmap_q, plan, a, num_sms, stream);
+  if (ntok_per_block == 1)
+    return fp4 ? launch_logits_t<1, true>(tmap_k, tmap_q, plan, a, num_sms, stream)
+               : launch_logits_t<1, false>(tmap_k, tmap_q, plan, a, num_sms, stream);
+  return fp4 ? launch_logits_t<kPrefillTok, true>(tmap_k, tmap_q, plan, a, num_sms, stream)
+             : launch_logits_t<kPrefillTok, false>(tmap_k, tmap_q, plan, a, num_sms, stream);
 }
 
 }  // namespace dsa

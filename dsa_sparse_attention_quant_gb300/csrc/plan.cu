@@ -143,6 +143,9 @@ __device__ void plan_batch(const PlanArgs& p, PlanSmem& S) {
 // CTAs fit beside a score-kernel CTA that starts early on the same SM.
 constexpr int kPrologueThreads = 256;
 
+// FP4: the K cache has FP4 pages (a.k_fp4), fixed per instance so that the
+// K store of the other format costs no registers.
+template <bool FP4>
 __global__ void __launch_bounds__(kPrologueThreads, 6) prologue_kernel(PrologueArgs a) {
   extern __shared__ __align__(16) uint8_t plan_smem[];
   pdl_launch_dependents();  // the score kernel may start its set-up now
@@ -203,12 +206,7 @@ __global__ void __launch_bounds__(kPrologueThreads, 6) prologue_kernel(PrologueA
         const float* cs = rope_row(a.rope, t, a.err, lane);
         if (cs != nullptr) raw = rope_row_lane(raw, cs);
       }
-      float s;
-      const uint32_t codes = quant_row_lane(raw, &s);
-      uint8_t* page = a.k_cache + (slot / kBlock) * kPageBytes;
-      const int off = static_cast<int>(slot % kBlock);
-      reinterpret_cast<uint32_t*>(page + off * kDim)[lane] = codes;
-      if (lane == 0) *reinterpret_cast<float*>(page + kScaleOffset + off * 4) = s;
+      quant_store_k_row(a.k_cache, slot, raw, FP4, lane);
     } else {
       const int64_t t = j - q_groups - k_rows;
       uint4* h = reinterpret_cast<uint4*>(a.hist + t * kHistBins);
@@ -228,7 +226,11 @@ cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t stream) {
   if (quant > 1216) quant = 1216;  // one wave of 8 CTAs per SM; the rest loops
   const size_t smem = a.plan ? sizeof(PlanSmem) : 0;
   static_assert(sizeof(PlanSmem) <= 48 * 1024, "plan staging fits the default dynamic shared memory");
-  prologue_kernel<<<static_cast<unsigned>(quant + (a.plan ? 1 : 0)), kPrologueThreads, smem, stream>>>(a);
+  const unsigned grid = static_cast<unsigned>(quant + (a.plan ? 1 : 0));
+  if (a.k_fp4)
+    prologue_kernel<true><<<grid, kPrologueThreads, smem, stream>>>(a);
+  else
+    prologue_kernel<false><<<grid, kPrologueThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 

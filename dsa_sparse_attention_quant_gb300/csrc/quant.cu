@@ -9,8 +9,8 @@
 // rotated on their leading 64 dims (RoPE, as `Indexer.forward` applies
 // `rotary_emb` before quantising). One warp handles one 128-value row: each
 // lane loads 8 bytes (4 bf16), the warp reduces amax with shuffles, and the
-// 32 lanes store 128 contiguous code bytes — fully coalesced, one pass over
-// HBM in each direction.
+// 32 lanes store 128 contiguous code bytes (64 for the FP4 cache) — fully
+// coalesced, one pass over HBM in each direction.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -20,7 +20,7 @@ __global__ void __launch_bounds__(256) k_quant_write_kernel(const __nv_bfloat16*
                                                             int64_t row_stride,
                                                             const int64_t* __restrict__ slot_mapping,
                                                             uint8_t* __restrict__ cache, int64_t num_blocks,
-                                                            RopeArgs rope, int32_t* err) {
+                                                            bool fp4, RopeArgs rope, int32_t* err) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   for (int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < n; t += warps) {
@@ -35,12 +35,7 @@ __global__ void __launch_bounds__(256) k_quant_write_kernel(const __nv_bfloat16*
       const float* cs = rope_row(rope, t, err, lane);  // warp-uniform
       if (cs != nullptr) raw = rope_row_lane(raw, cs);
     }
-    float s;
-    const uint32_t codes = quant_row_lane(raw, &s);
-    uint8_t* page = cache + (slot / kBlock) * kPageBytes;
-    const int off = static_cast<int>(slot % kBlock);
-    reinterpret_cast<uint32_t*>(page + off * kDim)[lane] = codes;
-    if (lane == 0) *reinterpret_cast<float*>(page + kScaleOffset + off * 4) = s;
+    quant_store_k_row(cache, slot, raw, fp4, lane);
   }
 }
 
@@ -125,12 +120,12 @@ static int grid_for_rows(int64_t rows, int warps_per_block) {
 }
 
 cudaError_t launch_k_quant_write(const void* k, int64_t n, int64_t row_stride, const int64_t* slot_mapping,
-                                 uint8_t* cache, int64_t num_blocks, const RopeArgs& rope, int32_t* err,
+                                 uint8_t* cache, int64_t num_blocks, bool fp4, const RopeArgs& rope, int32_t* err,
                                  cudaStream_t stream) {
   if (n <= 0) return cudaSuccess;
   k_quant_write_kernel<<<grid_for_rows(n, 8), 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(k), n,
-                                                                row_stride, slot_mapping, cache, num_blocks, rope,
-                                                                err);
+                                                                row_stride, slot_mapping, cache, num_blocks, fp4,
+                                                                rope, err);
   return cudaGetLastError();
 }
 

@@ -35,7 +35,8 @@
  *    the offending access (no trap, no fault) and keeps going; results that
  *    depend on the skipped data are unspecified. dev_err may be NULL.
  *  - Alignment: all device pointers 16-byte aligned; the K cache is
- *    num_blocks pages of 8448 bytes.
+ *    num_blocks pages of 8448 bytes (FP8) or, 32-byte aligned, of 4352 bytes
+ *    (FP4, DsaBatch.k_cache_format = DSA_KCACHE_FP4).
  */
 #ifndef DSAIDX_H
 #define DSAIDX_H
@@ -75,6 +76,10 @@ typedef struct CUstream_st *dsa_stream_t; /* same type as cudaStream_t */
 #define DSA_BLOCK_SIZE 64
 #define DSA_SLOT_BYTES 132                        /* 128 B FP8 K + 4 B fp32 scale */
 #define DSA_PAGE_BYTES (DSA_BLOCK_SIZE * DSA_SLOT_BYTES) /* 8448 */
+#define DSA_FP4_SLOT_BYTES 68                             /* 64 B E2M1 K (two per byte) + 4 B fp32 scale */
+#define DSA_FP4_PAGE_BYTES (DSA_BLOCK_SIZE * DSA_FP4_SLOT_BYTES) /* 4352 */
+#define DSA_KCACHE_FP8 0
+#define DSA_KCACHE_FP4 1
 
 DSA_API const char *dsa_status_string(int status);
 DSA_API int dsa_version(void); /* major*10000 + minor*100 + patch */
@@ -108,6 +113,7 @@ typedef struct DsaBatch {
   const int32_t *seq_lens;         /* device [B] */
   const int32_t *block_table;      /* device [B, bt_stride] */
   const int32_t *req_id_per_token; /* device [T] */
+  int32_t k_cache_format;          /* DSA_KCACHE_FP8 (0) or DSA_KCACHE_FP4: the K cache's pages */
 } DsaBatch;
 
 /* ------------------------------------------------- S1: K quant + cache */
@@ -125,6 +131,28 @@ typedef struct DsaBatch {
 DSA_API int dsa_indexer_k_quant_write(const void *k, int64_t n_tokens, int64_t k_row_stride,
                               const int64_t *slot_mapping, uint8_t *k_cache,
                               int64_t num_blocks, int32_t *dev_err, dsa_stream_t stream);
+
+/* ---------------------------------- the FP4 indexer K cache (next row) */
+/* [IC] hands `sparse_attn_indexer` a `use_fp4_cache` flag beside
+ * `quant_block_size` and `scale_fmt`; the pages give no more of the format.
+ * Reading taken: the element is E2M1 (OCP Microscaling Formats (MX)
+ * Specification v1.0, FP4: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6) and the
+ * quantiser is the FP8 cache's with E2M1 for E4M3 — one ue8m0 scale per
+ * token's 128 values, scale = 2^ceil(log2(max(amax, 1e-10)/6)), codes =
+ * RNE_satfinite(k/scale). Dim 2i goes to the low nibble and dim 2i+1 to the
+ * high nibble of byte i. A page holds the 64 rows of 64 code bytes, then the
+ * 64 fp32 scales: K bytes at page*4352 + (slot%64)*64, the scale at
+ * page*4352 + 4096 + (slot%64)*4. q stays FP8; the scores multiply E2M1 K by
+ * E4M3 q on the tensor cores (one kind::f8f6f4 MMA, the same fp32 sums).
+ * Select it for the score calls with DsaBatch.k_cache_format = DSA_KCACHE_FP4.
+ *   k_cache   device uint8 [num_blocks, 4352], 32-byte aligned, written
+ *   positions, cos_sin, max_pos: as dsa_indexer_k_rope_quant_write, or
+ *             cos_sin = NULL (positions unused) for rows that arrive rotated
+ * Everything else as dsa_indexer_k_quant_write. */
+DSA_API int dsa_indexer_k_quant_write_fp4(const void *k, int64_t n_tokens, int64_t k_row_stride,
+                                  const int64_t *positions, const float *cos_sin, int64_t max_pos,
+                                  const int64_t *slot_mapping, uint8_t *k_cache,
+                                  int64_t num_blocks, int32_t *dev_err, dsa_stream_t stream);
 
 /* ------------------------------- RoPE fused into S1 and S2a (next row) */
 /* [IC] `Indexer.forward` rotates the leading qk_rope_head_dim = 64 dims of
@@ -173,8 +201,11 @@ DSA_API int dsa_indexer_q_quant_fold(const void *q, const float *w, int64_t n_to
  * scores of row t, in no particular order, followed by -1 when the row has
  * fewer than `topk` keys. Every row [0, T) is written.
  *   q_fp8, w_folded  from dsa_indexer_q_quant_fold
- *   k_cache          device uint8 [num_blocks, 8448]; must hold every key the
- *                    rows see (write this step's K first, or pass k_new)
+ *   k_cache          device uint8 [num_blocks, 8448], or [num_blocks, 4352]
+ *                    with batch->k_cache_format = DSA_KCACHE_FP4 (E2M1 K, see
+ *                    dsa_indexer_k_quant_write_fp4); must hold every key the
+ *                    rows see (write this step's K first, or pass k_new, which
+ *                    is then quantised in the cache's format)
  *   topk             1..4096, multiple of 4
  *   topk_out         device int32 [T, topk]
  *   ws, ws_bytes     device scratch of dsa_indexer_workspace_size() bytes
@@ -311,7 +342,7 @@ typedef struct DsaLayerInputs {
   const void *q;        /* device bf16 [T, 64, 128] */
   const float *w;       /* device fp32 [T, 64] */
   const void *k_new;    /* device bf16 [T, 128] or NULL (skip the cache insert) */
-  uint8_t *k_cache;     /* device uint8 [num_blocks, 8448] */
+  uint8_t *k_cache;     /* device uint8 [num_blocks, 8448], or 4352 with an FP4 batch */
 } DsaLayerInputs;
 
 typedef void (*dsa_layer_consumer_fn)(int32_t layer, int32_t producer,

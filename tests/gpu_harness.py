@@ -16,16 +16,17 @@ def bf16_tensor(bits: np.ndarray) -> torch.Tensor:
 
 
 class DeviceBatch:
-    """A synth.Batch uploaded to the GPU, with its K cache filled by the CUDA path."""
+    """A synth.Batch uploaded to the GPU, with its K cache (FP8 or FP4 pages)
+    filled by the CUDA path."""
 
-    def __init__(self, hb: synth.Batch, fill_context: bool = True):
+    def __init__(self, hb: synth.Batch, fill_context: bool = True, fmt: str = "fp8"):
         self.hb = hb
         self.batch = dsa.Batch.from_host(hb, DEV)
         self.q = bf16_tensor(hb.q)
         self.w = torch.from_numpy(hb.w).to(DEV)
         self.k_new = bf16_tensor(hb.k_new)
         self.slot_mapping = torch.from_numpy(hb.slot_mapping).to(DEV)
-        self.k_cache = torch.zeros((hb.num_blocks, synth.BLOCK_SIZE * 132), dtype=torch.uint8, device=DEV)
+        self.k_cache = dsa.new_k_cache(hb.num_blocks, fmt, device=DEV)
         self.dev_err = torch.zeros(1, dtype=torch.int32, device=DEV)
         if fill_context and hb.ctx_k.shape[0]:
             ctx = bf16_tensor(hb.ctx_k)

@@ -32,11 +32,12 @@ def conversion_table(hb, row):
     return phys[0]
 
 
-def check_batch(hb, rows=None, check_logits=True):
-    db = DeviceBatch(hb)
+def check_batch(hb, rows=None, check_logits=True, fmt="fp8"):
+    """The whole path on ``hb`` with an FP8 or FP4 K cache against the oracle."""
+    db = DeviceBatch(hb, fmt=fmt)
     res = db.run(with_logits=check_logits)
     assert res["dev_err"] == 0, f"device error word {res['dev_err']:#x}"
-    cache = oracle.fill_cache(hb)
+    cache = oracle.fill_cache(hb, fmt=fmt)
     # S1: every byte of the cache
     assert np.array_equal(res["cache"].reshape(-1), cache.reshape(-1)), "K cache bytes differ"
     # S2a: q codes, scales, folded weights

@@ -17,7 +17,7 @@ from tests.gpu_harness import DEV, bf16_tensor
 pytestmark = pytest.mark.gpu
 
 
-def run_stack(n_layers, freq, scale, n_decode, pattern=None, check_rows=None):
+def run_stack(n_layers, freq, scale, n_decode, pattern=None, check_rows=None, fmt="fp8"):
     fs, prod = dsa.schedule_build(n_layers, True, freq, 2, pattern)
     fs_o, prod_o = oracle.schedule(n_layers, True, freq, 2, pattern)
     assert fs == fs_o and prod == prod_o.tolist()
@@ -34,7 +34,7 @@ def run_stack(n_layers, freq, scale, n_decode, pattern=None, check_rows=None):
             layers.append(None)
             continue
         hb = hbs[l]
-        cache = torch.zeros((hb.num_blocks, 8448), dtype=torch.uint8, device=DEV)
+        cache = dsa.new_k_cache(hb.num_blocks, fmt, device=DEV)
         dsa.indexer_k_quant_write(bf16_tensor(hb.ctx_k), torch.from_numpy(hb.ctx_slots).to(DEV), cache, err)
         layers.append(dict(q=bf16_tensor(hb.q), w=torch.from_numpy(hb.w).to(DEV), k_new=bf16_tensor(hb.k_new),
                            k_cache=cache))
@@ -60,7 +60,7 @@ def run_stack(n_layers, freq, scale, n_decode, pattern=None, check_rows=None):
         assert torch.equal(snap[l][2], snap[p][2]) and torch.equal(snap[l][3], snap[p][3])
     rows = np.arange(T) if check_rows is None else check_rows
     for l, hb in hbs.items():
-        cache = oracle.fill_cache(hb)
+        cache = oracle.fill_cache(hb, fmt=fmt)
         assert np.array_equal(layers[l]["k_cache"].cpu().numpy(), cache), f"layer {l}: cache bytes"
         _, scores = oracle.indexer(hb, cache, rows=rows, with_scores=True)
         lens = hb.positions[rows] + 1

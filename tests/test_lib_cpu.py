@@ -28,7 +28,7 @@ def test_library_exports_every_declared_symbol():
     lib = binding.load()
     for name in declared_symbols():
         assert hasattr(lib, name), name
-    assert lib.dsa_version() == 200
+    assert lib.dsa_version() == 300
     assert lib.dsa_status_string(0) == b"ok"
     assert b"invalid" in lib.dsa_status_string(1)
 
@@ -117,3 +117,55 @@ def test_rope_entry_points_reject_bad_arguments_on_the_host():
     assert q_fold(fake, fake, 4, fake, None, 16, 0.0, fake, None, fake, None, None) == binding.DSA_EINVAL
     assert q_fold(fake, fake, 4, fake, fake, 0, 0.0, fake, None, fake, None, None) == binding.DSA_EINVAL
     assert q_fold(fake, fake, 0, fake, fake, 16, 0.0, fake, None, fake, None, None) == binding.DSA_OK
+
+
+def test_fp4_cache_arguments_rejected_on_the_host():
+    lib = binding.load()
+    P = ctypes.c_void_p
+    fake = P(4096)  # never dereferenced: every call below fails its host checks first
+    w4 = lib.dsa_indexer_k_quant_write_fp4
+    # the FP4 cache must be 32-byte aligned (the packed 4-bit tensor-map type)
+    assert w4(fake, 4, 128, None, None, 0, fake, P(4112), 8, None, None) == binding.DSA_EINVAL
+    # a cos/sin table needs positions and a positive max_pos
+    assert w4(fake, 4, 128, None, fake, 16, fake, fake, 8, None, None) == binding.DSA_EINVAL
+    assert w4(fake, 4, 128, fake, fake, 0, fake, fake, 8, None, None) == binding.DSA_EINVAL
+    assert w4(fake, 4, 100, None, None, 0, fake, fake, 8, None, None) == binding.DSA_EINVAL
+    assert w4(fake, 0, 128, None, None, 0, fake, fake, 8, None, None) == binding.DSA_OK
+    # an unknown cache format, and an FP4 cache that is only 16-byte aligned
+    bad = binding.DsaBatchC(1, 1, 1, 1, 10, 1, 1, fake, fake, fake, fake, 2)
+    assert lib.dsa_indexer_logits_topk(ctypes.byref(bad), fake, fake, fake, 64, fake, fake, 1 << 30, None, None,
+                                       None, None) == binding.DSA_EINVAL
+    fp4 = binding.DsaBatchC(1, 1, 1, 1, 10, 1, 1, fake, fake, fake, fake, 1)
+    assert lib.dsa_indexer_logits_topk(ctypes.byref(fp4), fake, fake, P(4112), 64, fake, fake, 1 << 30, None, None,
+                                       None, None) == binding.DSA_EINVAL
+
+
+def test_cache_format_from_page_size():
+    assert binding.cache_format(torch.zeros((3, 8448), dtype=torch.uint8)) == 0
+    assert binding.cache_format(torch.zeros((3, 4352), dtype=torch.uint8)) == 1
+    assert binding.cache_format(torch.zeros((3, 64, 68), dtype=torch.uint8)) == 1
+    with pytest.raises(binding.DsaError):
+        binding.cache_format(torch.zeros((3, 4096), dtype=torch.uint8))
+
+
+def test_fp4_scale_exponent_rule_equals_division_for_every_bf16_amax():
+    # The GPU's FP4 scale comes from amax's exponent bits (e = E - 2, plus one
+    # when the significand exceeds 1.5) instead of dividing by 6; for every
+    # finite bf16 amax (and the 1e-10 floor) that equals the oracle's rule,
+    # RN(amax / 6) rounded up to a power of two.
+    b = np.arange(0x0000, 0x7F80, dtype=np.uint32)
+    a = np.maximum((b << 16).view(np.float32), np.float32(1e-10))
+    ref = np.array([oracle.ue8m0_scale_e2m1(float(x)) for x in a[::97]], np.float32)
+    u = a.view(np.uint32)
+    rule = (((u >> 23) - 2 + ((u & 0x7FFFFF) > 0x400000)) << 23).astype(np.uint32).view(np.float32)
+    assert np.array_equal(rule[::97].view(np.uint32), ref.view(np.uint32))
+    r = (a / np.float32(6.0)).astype(np.float32).view(np.uint32)
+    up = np.where((r & 0x7FFFFF) != 0, (r & 0x7F800000) + 0x800000, r).astype(np.uint32)
+    assert np.array_equal(rule.view(np.uint32), up)
+
+
+def test_cache_format_of_an_empty_cache():
+    assert binding.cache_format(torch.zeros((0, 8448), dtype=torch.uint8)) == 0
+    assert binding.cache_format(torch.zeros((0, 4352), dtype=torch.uint8)) == 1
+    with pytest.raises(binding.DsaError):
+        binding.cache_format(torch.zeros(8448, dtype=torch.uint8))
