@@ -16,8 +16,9 @@
 //    persistent CTA takes one contiguous, equally sized slice of it, so the
 //    load is balanced to one tile whatever the mix of lengths.
 //  * Warp roles: warp 0 issues TMA (K pages, K scales, q block, w' block),
-//    warp 1 issues the MMAs, the remaining warps read TMEM and apply
-//    ReLU, the w' reduction and the K scale, and store fp32 scores.
+//    with warp 2 sharing the K tiles in the decode instance; warp 1 issues
+//    the MMAs; the remaining warps read TMEM and apply ReLU, the w'
+//    reduction and the K scale, and store fp32 scores.
 //  * Decode rows also get their score histogram (pass 1 of the top-k radix
 //    select), so the top-k never scans a decode row to find its boundary bin.
 //  * Every wait is bounded in time (DSA_DEVERR_TIMEOUT, then an orderly exit).
@@ -51,7 +52,16 @@ struct LogitsCfg {
   static constexpr int kEpiWG = kTeams * kTeamWG;
   static constexpr int kTokPerWG = NTOK / kTeamWG;          // tokens of a tile one warpgroup reduces
   static constexpr int kEpiWarps = 4 * kEpiWG;
-  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  // K-tile producers: warp 0 (which also loads the q / w' blocks) and, for
+  // decode, warp 2. Tile n is issued by producer n % kProducers: one issuing
+  // thread sustained only about one page copy per 0.2 us whatever its size
+  // (8448-byte FP8 and 4352-byte FP4 pages alike), so a decode score stream
+  // (two pages per tile and little else per tile) runs faster with two
+  // issuers (decode8x128k step 54.4 -> 50.9 us; three or four measured the
+  // same as two). Warp 1 issues the MMAs; the epilogue warpgroups follow.
+  static constexpr int kProducers = NTOK == 1 ? 2 : 1;
+  static constexpr int kEpiWarp0 = 1 + kProducers;
+  static constexpr int kThreads = 32 * kEpiWarp0 + 32 * kEpiWarps;
   static constexpr uint32_t kTmemCols = N * kAcc;         // 256 (decode) or 512 (prefill)
   static constexpr int kStageBytes = 17 * 1024;           // 2 x 8 KB K pages, 2 x 256 B scales, 1 KB aligned
   static constexpr int kScaleOff = 16384;
@@ -244,7 +254,7 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK, FP4>::kThreads, 1)
   const int items = it_end - it_begin;  // tiles of this CTA (an empty slice runs no loop)
   pdl_launch_dependents();
   if constexpr (NTOK == 1) {
-    if (warp != 0) pdl_wait();  // the producer waits after its early loads
+    if (warp == 1 || warp >= C::kEpiWarp0) pdl_wait();  // the producers wait after their early loads
   }
 
   // Issue the loads of tile kt of a block (pages 2kt, 2kt+1) into a stage.
@@ -265,8 +275,10 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK, FP4>::kThreads, 1)
     }
   };
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 0 || (warp >= 2 && warp < C::kEpiWarp0)) {
+    // ------------------------------------------------------------ producers
+    const int pi = warp == 0 ? 0 : warp - 1;  // this producer issues tiles n with n % np == pi
+    constexpr int np = C::kProducers;
     auto block_at = [&](int j, QBlock* qb, int* first_new) -> int {  // block j and its tile count
       if constexpr (NTOK == 1) {
         return decode_block(a, j, qb, first_new);
@@ -281,8 +293,9 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK, FP4>::kThreads, 1)
     QBlock qb{};
     int first_new = 0;
     int block_tiles = items > 0 ? block_at(j, &qb, &first_new) : 0;
-    // decode: before the wait, fill the ring with tiles of the first block
-    // whose two pages lie below the first page this step writes
+    // decode: before the wait, the producers fill the ring with their tiles
+    // of the first block whose two pages lie below the first page this step
+    // writes (the block table and the lengths are inputs of the step)
     int npre = 0;
     if constexpr (NTOK == 1) {
       const int safe_pages = first_new / kBlock;
@@ -291,29 +304,31 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK, FP4>::kThreads, 1)
       if (cnt > 0) {
         const int32_t* bt_row = a.block_table + static_cast<int64_t>(qb.req) * a.bt_stride;
         const int32_t id = lane < 2 * cnt ? __ldg(bt_row + 2 * kt + lane) : -1;
-        for (int e = 0; e < cnt; ++e) {
+        for (int e = pi; e < cnt; e += np) {
           const int id0 = __shfl_sync(0xffffffffu, id, 2 * e);
           const int id1 = __shfl_sync(0xffffffffu, id, 2 * e + 1);
           if (lane == 0) issue_tile(e, kt + e, 2 * (kt + e) + 2, id0, id1);
         }
-        npre = cnt;
       }
+      npre = max(cnt, 0);
       pdl_wait();
     }
     while (ok && n < items) {
       const int in_slice = min(block_tiles - kt, items - n);
-      const int qs = qcount & 1;
-      int w = 1;
-      if (lane == 0) w = mbar_wait(&qempty[qs], ((qcount >> 1) & 1) ^ 1, abort_flag, a.err);
-      if (!__shfl_sync(0xffffffffu, w, 0)) break;
-      if (lane == 0) {
-        qmeta[qs] = QMeta{qb, in_slice, kt};
-        mbar_arrive_expect_tx(&qfull[qs], C::kQBytes + qb.ntok * kHeads * 4);
-        tma_load_2d(smem + C::kOffQ + qs * C::kQBytes, &tmap_q, &qfull[qs], 0, qb.t0 * kHeads);
-        bulk_load(smem + C::kOffW + qs * C::kWBytes, a.w_folded + static_cast<int64_t>(qb.t0) * kHeads,
-                  qb.ntok * kHeads * 4, &qfull[qs]);
+      if (pi == 0) {  // the block's q codes and w'
+        const int qs = qcount & 1;
+        int w = 1;
+        if (lane == 0) w = mbar_wait(&qempty[qs], ((qcount >> 1) & 1) ^ 1, abort_flag, a.err);
+        if (!__shfl_sync(0xffffffffu, w, 0)) break;
+        if (lane == 0) {
+          qmeta[qs] = QMeta{qb, in_slice, kt};
+          mbar_arrive_expect_tx(&qfull[qs], C::kQBytes + qb.ntok * kHeads * 4);
+          tma_load_2d(smem + C::kOffQ + qs * C::kQBytes, &tmap_q, &qfull[qs], 0, qb.t0 * kHeads);
+          bulk_load(smem + C::kOffW + qs * C::kWBytes, a.w_folded + static_cast<int64_t>(qb.t0) * kHeads,
+                    qb.ntok * kHeads * 4, &qfull[qs]);
+        }
+        ++qcount;
       }
-      ++qcount;
       // page ids of this block, 32 at a time across the warp, one batch ahead
       const int npages = (qb.p0 + qb.ntok + kBlock - 1) / kBlock;
       const int32_t* bt_row = a.block_table + static_cast<int64_t>(qb.req) * a.bt_stride;
@@ -322,14 +337,15 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK, FP4>::kThreads, 1)
       int32_t cur_ids = p < npages ? __ldg(bt_row + p) : -1;
       int32_t nxt_ids = p + 32 < npages ? __ldg(bt_row + p + 32) : -1;
       for (int e = 0; e < in_slice; ++e, ++n, ++kt) {
-        if (n < npre) continue;  // loaded before the wait
+        if (n < npre || n % np != pi) continue;  // loaded before the wait, or another producer's
         const int stage = n % S;
+        int w = 1;
         if (lane == 0) w = mbar_wait(&empty[stage], ((n / S) & 1) ^ 1, abort_flag, a.err);
         if (!__shfl_sync(0xffffffffu, w, 0)) {
           ok = false;
           break;
         }
-        if (((2 * kt) >> 5) != batch) {  // moved into the next batch of 32 page ids
+        while (((2 * kt) >> 5) != batch) {  // moved on to a later batch of 32 page ids
           ++batch;
           cur_ids = nxt_ids;
           p = (batch + 1) * 32 + lane;
@@ -344,11 +360,13 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK, FP4>::kThreads, 1)
       if (ok && n < items) block_tiles = block_at(j, &qb, &first_new);
     }
     if (lane == 0 && *abort_flag) {
-      // let copies already issued land before the CTA's shared memory goes away
+      // let the copies this producer issued land before the CTA's shared memory goes away
       const unsigned long long deadline = global_ns() + kWaitLimitNs;
-      for (int m = (n > S ? n - S : 0); m < n; ++m) mbar_wait_until(&full[m % S], (m / S) & 1, deadline);
-      for (int m = n; m < npre; ++m) mbar_wait_until(&full[m % S], 0, deadline);
-      if (qcount > 0) mbar_wait_until(&qfull[(qcount - 1) & 1], ((qcount - 1) >> 1) & 1, deadline);
+      for (int m = (n > S ? n - S : 0); m < n; ++m)
+        if (m % np == pi) mbar_wait_until(&full[m % S], (m / S) & 1, deadline);
+      for (int m = n; m < npre; ++m)
+        if (m % np == pi) mbar_wait_until(&full[m % S], 0, deadline);
+      if (pi == 0 && qcount > 0) mbar_wait_until(&qfull[(qcount - 1) & 1], ((qcount - 1) >> 1) & 1, deadline);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -385,12 +403,12 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK, FP4>::kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int g = (warp - 2) >> 2;                     // warpgroup
+    const int g = (warp - C::kEpiWarp0) >> 2;          // warpgroup
     const int team = g / C::kTeamWG;                   // takes every kTeams-th tile
     const int tok0 = (g % C::kTeamWG) * C::kTokPerWG;  // the tokens of a tile this warpgroup reduces
     const int quarter = warp & 3;                      // TMEM lanes this warp may read
     const int row = quarter * 32 + lane;               // key within the tile
-    const int part = (warp - 2) & 3;                   // this warp's quarter of the group's histogram bins
+    const int part = (warp - C::kEpiWarp0) & 3;        // this warp's quarter of the group's histogram bins
     // decode rows: the warpgroup's histogram of the keys of its stored
     // scores, added to the row's global histogram when the group leaves the row
     uint32_t* ghist = reinterpret_cast<uint32_t*>(smem + C::kOffHist) + g * kHistBins;
