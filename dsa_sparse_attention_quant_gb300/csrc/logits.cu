@@ -58,9 +58,15 @@ struct LogitsCfg {
   // (8448-byte FP8 and 4352-byte FP4 pages alike), so a decode score stream
   // (two pages per tile and little else per tile) runs faster with two
   // issuers (decode8x128k step 54.4 -> 50.9 us; three or four measured the
-  // same as two). Warp 1 issues the MMAs; the epilogue warpgroups follow.
+  // same as two).
+  // MMA issuers: warp 1 and, for decode, warp 3; tile n is issued by MMA
+  // warp n % kMmaWarps into accumulator n % kAcc. A decode tile is only four
+  // small MMAs, and one thread's issue loop (waits, four MMAs, commit) took
+  // about 0.38 us per tile while the tensor pipe idled.
+  // The epilogue warpgroups follow.
   static constexpr int kProducers = NTOK == 1 ? 2 : 1;
-  static constexpr int kEpiWarp0 = 1 + kProducers;
+  static constexpr int kMmaWarps = NTOK == 1 ? 2 : 1;
+  static constexpr int kEpiWarp0 = kProducers + kMmaWarps;
   static constexpr int kThreads = 32 * kEpiWarp0 + 32 * kEpiWarps;
   static constexpr uint32_t kTmemCols = N * kAcc;         // 256 (decode) or 512 (prefill)
   static constexpr int kStageBytes = 17 * 1024;           // 2 x 8 KB K pages, 2 x 256 B scales, 1 KB aligned
@@ -83,6 +89,7 @@ struct LogitsCfg {
   static constexpr uint32_t kPageTx = (FP4 ? 4096 : 8192) + 256;          // TMA + scale bytes per page
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation must be a power of two");
+  static_assert(kAcc % kMmaWarps == 0, "each MMA warp owns every kMmaWarps-th accumulator");
 };
 
 __device__ __forceinline__ bool mbar_wait_until(uint64_t* bar, uint32_t parity, unsigned long long deadline) {
@@ -202,21 +209,24 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK, FP4>::kThreads, 1)
   int* scan = slice + 4;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool is_producer = warp == 0 || (warp >= 2 && warp < 1 + C::kProducers);
+  const bool is_mma = warp == 1 || (warp >= 1 + C::kProducers && warp < C::kEpiWarp0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1 + 4 * C::kTeamWG);  // MMA commit + the tile's epilogue warps (they read its scales)
+      // the tile's epilogue warps, after its MMAs completed (tfull) and they read its scales
+      mbar_init(&empty[s], 4 * C::kTeamWG);
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(&qfull[q], 1);
-      mbar_init(&qempty[q], 1 + C::kEpiWarps);
+      mbar_init(&qempty[q], C::kMmaWarps + C::kEpiWarps);
     }
     for (int c = 0; c < A; ++c) {
       mbar_init(&tfull[c], 1);
       mbar_init(&tempty[c], 4 * C::kTeamWG);
     }
-    mbar_init(done, 1);
+    mbar_init(done, C::kMmaWarps);
     for (int g = 0; g < C::kEpiWG; ++g) mbar_init(&wgbar[g], 4);
     *abort_flag = 0;
     fence_barrier_init();
@@ -254,7 +264,7 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK, FP4>::kThreads, 1)
   const int items = it_end - it_begin;  // tiles of this CTA (an empty slice runs no loop)
   pdl_launch_dependents();
   if constexpr (NTOK == 1) {
-    if (warp == 1 || warp >= C::kEpiWarp0) pdl_wait();  // the producers wait after their early loads
+    if (!is_producer) pdl_wait();  // the producers wait after their early loads
   }
 
   // Issue the loads of tile kt of a block (pages 2kt, 2kt+1) into a stage.
@@ -275,7 +285,7 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK, FP4>::kThreads, 1)
     }
   };
 
-  if (warp == 0 || (warp >= 2 && warp < C::kEpiWarp0)) {
+  if (is_producer) {
     // ------------------------------------------------------------ producers
     const int pi = warp == 0 ? 0 : warp - 1;  // this producer issues tiles n with n % np == pi
     constexpr int np = C::kProducers;
@@ -368,8 +378,9 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK, FP4>::kThreads, 1)
         if (m % np == pi) mbar_wait_until(&full[m % S], 0, deadline);
       if (pi == 0 && qcount > 0) mbar_wait_until(&qfull[(qcount - 1) & 1], ((qcount - 1) >> 1) & 1, deadline);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (is_mma) {
+    // ------------------------------------------------------------ MMA issuers
+    const int mi = warp == 1 ? 0 : warp - C::kProducers;  // issues tiles n with n % kMmaWarps == mi
     if (lane == 0) {
       int n = 0, qcount = 0;
       bool ok = true;
@@ -380,6 +391,7 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK, FP4>::kThreads, 1)
         const int in_slice = qmeta[qs].tiles;
         const uint32_t sb = smem_u32(smem + C::kOffQ + qs * C::kQBytes);
         for (int e = 0; e < in_slice; ++e, ++n) {
+          if (n % C::kMmaWarps != mi) continue;
           const int stage = n % S;
           const int acc = n % A;
           if (!mbar_wait(&full[stage], (n / S) & 1, abort_flag, a.err) ||
@@ -393,7 +405,6 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK, FP4>::kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             mma_f8(d, sw128_kmajor_desc(sa + 32 * k), sw128_kmajor_desc(sb + 32 * k), C::kIdesc, k > 0 ? 1u : 0u);
-          mma_commit(&empty[stage]);
           mma_commit(&tfull[acc]);
         }
         if (ok) mma_commit(&qempty[qs]);  // the block's q / w' buffer is free once its MMAs are done
