@@ -474,6 +474,13 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK, FP4>::kThreads, 1)
             const float4* wt = reinterpret_cast<const float4*>(wq + tok * kHeads);
             float v[kHeads];
             tmem_ld64_sync(tbase + tok * kHeads, v);
+            if (tt == C::kTokPerWG - 1) {
+              // the accumulator's last columns this warp reads are in registers:
+              // hand it back to the MMA before reducing them
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&tempty[acc]);
+            }
             // four chains (heads h mod 4), two per packed fma (one issue slot
             // for two chains' steps)
             uint64_t s01 = 0, s23 = 0;
@@ -491,11 +498,12 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK, FP4>::kThreads, 1)
                 if (use_hist) atomicAdd(&ghist[f32_key(score) >> kHistShift], 1u);
               }
             }
+          } else if (tt == C::kTokPerWG - 1) {  // a short block: nothing to read from the last columns
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[acc]);
       }
       if (!ok) break;
       __syncwarp();
