@@ -465,11 +465,23 @@ class LayerStack:
     ``k_cache`` and optionally ``k_new``. ``consumer(layer, producer, phys_ptr,
     valid_ptr)`` is called per layer. With ``rope_cos_sin`` ([max_pos, 64]
     fp32) and ``positions`` (int64 [T]), q and k_new arrive un-rotated and each
-    F layer rotates them (RoPE) on the way into the quantiser."""
+    F layer rotates them (RoPE) on the way into the quantiser.
+
+    ``graphed=True``: the first ``run()`` runs the stack and captures the same
+    call into a CUDA graph; later calls replay the graph on the given stream,
+    which saves the host work of each call (argument checks, tensor maps,
+    launches). The graph reads and writes the same buffers, so a step's new
+    inputs go into them before ``run()``; metadata that sizes the launch (the
+    batch's lengths) must not change. A graphed stack takes no consumer (a
+    host callback would run at capture only)."""
 
     def __init__(self, batch: Batch, fs: str, layers, topk: int, slot_mapping=None, topk_buf=None, phys_buf=None,
                  valid_buf=None, consumer=None, ws=None, softmax_scale: float = 0.0, block_stride_rows: int = 0,
-                 dev_err=None, positions=None, rope_cos_sin=None):
+                 dev_err=None, positions=None, rope_cos_sin=None, graphed: bool = False):
+        if graphed and consumer is not None:
+            raise DsaError("a graphed LayerStack takes no consumer: a host callback runs only at capture")
+        self._graphed = bool(graphed)
+        self._graph = None
         n = len(fs)
         self._arr = (DsaLayerInputsC * max(n, 1))()
         self._keep = [batch, slot_mapping, dev_err, positions, rope_cos_sin]
@@ -511,8 +523,22 @@ class LayerStack:
                       _ptr(dev_err))
 
     def run(self, stream=None):
-        st = self._fn(*self._args, _stream(stream))
+        s = stream if stream is not None else torch.cuda.current_stream()
+        if self._graph is not None:
+            with torch.cuda.stream(s):
+                self._graph.replay()
+            return self.topk_buf, self.phys_buf, self.valid_buf
+        st = self._fn(*self._args, ctypes.c_void_p(s.cuda_stream))
         _check(st, "dsa_layer_stack_run")
+        if self._graphed:  # capture the same call (the eager call above did any first-use set-up)
+            side = torch.cuda.Stream(device=s.device)
+            side.wait_stream(s)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                st = self._fn(*self._args, ctypes.c_void_p(side.cuda_stream))
+            s.wait_stream(side)
+            _check(st, "dsa_layer_stack_run (capture)")
+            self._graph = g
         return self.topk_buf, self.phys_buf, self.valid_buf
 
 

@@ -59,3 +59,40 @@ def test_captured_layer_run_replays_on_new_inputs():
     _, scores = oracle.indexer(second, ref_cache, rows=rows, with_scores=True)
     fails = compare.check_topk(stack.topk_buf.cpu().numpy(), scores, second.positions + 1, second.topk)
     assert not fails, f"top-k mismatches in {len(fails)} rows, first {fails[0]}"
+
+
+def test_graphed_layer_stack_first_call_then_replays():
+    """LayerStack(graphed=True): the first run() computes the step and captures
+    it; the next run() replays the capture on the buffers' new contents."""
+    shape = ([700, 3000, 1], [(400, 300)])
+    first = synth.make_batch(43, *shape, 128, table_seed=44)
+    second = synth.make_batch(45, *shape, 128, table_seed=44)
+    batch = dsa.Batch.from_host(first, DEV)
+    q, w, kn = bf16_tensor(first.q), torch.from_numpy(first.w).to(DEV), bf16_tensor(first.k_new)
+    slots = torch.from_numpy(first.slot_mapping).to(DEV)
+    ctx_slots = torch.from_numpy(first.ctx_slots).to(DEV)
+    cache = dsa.new_k_cache(first.num_blocks, device=DEV)
+    dsa.indexer_k_quant_write(bf16_tensor(first.ctx_k), ctx_slots, cache)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    stack = dsa.LayerStack(batch, "F", [dict(q=q, w=w, k_new=kn, k_cache=cache)], first.topk, slot_mapping=slots,
+                           dev_err=err, graphed=True)
+    for hb, refill in ((first, False), (second, True)):
+        if refill:
+            q.copy_(bf16_tensor(hb.q))
+            w.copy_(torch.from_numpy(hb.w).to(DEV))
+            kn.copy_(bf16_tensor(hb.k_new))
+            cache.zero_()
+            dsa.indexer_k_quant_write(bf16_tensor(hb.ctx_k), ctx_slots, cache)
+            stack.topk_buf.fill_(-7)
+        topk, phys, valid = stack.run()
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        ref_cache = oracle.fill_cache(hb)
+        assert np.array_equal(cache.cpu().numpy(), ref_cache)
+        _, scores = oracle.indexer(hb, ref_cache, rows=np.arange(hb.num_tokens), with_scores=True)
+        assert not compare.check_topk(topk.cpu().numpy(), scores, hb.positions + 1, hb.topk)
+        t = topk.cpu().numpy()
+        ph, _ = oracle.convert(t, hb.req_id_per_token, hb.block_table)
+        assert np.array_equal(phys.cpu().numpy(), ph)
+        assert np.array_equal(valid.cpu().numpy(), (t >= 0).sum(axis=1))
+    assert stack._graph is not None

@@ -169,3 +169,8 @@ def test_cache_format_of_an_empty_cache():
     assert binding.cache_format(torch.zeros((0, 4352), dtype=torch.uint8)) == 1
     with pytest.raises(binding.DsaError):
         binding.cache_format(torch.zeros(8448, dtype=torch.uint8))
+
+
+def test_graphed_layer_stack_refuses_a_consumer():
+    with pytest.raises(binding.DsaError, match="consumer"):
+        binding.LayerStack(None, "F", [None], 4, consumer=lambda *a: None, graphed=True)
