@@ -16,7 +16,7 @@
 //    persistent CTA takes one contiguous, equally sized slice of it, so the
 //    load is balanced to one tile whatever the mix of lengths.
 //  * Warp roles: warp 0 issues TMA (K pages, K scales, q block, w' block),
-//    with warp 2 sharing the K tiles in the decode instance; warp 1 issues
+//    with warp 2 sharing the K tiles; warp 1 (and warp 3 for decode) issues
 //    the MMAs; the remaining warps read TMEM and apply ReLU, the w'
 //    reduction and the K scale, and store fp32 scores.
 //  * Decode rows also get their score histogram (pass 1 of the top-k radix
@@ -52,19 +52,18 @@ struct LogitsCfg {
   static constexpr int kEpiWG = kTeams * kTeamWG;
   static constexpr int kTokPerWG = NTOK / kTeamWG;          // tokens of a tile one warpgroup reduces
   static constexpr int kEpiWarps = 4 * kEpiWG;
-  // K-tile producers: warp 0 (which also loads the q / w' blocks) and, for
-  // decode, warp 2. Tile n is issued by producer n % kProducers: one issuing
-  // thread sustained only about one page copy per 0.2 us whatever its size
-  // (8448-byte FP8 and 4352-byte FP4 pages alike), so a decode score stream
-  // (two pages per tile and little else per tile) runs faster with two
-  // issuers (decode8x128k step 54.4 -> 50.9 us; three or four measured the
-  // same as two).
+  // K-tile producers: warp 0 (which also loads the q / w' blocks) and warp 2.
+  // Tile n is issued by producer n % kProducers: one issuing thread sustained
+  // only about one page copy per 0.2 us whatever its size (8448-byte FP8 and
+  // 4352-byte FP4 pages alike), which capped the tile rate (decode8x128k step
+  // 54.4 -> 50.9 us with two issuers, prefill4x8k scores 1319 -> 1194 us;
+  // three or four measured the same as two on decode).
   // MMA issuers: warp 1 and, for decode, warp 3; tile n is issued by MMA
   // warp n % kMmaWarps into accumulator n % kAcc. A decode tile is only four
   // small MMAs, and one thread's issue loop (waits, four MMAs, commit) took
   // about 0.38 us per tile while the tensor pipe idled.
   // The epilogue warpgroups follow.
-  static constexpr int kProducers = NTOK == 1 ? 2 : 1;
+  static constexpr int kProducers = 2;
   static constexpr int kMmaWarps = NTOK == 1 ? 2 : 1;
   static constexpr int kEpiWarp0 = kProducers + kMmaWarps;
   static constexpr int kThreads = 32 * kEpiWarp0 + 32 * kEpiWarps;
