@@ -28,4 +28,4 @@ from .binding import (  # noqa: F401
     topk_logical_to_physical,
 )
 
-__version__ = "0.3.0"
+__version__ = "0.3.1"

@@ -123,7 +123,7 @@ def load(build_if_missing: bool = True):
             "dsa_indexer_plan": (ctypes.c_int, [BP, P, SZ, P, P]),
             "dsa_indexer_logits": (ctypes.c_int, [BP, P, P, P, P, I64, P, SZ, P, P]),
             "dsa_indexer_topk": (ctypes.c_int, [BP, P, I64, I32, P, P, SZ, P]),
-            "dsa_topk_logical_to_physical": (ctypes.c_int, [P, I64, I32, P, P, I64, I32, P, P, P, P]),
+            "dsa_topk_logical_to_physical": (ctypes.c_int, [P, I64, I32, P, P, I32, I64, I32, P, P, P, P]),
             "dsa_schedule_build": (ctypes.c_int, [I32, I32, I32, I32, ctypes.c_char_p, P, P]),
             "dsa_layer_stack_workspace_size": (SZ, [BP, I32]),
             "dsa_layer_stack_run": (ctypes.c_int, [ctypes.POINTER(DsaStackPlanC), BP, P, P, P, P, CONSUMER_FN, P, P,
@@ -419,7 +419,8 @@ def topk_logical_to_physical(logical, req_id_per_token, block_table, block_strid
     if valid_counts is None and with_valid_counts:
         valid_counts = torch.empty(T, dtype=torch.int32, device=logical.device)
     st = load().dsa_topk_logical_to_physical(_ptr(logical), int(T), int(k), _ptr(req_id_per_token),
-                                             _ptr(block_table), int(block_table.shape[1]), int(block_stride_rows),
+                                             _ptr(block_table), int(block_table.shape[0]),
+                                             int(block_table.shape[1]), int(block_stride_rows),
                                              _ptr(physical), _ptr(valid_counts), _ptr(dev_err), _stream(stream))
     _check(st, "dsa_topk_logical_to_physical")
     return physical, valid_counts

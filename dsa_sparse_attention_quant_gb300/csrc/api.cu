@@ -279,7 +279,7 @@ const char* dsa_status_string(int status) {
   }
 }
 
-int dsa_version(void) { return 300; }
+int dsa_version(void) { return 301; }
 
 int dsa_check_device_error(const int32_t* dev_err, uint32_t* out, dsa_stream_t stream) {
   if (dev_err == nullptr) return DSA_EINVAL;
@@ -461,10 +461,10 @@ int dsa_indexer_logits_topk(const DsaBatch* batch, const uint8_t* q_fp8, const f
 }
 
 int dsa_topk_logical_to_physical(const int32_t* logical, int64_t n_tokens, int32_t topk,
-                                 const int32_t* req_id_per_token, const int32_t* block_table, int64_t bt_stride,
-                                 int32_t block_stride_rows, int32_t* physical, int32_t* valid_counts,
-                                 int32_t* dev_err, dsa_stream_t stream) {
-  if (n_tokens < 0 || !topk_ok(topk) || bt_stride < 1) return DSA_EINVAL;
+                                 const int32_t* req_id_per_token, const int32_t* block_table, int32_t num_reqs,
+                                 int64_t bt_stride, int32_t block_stride_rows, int32_t* physical,
+                                 int32_t* valid_counts, int32_t* dev_err, dsa_stream_t stream) {
+  if (n_tokens < 0 || !topk_ok(topk) || bt_stride < 1 || num_reqs < 0) return DSA_EINVAL;
   if (n_tokens == 0) return DSA_OK;
   if (!logical || !req_id_per_token || !block_table || !physical || !aligned16(logical) || !aligned16(physical))
     return DSA_EINVAL;
@@ -473,7 +473,7 @@ int dsa_topk_logical_to_physical(const int32_t* logical, int64_t n_tokens, int32
   int st = device_sms(&sms);
   if (st != DSA_OK) return st;
   if (block_stride_rows <= 0) block_stride_rows = kBlock;
-  return from_cuda(launch_convert(logical, n_tokens, topk, req_id_per_token, block_table, bt_stride,
+  return from_cuda(launch_convert(logical, n_tokens, topk, req_id_per_token, block_table, num_reqs, bt_stride,
                                   block_stride_rows, physical, valid_counts, dev_err, stream));
 }
 

@@ -64,8 +64,8 @@ cudaError_t launch_q_quant_fold(const void* q, const float* w, int64_t n_tokens,
                                 uint8_t* q_fp8, float* q_scale, float* w_folded, const RopeArgs& rope,
                                 int32_t* err, cudaStream_t stream);
 cudaError_t launch_convert(const int32_t* logical, int64_t n_tokens, int topk, const int32_t* req_id,
-                           const int32_t* block_table, int64_t bt_stride, int stride_rows, int32_t* physical,
-                           int32_t* valid_counts, int32_t* err, cudaStream_t stream);
+                           const int32_t* block_table, int num_reqs, int64_t bt_stride, int stride_rows,
+                           int32_t* physical, int32_t* valid_counts, int32_t* err, cudaStream_t stream);
 
 struct PlanArgs {
   const int32_t* qsl;

@@ -67,12 +67,15 @@ __global__ void __launch_bounds__(256) q_quant_fold_kernel(const __nv_bfloat16* 
 // S5: one CTA per query row, each thread converts four ids per step.
 __global__ void __launch_bounds__(256) convert_kernel(const int32_t* __restrict__ logical, int64_t n_tokens,
                                                       int topk, const int32_t* __restrict__ req_id,
-                                                      const int32_t* __restrict__ block_table, int64_t bt_stride,
-                                                      int stride_rows, int32_t* __restrict__ physical,
+                                                      const int32_t* __restrict__ block_table, int num_reqs,
+                                                      int64_t bt_stride, int stride_rows,
+                                                      int32_t* __restrict__ physical,
                                                       int32_t* __restrict__ valid_counts, int32_t* err) {
   const int64_t t = blockIdx.x;
   if (t >= n_tokens) return;
-  const int32_t* bt_row = block_table + static_cast<int64_t>(__ldg(req_id + t)) * bt_stride;
+  const int r = __ldg(req_id + t);
+  const bool req_ok = r >= 0 && r < num_reqs;  // else every id of the row is flagged and left -1
+  const int32_t* bt_row = block_table + static_cast<int64_t>(req_ok ? r : 0) * bt_stride;
   const int4* in = reinterpret_cast<const int4*>(logical + t * topk);
   int4* out = reinterpret_cast<int4*>(physical + t * topk);
   int valid = 0;
@@ -86,7 +89,7 @@ __global__ void __launch_bounds__(256) convert_kernel(const int32_t* __restrict_
       int p = -1;
       if (id >= 0) {
         const int64_t page = id / kBlock;
-        const int32_t blk = page < bt_stride ? __ldg(bt_row + page) : -1;
+        const int32_t blk = req_ok && page < bt_stride ? __ldg(bt_row + page) : -1;
         if (blk >= 0) {
           p = blk * stride_rows + id % kBlock;
           ++valid;
@@ -141,12 +144,12 @@ cudaError_t launch_q_quant_fold(const void* q, const float* w, int64_t n_tokens,
 }
 
 cudaError_t launch_convert(const int32_t* logical, int64_t n_tokens, int topk, const int32_t* req_id,
-                           const int32_t* block_table, int64_t bt_stride, int stride_rows, int32_t* physical,
-                           int32_t* valid_counts, int32_t* err, cudaStream_t stream) {
+                           const int32_t* block_table, int num_reqs, int64_t bt_stride, int stride_rows,
+                           int32_t* physical, int32_t* valid_counts, int32_t* err, cudaStream_t stream) {
   if (n_tokens <= 0) return cudaSuccess;
   convert_kernel<<<static_cast<unsigned>(n_tokens), 256, 0, stream>>>(logical, n_tokens, topk, req_id,
-                                                                      block_table, bt_stride, stride_rows,
-                                                                      physical, valid_counts, err);
+                                                                      block_table, num_reqs, bt_stride,
+                                                                      stride_rows, physical, valid_counts, err);
   return cudaGetLastError();
 }
 

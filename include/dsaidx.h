@@ -282,15 +282,16 @@ DSA_API int dsa_indexer_logits_topk_static(const DsaBatch *batch, const uint8_t 
  * valid_counts[t] = number of ids >= 0 in row t.
  *   logical          device int32 [n_tokens, topk]
  *   req_id_per_token device int32 [n_tokens]
- *   block_table      device int32 [*, bt_stride]
+ *   block_table      device int32 [num_reqs, bt_stride]
  *   block_stride_rows  rows per physical block; <= 0 selects 64
  *   physical         device int32 [n_tokens, topk], written
  *   valid_counts     device int32 [n_tokens] or NULL, written
  * An id whose page lies past bt_stride, or a negative block entry, gives -1
- * and flags DSA_DEVERR_ID_RANGE. */
+ * and flags DSA_DEVERR_ID_RANGE; so does every id of a token whose request
+ * lies outside [0, num_reqs) (the block table is not read for it). */
 DSA_API int dsa_topk_logical_to_physical(const int32_t *logical, int64_t n_tokens, int32_t topk,
                                  const int32_t *req_id_per_token, const int32_t *block_table,
-                                 int64_t bt_stride, int32_t block_stride_rows,
+                                 int32_t num_reqs, int64_t bt_stride, int32_t block_stride_rows,
                                  int32_t *physical, int32_t *valid_counts,
                                  int32_t *dev_err, dsa_stream_t stream);
 

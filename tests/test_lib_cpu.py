@@ -28,7 +28,7 @@ def test_library_exports_every_declared_symbol():
     lib = binding.load()
     for name in declared_symbols():
         assert hasattr(lib, name), name
-    assert lib.dsa_version() == 300
+    assert lib.dsa_version() == 301
     assert lib.dsa_status_string(0) == b"ok"
     assert b"invalid" in lib.dsa_status_string(1)
 
@@ -65,10 +65,12 @@ def test_host_validation_without_gpu():
     # negative token count, bad row stride, bad top-k: rejected on the host
     assert lib.dsa_indexer_k_quant_write(P(16), -1, 128, P(16), P(16), 1, None, None) == binding.DSA_EINVAL
     assert lib.dsa_indexer_k_quant_write(P(16), 4, 100, P(16), P(16), 1, None, None) == binding.DSA_EINVAL
-    assert lib.dsa_topk_logical_to_physical(P(16), 4, 6, P(16), P(16), 1, 0, P(16), None, None,
+    assert lib.dsa_topk_logical_to_physical(P(16), 4, 6, P(16), P(16), 1, 1, 0, P(16), None, None,
                                             None) == binding.DSA_EINVAL
-    assert lib.dsa_topk_logical_to_physical(P(16), 4, 8192, P(16), P(16), 1, 0, P(16), None, None,
+    assert lib.dsa_topk_logical_to_physical(P(16), 4, 8192, P(16), P(16), 1, 1, 0, P(16), None, None,
                                             None) == binding.DSA_EINVAL
+    assert lib.dsa_topk_logical_to_physical(P(16), 4, 64, P(16), P(16), -1, 1, 0, P(16), None, None,
+                                            None) == binding.DSA_EINVAL  # negative request count
     b = binding.DsaBatchC(1, 2, 1, 1, 10, 1, 1, 16, 16, 16, 16)  # num_decodes > num_reqs
     assert lib.dsa_indexer_workspace_size(ctypes.byref(b), 64) == 0
     # empty batches are no-ops that succeed without a device
