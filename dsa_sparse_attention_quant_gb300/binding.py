@@ -40,7 +40,7 @@ SYMBOLS = [
     "dsa_layer_stack_workspace_size", "dsa_layer_stack_run",
     "dsa_indexer_logits_topk_static", "dsa_set_launch_events",
     "dsa_indexer_k_rope_quant_write", "dsa_indexer_q_rope_quant_fold", "dsa_gather_rows",
-    "dsa_indexer_k_quant_write_fp4",
+    "dsa_indexer_k_quant_write_fp4", "dsa_selftest_wait_timeout",
 ]
 STATIC_WORKSPACE_BYTES = 32 << 20
 
@@ -132,6 +132,7 @@ def load(build_if_missing: bool = True):
             "dsa_set_launch_events": (ctypes.c_int, [P, I32]),
             "dsa_indexer_k_rope_quant_write": (ctypes.c_int, [P, I64, I64, P, P, I64, P, P, I64, P, P]),
             "dsa_indexer_k_quant_write_fp4": (ctypes.c_int, [P, I64, I64, P, P, I64, P, P, I64, P, P]),
+            "dsa_selftest_wait_timeout": (ctypes.c_int, [P, P]),
             "dsa_indexer_q_rope_quant_fold": (ctypes.c_int, [P, P, I64, P, P, I64, F32, P, P, P, P, P]),
             "dsa_gather_rows": (ctypes.c_int, [P, I64, I64, I64, P, I64, I32, P, P, P]),
         }
@@ -206,6 +207,13 @@ class Batch:
         return cls(d(hb.query_start_loc), d(hb.seq_lens), d(hb.block_table), d(hb.req_id_per_token),
                    hb.num_decodes, hb.num_blocks, int(hb.seq_lens.max()) if hb.num_reqs else 1,
                    int(hb.query_start_loc[hb.num_decodes]) if hb.num_reqs else 0)
+
+
+def selftest_wait_timeout(dev_err, stream=None):
+    """Diagnostic: a bounded pipeline wait on a barrier nothing completes; after
+    about 1 s it sets DSA_DEVERR_TIMEOUT (8) in ``dev_err`` and returns."""
+    _need(dev_err, torch.int32, "dev_err")
+    _check(load().dsa_selftest_wait_timeout(_ptr(dev_err), _stream(stream)), "dsa_selftest_wait_timeout")
 
 
 # ---------------------------------------------------------------- K caches

@@ -281,6 +281,14 @@ const char* dsa_status_string(int status) {
 
 int dsa_version(void) { return 301; }
 
+int dsa_selftest_wait_timeout(int32_t* dev_err, dsa_stream_t stream) {
+  if (dev_err == nullptr || reinterpret_cast<uintptr_t>(dev_err) % 4 != 0) return DSA_EINVAL;
+  int sms;
+  int st = device_sms(&sms);
+  if (st != DSA_OK) return st;
+  return from_cuda(launch_wait_selftest(dev_err, stream));
+}
+
 int dsa_check_device_error(const int32_t* dev_err, uint32_t* out, dsa_stream_t stream) {
   if (dev_err == nullptr) return DSA_EINVAL;
   uint32_t v = 0;

@@ -56,6 +56,9 @@ struct SegmentPlan {
   int32_t max_qb;       // capacity of qb / tile_start
 };
 
+// One bounded pipeline wait that runs out (see dsa_selftest_wait_timeout).
+cudaError_t launch_wait_selftest(int32_t* err, cudaStream_t stream);
+
 // fp4: the cache has FP4 pages (E2M1 codes) instead of FP8 pages.
 cudaError_t launch_k_quant_write(const void* k, int64_t n, int64_t row_stride, const int64_t* slot_mapping,
                                  uint8_t* cache, int64_t num_blocks, bool fp4, const RopeArgs& rope, int32_t* err,

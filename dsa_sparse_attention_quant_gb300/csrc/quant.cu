@@ -143,6 +143,24 @@ cudaError_t launch_q_quant_fold(const void* q, const float* w, int64_t n_tokens,
   return cudaGetLastError();
 }
 
+// The failure path of a pipeline wait: an mbarrier that nothing completes,
+// waited on with the bounded wait of the pipelines; after the limit the wait
+// flags DSA_DEVERR_TIMEOUT and the kernel returns.
+__global__ void wait_selftest_kernel(int32_t* err) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  mbar_init(&bar, 1);
+  fence_barrier_init();
+  mbar_wait(&bar, 0, &abort_flag, err);  // no arrival: gives up after kWaitLimitNs
+}
+
+cudaError_t launch_wait_selftest(int32_t* err, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(err);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_convert(const int32_t* logical, int64_t n_tokens, int topk, const int32_t* req_id,
                            const int32_t* block_table, int num_reqs, int64_t bt_stride, int stride_rows,
                            int32_t* physical, int32_t* valid_counts, int32_t* err, cudaStream_t stream) {

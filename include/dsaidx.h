@@ -88,6 +88,13 @@ DSA_API int dsa_version(void); /* major*10000 + minor*100 + patch */
  * DSA_EDEVICE if it is nonzero, DSA_OK otherwise. */
 DSA_API int dsa_check_device_error(const int32_t *dev_err, uint32_t *out, dsa_stream_t stream);
 
+/* Diagnostic, not part of the indexer: one thread waits, with the bounded
+ * wait every pipeline of this library uses, on an mbarrier that nothing
+ * completes. After about 1 s the wait gives up, ORs DSA_DEVERR_TIMEOUT into
+ * *dev_err (device int32) and the kernel returns; the context stays usable.
+ * It shows the failure path of the pipelines without a hang or a fault. */
+DSA_API int dsa_selftest_wait_timeout(int32_t *dev_err, dsa_stream_t stream);
+
 /* ------------------------------------------------------------ the batch */
 /* One step's attention metadata, after [IC] `DeepseekV32IndexerMetadata`
  * (seq_lens, slot_mapping, num_decodes, ...) and the decode-first ordering of

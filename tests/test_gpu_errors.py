@@ -58,3 +58,18 @@ def test_conversion_of_unmappable_ids_is_flagged():
                      [-1, -1, -1, -1]], np.int32)
     assert np.array_equal(phys.cpu().numpy(), want)
     assert valid.cpu().tolist() == [2, 2, 0, 0]
+
+
+def test_a_pipeline_wait_that_runs_out_reports_a_timeout():
+    """The bounded wait every pipeline uses, on a barrier nothing completes:
+    the kernel gives up after about a second, sets the timeout bit and
+    returns; the context keeps working (a normal batch after it is correct)."""
+    import time
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    t0 = time.perf_counter()
+    dsa.binding.selftest_wait_timeout(err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 8  # DSA_DEVERR_TIMEOUT
+    assert 0.5 < time.perf_counter() - t0 < 30.0
+    from tests.test_gpu_parity import check_batch
+    check_batch(synth.make_batch(63, [300, 90], [(200, 40)], 32))
