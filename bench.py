@@ -342,9 +342,15 @@ def run_ours(args):
         # uploads its inputs (q, w, new K, slots, the batch metadata, positions
         # with --rope) packed in one pinned buffer with one copy, runs the layer
         # runner (a prepared dsa.LayerStack on views of that upload), and reads
-        # the physical ids and valid counts back with one copy. (Replaying the
-        # call from a CUDA graph, LayerStack(graphed=True), measured slower here:
-        # 57.4 against 49.5 us per decode32 step.)
+        # the physical ids and valid counts back with one copy. Consecutive
+        # steps alternate between two streams, each with its own workspace and
+        # output buffers (and their inputs are different replicas): a step's
+        # upload overlaps the previous step's kernels and its read-back, while
+        # its kernels still start only after the previous step's kernels (an
+        # event), so the device work per step is that of `value`. The host
+        # waits for step i's result before it enqueues step i + 2. (Replaying
+        # the call from a CUDA graph, LayerStack(graphed=True), measured slower:
+        # 57.4 against 49.5 us per serial decode32 step.)
         parts = [("q", hb.q), ("w", hb.w), ("k_new", hb.k_new), ("slots", hb.slot_mapping),
                  ("qsl", hb.query_start_loc.astype(np.int32)), ("seq", hb.seq_lens.astype(np.int32)),
                  ("bt", hb.block_table.astype(np.int32)), ("req", hb.req_id_per_token.astype(np.int32))]
@@ -365,11 +371,17 @@ def run_ours(args):
             o, arr = offs[name]
             return buf[o:o + arr.nbytes].view(dtype).view(shape)
 
-        stacks, dev_in = [], []
-        dev_out = torch.empty(max(out_bytes, 256), dtype=torch.uint8, device=dev)
-        phys_e = dev_out[:T * k * 4].view(torch.int32).view(T, k)
+        lanes = 2 if n_rep >= 2 else 1
         voff = (T * k * 4 + 255) // 256 * 256
-        valid_e = dev_out[voff:voff + T * 4].view(torch.int32)
+        lane_bufs = []  # per stream: workspace, logical ids, packed device output, pinned host output
+        for ln in range(lanes):
+            dev_out = torch.empty(max(out_bytes, 256), dtype=torch.uint8, device=dev)
+            lane_bufs.append(dict(
+                ws=ws if ln == 0 else torch.empty_like(ws), topk=topk if ln == 0 else torch.empty_like(topk),
+                dev_out=dev_out, phys=dev_out[:T * k * 4].view(torch.int32).view(T, k),
+                valid=dev_out[voff:voff + T * 4].view(torch.int32),
+                host_out=host_out if ln == 0 else torch.empty_like(host_out).pin_memory()))
+        stacks, dev_in = [[] for _ in range(lanes)], []
         for r in reps:
             d = torch.empty(max(total, 256), dtype=torch.uint8, device=dev)
             d.copy_(host_in)
@@ -378,28 +390,47 @@ def run_ours(args):
                            hb.num_decodes, hb.num_blocks, batch.max_seq_len, batch.num_decode_tokens)
             le = [dict(q=view(d, "q", torch.bfloat16, (T, 64, 128)), w=view(d, "w", torch.float32, (T, 64)),
                        k_new=view(d, "k_new", torch.bfloat16, (T, 128)), k_cache=r.k_cache)]
-            stacks.append(dsa.LayerStack(be, fs, le, k, slot_mapping=view(d, "slots", torch.int64, (-1,)),
-                                         topk_buf=topk, phys_buf=phys_e, valid_buf=valid_e, ws=ws, dev_err=err,
-                                         positions=view(d, "pos", torch.int64, (-1,)) if args.rope else None,
-                                         rope_cos_sin=rope_cs))
+            for ln, lb in enumerate(lane_bufs):
+                stacks[ln].append(dsa.LayerStack(be, fs, le, k, slot_mapping=view(d, "slots", torch.int64, (-1,)),
+                                                 topk_buf=lb["topk"], phys_buf=lb["phys"], valid_buf=lb["valid"],
+                                                 ws=lb["ws"], dev_err=err,
+                                                 positions=view(d, "pos", torch.int64, (-1,)) if args.rope else None,
+                                                 rope_cos_sin=rope_cs))
             dev_in.append(d)
         h2d, d2h = host_in.numel(), host_out.numel()  # the bytes each step copies
-        cur = torch.cuda.current_stream()
+        streams = [torch.cuda.current_stream()] + [torch.cuda.Stream() for _ in range(lanes - 1)]
+        kernels_done = [torch.cuda.Event() for _ in range(lanes)]
+        started = [False]
 
         def e2e_step(i):
-            j = i % n_rep
-            dev_in[j].copy_(host_in, non_blocking=True)
-            stacks[j].run(cur)
-            host_out.copy_(dev_out, non_blocking=True)
-            cur.synchronize()
+            ln, j = i % lanes, i % n_rep
+            st, lb = streams[ln], lane_bufs[ln]
+            with torch.cuda.stream(st):
+                dev_in[j].copy_(host_in, non_blocking=True)
+                if started[0]:
+                    st.wait_event(kernels_done[(i - 1) % lanes])  # one step's kernels at a time
+                stacks[ln][j].run(st)
+                kernels_done[ln].record(st)
+                started[0] = True
+                lb["host_out"].copy_(lb["dev_out"], non_blocking=True)
+            if lanes == 1:
+                st.synchronize()
+            elif i > 0:
+                streams[(i - 1) % lanes].synchronize()  # step i - 1's result is on the host
+
+        def e2e_drain(last):
+            streams[last % lanes].synchronize()
 
         for i in range(args.warmup):
             e2e_step(i)
+        e2e_drain(args.warmup - 1)
+        torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         e0 = time.perf_counter()
         for i in range(args.steps):
             e2e_step(i)
+        e2e_drain(args.steps - 1)
         e1 = time.perf_counter()
         e2e_s = e1 - e0
         e2e_s = max_over_ranks(e2e_s, dev)
@@ -479,8 +510,11 @@ def run_ours(args):
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
             "ms_per_step": e2e_s / args.steps * 1e3,
-            "path": "pinned host -> device (one copy), LayerStack.run (one C call, three launches), "
-                    "device -> pinned host (one copy), stream synchronize",
+            "path": "per step: pinned host -> device (one copy), LayerStack.run (one C call, three launches), "
+                    "device -> pinned host (one copy); steps alternate between two streams with their own "
+                    "buffers so that copies overlap the neighbouring steps' kernels, kernels of consecutive steps "
+                    "ordered by an event; the host waits for each step's result one step later and for the last "
+                    "at the end",
         },
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
