@@ -72,6 +72,9 @@ class DsaLayerInputsC(ctypes.Structure):
         ("w", ctypes.c_void_p),
         ("k_new", ctypes.c_void_p),
         ("k_cache", ctypes.c_void_p),
+        ("k_row_stride", ctypes.c_int64),
+        ("w_row_stride", ctypes.c_int64),
+        ("w_dtype", ctypes.c_int32),
     ]
 
 
@@ -466,6 +469,21 @@ def layer_stack_workspace_size(batch: Batch, topk: int) -> int:
     return int(load().dsa_layer_stack_workspace_size(ctypes.byref(batch.c), int(topk)))
 
 
+def _layer_inputs(L) -> DsaLayerInputsC:
+    """The C inputs of an F layer. ``w`` may be fp32 or bf16 and ``w`` and
+    ``k_new`` may be row-strided 2-D views (unit inner stride), e.g. the column
+    views ``kw[:, :128]`` and ``kw[:, 128:]`` of one fused projection output."""
+    q, w, kn = L["q"], L["w"], L.get("k_new")
+    _need(q, torch.bfloat16, "q")
+    if w.dtype not in (torch.float32, torch.bfloat16) or not w.is_cuda or w.dim() != 2 or w.stride(1) != 1:
+        raise DsaError("w must be a CUDA fp32 or bf16 [T, 64] tensor with unit inner stride")
+    if kn is not None and (kn.dtype != torch.bfloat16 or not kn.is_cuda or kn.dim() != 2 or kn.stride(1) != 1):
+        raise DsaError("k_new must be a CUDA bf16 [T, 128] tensor with unit inner stride")
+    return DsaLayerInputsC(q.data_ptr(), w.data_ptr(), kn.data_ptr() if kn is not None else None,
+                           L["k_cache"].data_ptr(), int(kn.stride(0)) if kn is not None else 0, int(w.stride(0)),
+                           1 if w.dtype == torch.bfloat16 else 0)
+
+
 class LayerStack:
     """A prepared ``dsa_layer_stack_run``: the C plan, the per-layer input table,
     the output buffers and the workspace are built once; ``run()`` issues the
@@ -503,9 +521,7 @@ class LayerStack:
             if L is None:
                 continue
             self._keep.append(L)
-            self._arr[l] = DsaLayerInputsC(L["q"].data_ptr(), L["w"].data_ptr(),
-                                           L["k_new"].data_ptr() if L.get("k_new") is not None else None,
-                                           L["k_cache"].data_ptr())
+            self._arr[l] = _layer_inputs(L)
         max_pos = 0
         if rope_cos_sin is not None:
             max_pos = _rope_table(rope_cos_sin)

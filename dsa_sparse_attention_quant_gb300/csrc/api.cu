@@ -14,6 +14,23 @@
 using namespace dsa;
 
 namespace {
+std::mutex g_attr_mutex;
+}  // namespace
+
+cudaError_t dsa::raise_smem_limit(const void* func, int bytes, uint64_t* done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const uint64_t bit = uint64_t{1} << dev;
+  std::lock_guard<std::mutex> lock(g_attr_mutex);
+  if (*done & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) *done |= bit;
+  return e;
+}
+
+namespace {
 
 constexpr int kMaxDevices = 64;
 
@@ -186,6 +203,8 @@ PrologueArgs plan_only(const DsaBatch* b, const IndexerWs& ws, int sms, const vo
                        const int64_t* slot_mapping, uint8_t* k_cache, int32_t* dev_err) {
   PrologueArgs pa{};
   pa.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  pa.k_row_stride = kDim;
+  pa.w_row_stride = kHeads;
   pa.slot_mapping = slot_mapping;
   pa.k_cache = k_cache;
   pa.num_blocks = b->num_blocks;
@@ -544,6 +563,11 @@ int dsa_layer_stack_run(const DsaStackPlan* plan, const DsaBatch* batch, const i
       const DsaLayerInputs& L = plan->layers[l];
       if (!L.q || !L.w || !L.k_cache || !aligned16(L.q) || !kcache_aligned(batch, L.k_cache)) return DSA_EINVAL;
       if (L.k_new != nullptr && (slot_mapping == nullptr || !aligned16(L.k_new))) return DSA_EINVAL;
+      if (L.w_dtype != DSA_W_FP32 && L.w_dtype != DSA_W_BF16) return DSA_EINVAL;
+      const int64_t ks = L.k_row_stride > 0 ? L.k_row_stride : kDim;
+      const int64_t wst = L.w_row_stride > 0 ? L.w_row_stride : kHeads;
+      if (L.k_row_stride < 0 || ks < kDim || ks % 8 != 0 || L.w_row_stride < 0 || wst < kHeads) return DSA_EINVAL;
+      if (reinterpret_cast<uintptr_t>(L.w) % (L.w_dtype == DSA_W_BF16 ? 2 : 4) != 0) return DSA_EINVAL;
     }
   }
   if (batch->num_tokens > 0 && (!topk_buf || !phys_buf || !ws || !aligned16(ws))) return DSA_EINVAL;
@@ -571,6 +595,9 @@ int dsa_layer_stack_run(const DsaStackPlan* plan, const DsaBatch* batch, const i
         PrologueArgs pa = plan_only(batch, w, sms, L.k_new, slot_mapping, L.k_cache, dev_err);
         pa.q = static_cast<const __nv_bfloat16*>(L.q);
         pa.w = L.w;
+        pa.w_bf16 = L.w_dtype == DSA_W_BF16;
+        pa.w_row_stride = L.w_row_stride > 0 ? L.w_row_stride : kHeads;
+        pa.k_row_stride = L.k_row_stride > 0 ? L.k_row_stride : kDim;
         pa.softmax_scale = softmax_scale;
         pa.rope = RopeArgs{plan->positions, plan->rope_cos_sin, plan->rope_max_pos};
         pa.q_fp8 = q8;

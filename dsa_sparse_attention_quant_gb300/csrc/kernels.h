@@ -56,6 +56,11 @@ struct SegmentPlan {
   int32_t max_qb;       // capacity of qb / tile_start
 };
 
+// Raises func's dynamic shared-memory limit to `bytes` on the current device.
+// The attribute is held per device, so it is set once per device: *done has
+// one bit per device ordinal (below 64), read and updated under a lock.
+cudaError_t raise_smem_limit(const void* func, int bytes, uint64_t* done);
+
 // One bounded pipeline wait that runs out (see dsa_selftest_wait_timeout).
 cudaError_t launch_wait_selftest(int32_t* err, cudaStream_t stream);
 
@@ -85,11 +90,14 @@ struct PlanArgs {
 // with the weight fold, and (when `plan`) the work plan.
 struct PrologueArgs {
   const __nv_bfloat16* q;   // [T, 64, 128]
-  const float* w;           // [T, 64]
+  const void* w;            // [T, w_row_stride]: fp32, or bf16 when w_bf16; the first 64 used
+  int64_t w_row_stride;     // elements between the rows of w
+  bool w_bf16;
   float softmax_scale;
   uint8_t* q_fp8;           // [T, 64, 128]
   float* w_folded;          // [T, 64]
-  const __nv_bfloat16* k_new;     // [T, 128] or nullptr
+  const __nv_bfloat16* k_new;     // [T, k_row_stride] (first 128 used) or nullptr
+  int64_t k_row_stride;           // elements between the rows of k_new
   const int64_t* slot_mapping;    // [T]
   uint8_t* k_cache;
   int64_t num_blocks;

@@ -538,13 +538,10 @@ template <int NTOK, bool FP4>
 static cudaError_t launch_logits_t(const CUtensorMap* tmap_k, const CUtensorMap* tmap_q, SegmentPlan plan,
                                    const LogitsArgs& a, int num_sms, cudaStream_t stream) {
   using C = LogitsCfg<NTOK, FP4>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(logits_kernel<NTOK, FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static uint64_t configured = 0;  // devices whose limit is raised
+  cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(logits_kernel<NTOK, FP4>), C::kSmemBytes,
+                                   &configured);
+  if (e != cudaSuccess) return e;
   return launch_pdl(logits_kernel<NTOK, FP4>, dim3(num_sms), dim3(C::kThreads), C::kSmemBytes, stream, *tmap_k,
                     *tmap_q, plan, a);
 }

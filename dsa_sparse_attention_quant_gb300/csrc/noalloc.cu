@@ -14,6 +14,7 @@
 // the score histograms and top-k counters before the later kernels read them.
 // Calls whose kernels overlap on the GPU (two streams, or two host threads)
 // race on the array; serialise them.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -31,22 +32,55 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
 
 std::mutex g_static_mutex;
-void* g_static_addr[kMaxDevices];  // device address of the array, per device
+void* g_static_addr[kMaxDevices];                  // device address of the array, per device
+unsigned long long g_static_ctx[kMaxDevices];      // id of the context the address belongs to
 
-// Look up (once per device, with that device current) the device address of
-// the array.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+// The process-unique id of the current context (the driver never reuses one),
+// or false when there is none yet. Called under g_static_mutex.
+bool current_context_id(unsigned long long* id) {
+  if (g_ctx_get_current == nullptr || g_ctx_get_id == nullptr) {
+    void* a = nullptr;
+    void* b = nullptr;
+    cudaDriverEntryPointQueryResult qa, qb;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 4000, cudaEnableDefault, &qa) != cudaSuccess ||
+        qa != cudaDriverEntryPointSuccess || a == nullptr ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) != cudaSuccess ||
+        qb != cudaDriverEntryPointSuccess || b == nullptr)
+      return false;
+    g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(a);
+    g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(b);
+  }
+  CUcontext ctx = nullptr;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return g_ctx_get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// The device address of the array in the current device's context. It is
+// looked up (cudaGetSymbolAddress, with that device current) on the first
+// call on a device, and again whenever the device's context has changed since
+// (after cudaDeviceReset the array lives at a new address in a new context).
 int static_workspace(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DSA_ENODEV;
   std::lock_guard<std::mutex> lock(g_static_mutex);
-  if (g_static_addr[dev] == nullptr) {
+  unsigned long long ctx = 0;
+  const bool have_ctx = current_context_id(&ctx);
+  if (g_static_addr[dev] == nullptr || !have_ctx || g_static_ctx[dev] != ctx) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_static_workspace);
     if (e != cudaSuccess || p == nullptr) {
       (void)cudaGetLastError();
       return e == cudaErrorNoKernelImageForDevice ? DSA_ENODEV : DSA_ECUDA;
     }
+    // the lookup made the device's context current if it was not yet
+    if (!current_context_id(&ctx)) return DSA_ECUDA;
     g_static_addr[dev] = p;
+    g_static_ctx[dev] = ctx;
   }
   *out = g_static_addr[dev];
   return DSA_OK;

@@ -175,7 +175,12 @@ __global__ void __launch_bounds__(kPrologueThreads, 6) prologue_kernel(PrologueA
       for (int u = 0; u < kGroup; ++u) {
         const int64_t r = r0 + u;
         raw[u] = r < q_rows ? __ldg(reinterpret_cast<const uint2*>(a.q + r * kDim) + lane) : make_uint2(0, 0);
-        wv[u] = (lane == 0 && r < q_rows) ? __ldg(a.w + r) : 0.0f;
+        wv[u] = 0.0f;
+        if (lane == 0 && r < q_rows) {  // w[token][head]: row r is head r % 64 of token r / 64
+          const int64_t wi = (r / kHeads) * a.w_row_stride + (r % kHeads);
+          wv[u] = a.w_bf16 ? __bfloat162float(__ldg(static_cast<const __nv_bfloat16*>(a.w) + wi))
+                           : __ldg(static_cast<const float*>(a.w) + wi);
+        }
       }
       if (a.rope.cos_sin != nullptr) {  // the group's rows are heads of one token (64 % kGroup == 0)
         const float* cs = rope_row(a.rope, r0 / kHeads, a.err, lane);
@@ -201,7 +206,7 @@ __global__ void __launch_bounds__(kPrologueThreads, 6) prologue_kernel(PrologueA
         if (lane == 0) flag_error(a.err, DSA_DEVERR_SLOT_RANGE);
         continue;
       }
-      uint2 raw = __ldg(reinterpret_cast<const uint2*>(a.k_new + t * kDim) + lane);
+      uint2 raw = __ldg(reinterpret_cast<const uint2*>(a.k_new + t * a.k_row_stride) + lane);
       if (a.rope.cos_sin != nullptr) {
         const float* cs = rope_row(a.rope, t, a.err, lane);
         if (cs != nullptr) raw = rope_row_lane(raw, cs);

@@ -169,25 +169,19 @@ cudaError_t launch_topk(const float* logits, int64_t ld, const int32_t* qsl, con
   if (ld <= kTopkRowCap) {
     const int cap = kStagedCandCap;
     const int smem = (kSelBins + 2 * cap + ids + static_cast<int>((ld + 3) & ~3)) * 4;
-    static bool configured = false;
-    if (!configured) {  // the largest layout: k = kMaxTopk, ld = kTopkRowCap
-      cudaError_t e = cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (kSelBins + 2 * kStagedCandCap + kMaxTopk + kTopkRowCap) * 4);
-      if (e != cudaSuccess) return e;
-      configured = true;
-    }
+    static uint64_t configured = 0;  // the largest layout: k = kMaxTopk, ld = kTopkRowCap
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(topk_kernel<true>),
+                                     (kSelBins + 2 * kStagedCandCap + kMaxTopk + kTopkRowCap) * 4, &configured);
+    if (e != cudaSuccess) return e;
     return launch_pdl(topk_kernel<true>, dim3(rows), dim3(kRowThreads), smem, stream, logits, ld, qsl, seq_lens,
                       req_id, num_reqs, row_begin, topk, out, po, hist, hist_rows, cap);
   } else {
     const int cap = kCandCap;
     const int smem = (kSelBins + 2 * cap + ids) * 4;
-    static bool configured = false;
-    if (!configured) {
-      cudaError_t e = cudaFuncSetAttribute(topk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (kSelBins + 2 * kCandCap + kMaxTopk) * 4);
-      if (e != cudaSuccess) return e;
-      configured = true;
-    }
+    static uint64_t configured = 0;
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(topk_kernel<false>),
+                                     (kSelBins + 2 * kCandCap + kMaxTopk) * 4, &configured);
+    if (e != cudaSuccess) return e;
     return launch_pdl(topk_kernel<false>, dim3(rows), dim3(kRowThreads), smem, stream, logits, ld, qsl, seq_lens,
                       req_id, num_reqs, row_begin, topk, out, po, hist, hist_rows, cap);
   }
@@ -353,12 +347,9 @@ cudaError_t launch_select(const SelectArgs& a, const TopkPhys* phys, int num_sms
   int chunk = 1024;
   while (chunk < 8192 && static_cast<int64_t>(a.n_rows) * a.ld / chunk > 2 * static_cast<int64_t>(num_sms)) chunk *= 2;
   const int max_smem = (kSelBins + 2 * 8192) * 4;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static uint64_t configured = 0;
+  cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(select_kernel), max_smem, &configured);
+  if (e != cudaSuccess) return e;
   const int64_t chunks = (a.ld + chunk - 1) / chunk;
   dim3 grid(static_cast<unsigned>(chunks < 1 ? 1 : chunks), static_cast<unsigned>(a.n_rows));
   return launch_pdl(select_kernel, grid, dim3(kSelectThreads), (kSelBins + 2 * chunk) * 4, stream, a, phys_out(phys),

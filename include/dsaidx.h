@@ -139,7 +139,7 @@ DSA_API int dsa_indexer_k_quant_write(const void *k, int64_t n_tokens, int64_t k
                               const int64_t *slot_mapping, uint8_t *k_cache,
                               int64_t num_blocks, int32_t *dev_err, dsa_stream_t stream);
 
-/* ---------------------------------- the FP4 indexer K cache (next row) */
+/* ------------------------------------------------ the FP4 indexer K cache */
 /* [IC] hands `sparse_attn_indexer` a `use_fp4_cache` flag beside
  * `quant_block_size` and `scale_fmt`; the pages give no more of the format.
  * Reading taken: the element is E2M1 (OCP Microscaling Formats (MX)
@@ -161,7 +161,7 @@ DSA_API int dsa_indexer_k_quant_write_fp4(const void *k, int64_t n_tokens, int64
                                   const int64_t *slot_mapping, uint8_t *k_cache,
                                   int64_t num_blocks, int32_t *dev_err, dsa_stream_t stream);
 
-/* ------------------------------- RoPE fused into S1 and S2a (next row) */
+/* ------------------------------------------ RoPE fused into S1 and S2a */
 /* [IC] `Indexer.forward` rotates the leading qk_rope_head_dim = 64 dims of
  * every q head and of the shared K row, `rotary_emb(positions, q_pe, k_pe)`,
  * before the quantisation. These calls take un-rotated bf16 rows and rotate
@@ -272,6 +272,9 @@ DSA_API int dsa_set_launch_events(void *const *events, int32_t n_events);
  *    8K: their score rows, histograms and boundary candidates).
  *  - The first call on a device looks up the array's device address (with
  *    that device current); make that first call before any stream capture.
+ *    The address belongs to the device's context: when that context has
+ *    changed since (after cudaDeviceReset), the next call looks it up again,
+ *    so that call too must come before any capture.
  *  - All calls share the array and it keeps the last call's contents; each
  *    call's first kernel writes the plan and clears the histograms and
  *    counters that must start at zero. Calls whose kernels overlap on the GPU —
@@ -317,7 +320,7 @@ DSA_API int dsa_schedule_build(int32_t n_layers, int32_t use_index_cache, int32_
                        int32_t offset, const char *pattern, char *fs_out,
                        int32_t *producer_out);
 
-/* ------------------------------- the consumer's gather (next row 4) */
+/* ------------------------------------ the consumer's gather of the rows */
 /* [IC]: the sparse MLA of each layer reads, per query token, the KV rows of the
  * selected keys; [IG] `_convert_once` gives it physical slots for that read.
  * The row format is not on the pages, so this copies bytes:
@@ -346,12 +349,23 @@ DSA_API int dsa_gather_rows(const uint8_t *rows, int64_t num_rows, int64_t row_b
  * queued on `stream`; it may enqueue its own work on the stream (the sparse
  * attention that reads the indices). 'S' layers own no indexer inputs: their
  * entries of `layers` are ignored and may be zero. */
+#define DSA_W_FP32 0
+#define DSA_W_BF16 1
 typedef struct DsaLayerInputs {
   const void *q;        /* device bf16 [T, 64, 128] */
-  const float *w;       /* device fp32 [T, 64] */
-  const void *k_new;    /* device bf16 [T, 128] or NULL (skip the cache insert) */
+  const void *w;        /* device [T, w_row_stride], the first 64 of a row used: fp32, or bf16 with
+                           w_dtype = DSA_W_BF16 (converted exactly to fp32 before the fold) */
+  const void *k_new;    /* device bf16 [T, k_row_stride] (first 128 used) or NULL (skip the cache insert) */
   uint8_t *k_cache;     /* device uint8 [num_blocks, 8448], or 4352 with an FP4 batch */
+  int64_t k_row_stride; /* elements between k_new rows: 0 = 128, else >= 128 and a multiple of 8 */
+  int64_t w_row_stride; /* elements between w rows: 0 = 64, else >= 64 */
+  int32_t w_dtype;      /* DSA_W_FP32 (0) or DSA_W_BF16 (1) */
 } DsaLayerInputs;
+/* [IC] `Indexer.forward` takes k = kw[:, :128] and weights = kw[:, 128:] as
+ * column views of one fused projection output kw, bf16 [T, 128 + 64]; pass
+ * them as they are: k_new = kw, k_row_stride = 192, w = kw + 128 (elements),
+ * w_row_stride = 192, w_dtype = DSA_W_BF16. Zero strides and w_dtype keep the
+ * contiguous fp32 layout of the fields above. */
 
 typedef void (*dsa_layer_consumer_fn)(int32_t layer, int32_t producer,
                                       const int32_t *physical, const int32_t *valid_counts,

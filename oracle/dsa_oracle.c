@@ -480,7 +480,7 @@ int ora_schedule(int n_layers, int use_index_cache, int freq, int offset,
 }
 
 /* ------------------------------------------------------------------------ */
-/* The consumer's gather (next row 4): "IndexCache：DeepSeek 稀疏注意力中的跨层
+/* The consumer's gather of the selected rows: "IndexCache：DeepSeek 稀疏注意力中的跨层
  * 索引复用" — the sparse MLA of every layer of a group reads, for each query
  * token, the KV rows of the k selected keys; "vllm.v1.attention.backends.mla.
  * index_group" converts the ids to physical slots for exactly that read. The

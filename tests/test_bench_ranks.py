@@ -50,3 +50,28 @@ def test_one_rank_needs_no_process_group():
     assert not dist.is_initialized()
     assert bench.max_over_ranks(0.3, "cpu") == 0.3
     assert bench.whole_job_rate(10.0, 1, 2.0) == 5.0
+
+
+def test_gpus_flag_starts_one_rank_per_replica():
+    """`bench.py --gpus 2` starts two ranks itself (torch.distributed.run), each
+    with its own RANK; rank 0 prints one line for the whole job, timed by the
+    slowest rank (--dry-run: CPU tasks over gloo instead of GPU replicas)."""
+    import json
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_PORT")}
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2", "--dry-run", "--steps", "5",
+                        "--warmup", "3"], capture_output=True, text=True, timeout=300, env=env, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    line = json.loads(lines[0])
+    assert line["n_gpus"] == 2
+    assert sorted(line["ranks"]) == [0, 1]
+    per_rank = line["rank_ms_per_step"]
+    assert len(per_rank) == 2 and per_rank[1] > per_rank[0]  # rank r sleeps (r + 1) ms a step
+    assert line["ms_per_step"] == pytest.approx(max(per_rank))
+    assert line["value"] == pytest.approx(1000.0 * 2 / (line["ms_per_step"] / 1e3))
+    assert line["scaling"] == "weak"

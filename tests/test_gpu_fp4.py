@@ -144,3 +144,13 @@ def test_fp4_full_size_decode_rows_sampled():
         ok, worst, at = compare.check_scores(res["logits"][t, :lens[i]], scores[i, :lens[i]])
         assert ok, f"row {t}: score error {worst:.3g}x tolerance at key {at}"
     assert not compare.check_topk(res["topk"][rows], scores, lens, hb.topk)
+
+
+def test_fp4_full_size_prefill_rows_sampled():
+    """prefill4x8k at full size with the FP4 cache (K quantised into it by the
+    fused prologue): every cache byte, and scores and top-k of sampled rows of
+    every request against the oracle."""
+    from tests.test_gpu_fullsize import sampled_rows
+
+    hb = synth.prefill4x8k()
+    check_batch(hb, rows=sampled_rows(hb, 8, 37), check_logits=True, fmt="fp4")

@@ -1,4 +1,4 @@
-"""The consumer's gather of the selected rows (next row 4), GPU against oracle.
+"""The consumer's gather of the selected rows by physical slot, GPU against oracle.
 
 The sparse MLA of each layer reads, per query token, the KV rows of its
 selected keys, by the physical slots the indexer produced. The row format is

@@ -187,3 +187,20 @@ def test_slot_errors_are_flagged_not_written():
     assert oracle.k_quant_write(k, slots, want) == 1
     assert np.array_equal(cache.cpu().numpy(), want)
     assert dsa.check_device_error(err) == 1
+
+
+def test_k_quant_write_strided_view_bit_exact():
+    # k as the column view kw[:, :128] (row stride 192) of a fused projection
+    # output, as [IC] `Indexer.forward` slices it: every cache byte bit-exact
+    hb = synth.make_batch(15, [300, 70], [(200, 130)], 64)
+    kw_bits = np.concatenate([hb.k_new, synth.bf16_bits(hb.w)], axis=1)
+    from tests.gpu_harness import bf16_tensor
+    kw = bf16_tensor(kw_bits)
+    for fmt in ("fp8", "fp4"):
+        cache = dsa.new_k_cache(hb.num_blocks, fmt, device=DEV)
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        dsa.indexer_k_quant_write(kw[:, :128], torch.from_numpy(hb.slot_mapping).to(DEV), cache, err)
+        want = oracle.new_cache(hb.num_blocks, fmt)
+        assert oracle.k_quant_write(hb.k_new, hb.slot_mapping, want) == 0
+        assert dsa.check_device_error(err) == 0
+        assert np.array_equal(cache.cpu().numpy(), want), fmt

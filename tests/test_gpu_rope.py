@@ -1,4 +1,4 @@
-"""RoPE fused into the quantiser (the first of the next rows), GPU against oracle.
+"""RoPE of q and K fused into the quantiser, GPU against oracle.
 
 "IndexCache：DeepSeek 稀疏注意力中的跨层索引复用", `Indexer.forward`: the leading
 64 dims of every q head and of the shared K row are rotated by

@@ -17,7 +17,18 @@ from tests.gpu_harness import DEV, bf16_tensor
 pytestmark = pytest.mark.gpu
 
 
-def run_stack(n_layers, freq, scale, n_decode, pattern=None, check_rows=None, fmt="fp8"):
+def fused_projection(hb):
+    """[IC] `Indexer.forward`'s fused projection output kw, bf16 [T, 128 + 64]:
+    the new K rows in columns 0..127 and the head weights, rounded to bf16 (the
+    projection's dtype), in columns 128..191. Returns kw and the weights as the
+    fp32 values the oracle receives (bf16 converts to fp32 exactly)."""
+    w_bits = synth.bf16_bits(hb.w)
+    kw_bits = np.concatenate([hb.k_new, w_bits], axis=1)
+    return bf16_tensor(kw_bits), synth.bf16_to_f32(w_bits)
+
+
+def run_stack(n_layers, freq, scale, n_decode, pattern=None, check_rows=None, fmt="fp8", strided=False,
+              block_stride_rows=0):
     fs, prod = dsa.schedule_build(n_layers, True, freq, 2, pattern)
     fs_o, prod_o = oracle.schedule(n_layers, True, freq, 2, pattern)
     assert fs == fs_o and prod == prod_o.tolist()
@@ -36,8 +47,13 @@ def run_stack(n_layers, freq, scale, n_decode, pattern=None, check_rows=None, fm
         hb = hbs[l]
         cache = dsa.new_k_cache(hb.num_blocks, fmt, device=DEV)
         dsa.indexer_k_quant_write(bf16_tensor(hb.ctx_k), torch.from_numpy(hb.ctx_slots).to(DEV), cache, err)
-        layers.append(dict(q=bf16_tensor(hb.q), w=torch.from_numpy(hb.w).to(DEV), k_new=bf16_tensor(hb.k_new),
-                           k_cache=cache))
+        if strided:  # k and w as the column views of one fused projection output
+            kw, hb.w = fused_projection(hb)
+            assert kw.shape[1] == 192 and kw[:, 128:].stride(0) == 192
+            layers.append(dict(q=bf16_tensor(hb.q), w=kw[:, 128:], k_new=kw[:, :128], k_cache=cache, kw=kw))
+        else:
+            layers.append(dict(q=bf16_tensor(hb.q), w=torch.from_numpy(hb.w).to(DEV), k_new=bf16_tensor(hb.k_new),
+                               k_cache=cache))
     T, k = meta.num_tokens, meta.topk
     topk_buf = torch.empty((T, k), dtype=torch.int32, device=DEV)
     phys_buf = torch.empty((T, k), dtype=torch.int32, device=DEV)
@@ -49,7 +65,7 @@ def run_stack(n_layers, freq, scale, n_decode, pattern=None, check_rows=None, fm
         seen.append((layer, producer, phys_buf.clone(), valid_buf.clone(), topk_buf.clone()))
 
     dsa.layer_stack_run(batch, fs, layers, k, slot_mapping=slots, topk_buf=topk_buf, phys_buf=phys_buf,
-                        valid_buf=valid_buf, consumer=consumer, dev_err=err)
+                        valid_buf=valid_buf, consumer=consumer, dev_err=err, block_stride_rows=block_stride_rows)
     torch.cuda.synchronize()
     assert dsa.check_device_error(err) == 0
     assert [s[0] for s in seen] == list(range(n_layers))
@@ -68,10 +84,12 @@ def run_stack(n_layers, freq, scale, n_decode, pattern=None, check_rows=None, fm
         fails = compare.check_topk(topk, scores, lens, k)
         assert not fails, f"layer {l}: {fails[:2]}"
         phys = snap[l][2].cpu().numpy()[rows]
+        valid = snap[l][3].cpu().numpy()[rows]
+        assert np.array_equal(valid, (topk >= 0).sum(axis=1)), f"layer {l}: valid counts"
         for i, t in enumerate(rows):
             n = int(lens[i])
             table, _ = oracle.convert(np.arange(n, dtype=np.int32)[None, :], hb.req_id_per_token[t:t + 1],
-                                      hb.block_table)
+                                      hb.block_table, 64, block_stride_rows)
             want = np.where(topk[i] >= 0, table[0][np.clip(topk[i], 0, None)], -1)
             assert np.array_equal(phys[i], want)
     return fs
@@ -84,3 +102,20 @@ def test_stack_freq4_scaled():
 
 def test_stack_pattern_scaled():
     run_stack(6, 4, scale=0.03, n_decode=3, pattern="FSFFSS")
+
+
+def test_stack_fused_projection_views():
+    # k_new and w are the column views kw[:, :128] and kw[:, 128:] (bf16, row
+    # stride 192) of one fused projection output, as [IC] `Indexer.forward`
+    # slices them: cache bytes bit-exact, top-k and ids against the oracle
+    run_stack(5, 4, scale=0.05, n_decode=6, strided=True)
+
+
+def test_stack_block_stride_rows_128():
+    # the runner's fused conversion with 128 physical rows per block ([IG]
+    # `_convert_once`, BLOCK_STRIDE_ROWS), against the oracle's conversion
+    run_stack(5, 4, scale=0.05, n_decode=6, block_stride_rows=128)
+
+
+def test_stack_fused_projection_views_fp4_stride_1000():
+    run_stack(5, 4, scale=0.03, n_decode=3, fmt="fp4", strided=True, block_stride_rows=1000)

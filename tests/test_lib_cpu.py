@@ -176,3 +176,28 @@ def test_cache_format_of_an_empty_cache():
 def test_graphed_layer_stack_refuses_a_consumer():
     with pytest.raises(binding.DsaError, match="consumer"):
         binding.LayerStack(None, "F", [None], 4, consumer=lambda *a: None, graphed=True)
+
+
+def test_layer_inputs_strides_and_weight_dtype_checked_on_the_host():
+    """DsaLayerInputs row strides and w dtype: bad values are rejected before
+    any launch; the fused projection's views (strides 192, bf16 w) pass the
+    host checks (then report no device here)."""
+    lib = binding.load()
+    b = binding.DsaBatchC(1, 1, 1, 1, 100, 2, 4, 256, 256, 256, 256)
+    fs = b"F"
+
+    def run(**kw):
+        L = dict(q=256, w=256 + 256, k_new=256, k_cache=256, k_row_stride=0, w_row_stride=0, w_dtype=0)
+        L.update(kw)
+        arr = (binding.DsaLayerInputsC * 1)(binding.DsaLayerInputsC(**L))
+        plan = binding.DsaStackPlanC(1, fs, arr, 64, 0.0, 0, None, None, 0)
+        return lib.dsa_layer_stack_run(ctypes.byref(plan), ctypes.byref(b), ctypes.c_void_p(256),
+                                       ctypes.c_void_p(256), ctypes.c_void_p(256), None, binding.CONSUMER_FN(),
+                                       None, ctypes.c_void_p(256), 1 << 30, None, None)
+
+    for bad in [dict(w_dtype=2), dict(w_dtype=-1), dict(k_row_stride=100), dict(k_row_stride=132),
+                dict(k_row_stride=-8), dict(w_row_stride=63), dict(w_row_stride=-1),
+                dict(w=256 + 3, w_dtype=1), dict(w=256 + 2, w_dtype=0)]:
+        assert run(**bad) == binding.DSA_EINVAL, bad
+    if not torch.cuda.is_available():  # on a GPU these placeholder pointers would reach the kernels
+        assert run(k_row_stride=192, w_row_stride=192, w=256 + 256, w_dtype=1) == binding.DSA_ENODEV

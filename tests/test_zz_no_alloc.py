@@ -4,15 +4,17 @@ It serves callers that cannot allocate device memory (plugins handed only an
 op's tensors, code that may not call the allocator): its scratch is a static
 device array inside the library. Here it is called through the C ABI twice in
 a row, on two different batches, and each result is checked against the
-allocating entry point dsa_indexer_logits_topk on the same inputs, with the
-top-k tolerance used by the other tests (ties within 2e-3 of the k-th score may
-resolve either way). The file is named to be collected last.
+allocating entry point dsa_indexer_logits_topk on the same inputs and against
+the oracle's fp64 scores, with the top-k tolerance used by the other tests
+(ties within 2e-3 of the k-th score may resolve either way). The file is named
+to be collected last.
 """
 import numpy as np
 import pytest
 import torch
 
 import dsa_sparse_attention_quant_gb300 as dsa
+import oracle
 from dsa_sparse_attention_quant_gb300 import binding, synth
 from oracle import compare
 from tests.gpu_harness import DeviceBatch
@@ -41,7 +43,15 @@ def _check(hb):
     scores = dsa.indexer_logits(db.batch, q8, wf, db.k_cache)
     torch.cuda.synchronize()
     assert dsa.check_device_error(db.dev_err) == 0
-    _same_topk(got.cpu().numpy(), want.cpu().numpy(), scores.cpu().numpy(), hb.positions + 1, hb.topk)
+    got, want = got.cpu().numpy(), want.cpu().numpy()
+    lens = hb.positions + 1
+    _same_topk(got, want, scores.cpu().numpy(), lens, hb.topk)
+    # against the oracle: the static call's cache bytes and its top-k sets
+    cache = oracle.fill_cache(hb)
+    assert np.array_equal(db.k_cache.cpu().numpy(), cache)
+    _, ora_scores = oracle.indexer(hb, cache, rows=np.arange(hb.num_tokens), with_scores=True)
+    fails = compare.check_topk(got, ora_scores, lens, hb.topk)
+    assert not fails, f"static call vs oracle: {fails[:2]}"
 
 
 def test_static_entry_point_two_calls_in_a_row():
