@@ -13,6 +13,7 @@
 namespace dsa {
 
 constexpr int kPlanStage = 2048;  // requests per segment staged in shared memory
+constexpr int kBlockCost = 2;     // cost of a query block's q / w' load, in tiles
 
 struct PlanSmem {
   int scan[33];
@@ -95,7 +96,11 @@ __device__ void plan_segment(const int32_t* qsl_g, const int32_t* sl_g, int r_be
   }
   for (int c = threadIdx.x; c < grid; c += blockDim.x) P.cta[c] = CtaWork{0, 0, 0, 0};
   __syncthreads();
-  // pass 2: tile prefix, and for every CTA the block holding the start of its slice
+  // pass 2: tile prefix, and for every CTA the start of its slice. Slices are
+  // equal in cost, where a block costs its tiles plus kBlockCost: a CTA whose
+  // blocks hold few tiles (the first blocks of a prefill, one tile each) waits
+  // on a q / w' load per block, and with equal tiles it finished last.
+  const int64_t W = static_cast<int64_t>(total) + static_cast<int64_t>(nqb) * kBlockCost;
   carry = 0;
   for (int b0 = 0; b0 < nqb; b0 += blockDim.x) {
     const int j = b0 + threadIdx.x;
@@ -108,18 +113,25 @@ __device__ void plan_segment(const int32_t* qsl_g, const int32_t* sl_g, int r_be
     if (j < nqb) {
       const int s = carry + incl - tiles;
       P.tile_start[j] = s;
-      // CTA c starts at floor(total*c/grid): the c with s <= start < s + tiles
-      const int64_t c_lo = (static_cast<int64_t>(s) * grid + total - 1) / total;
-      const int64_t c_hi = (static_cast<int64_t>(s + tiles) * grid + total - 1) / total - 1;
+      // block j spans costs [ws, ws + kBlockCost + tiles): its load, then its
+      // tiles. CTA c starts at cost floor(W*c/grid): the c whose start lies in
+      // that span begin at the tile it falls on (the first, if it falls on the load)
+      const int64_t ws = static_cast<int64_t>(s) + static_cast<int64_t>(j) * kBlockCost;
+      const int64_t c_lo = (ws * grid + W - 1) / W;
+      const int64_t c_hi = ((ws + kBlockCost + tiles) * grid + W - 1) / W - 1;
       for (int64_t c = c_lo; c <= c_hi && c < grid; ++c) {
-        const int b_lo = static_cast<int>(static_cast<int64_t>(total) * c / grid);
-        const int b_hi = static_cast<int>(static_cast<int64_t>(total) * (c + 1) / grid);
-        P.cta[c] = CtaWork{b_lo, b_hi, j, b_lo - s};
+        const int64_t off = W * c / grid - ws - kBlockCost;
+        const int kt = off > 0 ? static_cast<int>(off) : 0;
+        P.cta[c] = CtaWork{s + kt, 0, j, kt};
       }
     }
     carry += tot;
   }
   if (threadIdx.x == 0) P.tile_start[nqb] = carry;
+  __syncthreads();
+  // pass 3: each slice ends where the next begins
+  for (int c = threadIdx.x; c < grid; c += blockDim.x)
+    P.cta[c].it_end = nqb == 0 ? 0 : (c + 1 < grid ? P.cta[c + 1].it_begin : carry);
   __syncthreads();
 }
 

@@ -11,14 +11,15 @@
 //
 // Both kernels are exact radix selects (select.cuh); ids are emitted in no
 // particular order.
-//  * topk_kernel: one 256-thread CTA per row, shared memory sized to the row
-//    (several rows run per SM). Pass 1 comes from the histogram the score
-//    kernel built when there is one, else from the row. Rows that fit are
-//    staged once in shared memory; longer rows are re-read from L2.
-//  * select_kernel: decode rows, whose pass-1 histogram the score kernel
-//    accumulated. Several CTAs per row place the keys above the boundary bin
-//    and collect the boundary bin's keys; the last CTA of the row to finish
-//    resolves the boundary bin on those candidates only.
+//  * topk_kernel: one CTA per row. Pass 1 comes from the histogram the score
+//    kernel built when there is one (decode rows), else from the row. Rows
+//    that fit the launch's staging area are staged once in shared memory;
+//    longer rows are re-read from L2. Prefill rows run in 256-thread CTAs,
+//    several per SM; decode rows of up to 32768 scores in 1024-thread CTAs.
+//  * select_kernel: decode rows longer than that. Several CTAs per row place
+//    the keys above the boundary bin and collect the boundary bin's keys; the
+//    last CTA of the row to finish resolves the boundary bin on those
+//    candidates only.
 #include "select.cuh"
 
 namespace dsa {
@@ -75,23 +76,38 @@ __device__ __forceinline__ RowOut row_out(const PhysOut& po, int32_t* out, int t
   return o;
 }
 
+// Shapes of the per-row top-k: 256-thread CTAs, several per SM, for the many
+// rows of a prefill; 1024-thread CTAs, one per SM, that stage rows of up to
+// 32768 scores, for the few long rows of a decode batch.
+template <int NT>
+struct RowCfg {
+  static constexpr int kStageMax = NT == 1024 ? 32768 : kTopkRowCap;  // scores staged per row, at most
+  static constexpr int kCand = NT == 1024 ? 4096 : kStagedCandCap;    // boundary-bin candidates staged
+  static constexpr int kLoads = NT == 1024 ? 8 : 12;                  // float4 loads in flight per thread
+};
+
 // One CTA per row (rows row_begin + blockIdx.x). Shared memory, sized by the
-// launch: the histogram, `cap` boundary-bin candidates (keys, ids), the row's
-// ids (topk, rounded up to 4) and, when staged, its keys.
-template <bool kStaged>
-__global__ void __launch_bounds__(kRowThreads) topk_kernel(const float* __restrict__ logits, int64_t ld,
-                                                           const int32_t* qsl, const int32_t* seq_lens,
-                                                           const int32_t* req_id, int num_reqs, int row_begin,
-                                                           int topk, int32_t* __restrict__ out, PhysOut po,
-                                                           const uint32_t* hist_g, int hist_rows, int cap) {
+// launch: the histogram, kCand boundary-bin candidates (keys, ids), the row's
+// ids (topk, rounded up to 4) and a staging area of stage_cap keys. A row of
+// at most stage_cap keys is staged there once; a longer row is re-read from
+// L2 and the staging area holds up to stage_cap / 2 candidates instead. The
+// choice is made per row, so the short prefill rows of a batch whose score
+// rows are long (decode requests at long context) still stage.
+template <int NT>
+__global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 4) topk_kernel(const float* __restrict__ logits, int64_t ld,
+                                                                      const int32_t* qsl, const int32_t* seq_lens,
+                                                                      const int32_t* req_id, int num_reqs,
+                                                                      int row_begin, int topk,
+                                                                      int32_t* __restrict__ out, PhysOut po,
+                                                                      const uint32_t* hist_g, int hist_rows,
+                                                                      int stage_cap) {
+  using R = RowCfg<NT>;
   extern __shared__ __align__(16) uint32_t sh[];
   uint32_t* hist = sh;
-  uint32_t* ckey = sh + kSelBins;
-  uint32_t* cidx = ckey + cap;
-  uint32_t* oid = cidx + cap;
+  uint32_t* oid = sh + kSelBins + 2 * R::kCand;
   uint32_t* keys = oid + ((topk + 3) & ~3);
   __shared__ SelState s;
-  __shared__ int32_t bts[kTopkRowCap / kBlock];
+  __shared__ int32_t bts[R::kStageMax / kBlock];
 
   // the request metadata and the block table are inputs of the step: read
   // them while the score kernel may still run
@@ -99,11 +115,12 @@ __global__ void __launch_bounds__(kRowThreads) topk_kernel(const float* __restri
   const int tid = threadIdx.x;
   int r;
   const int n = row_length(t, qsl, seq_lens, req_id, num_reqs, ld, &r);
+  const bool staged = n <= stage_cap;
   RowOut o = row_out(po, out, topk, t, r, num_reqs);
-  if (kStaged && o.prow != nullptr && n > topk) {  // the request's block-table row, for emit
-    const int cap = po.bt_stride < kTopkRowCap / kBlock ? static_cast<int>(po.bt_stride) : kTopkRowCap / kBlock;
+  if (staged && o.prow != nullptr && n > topk) {  // the request's block-table row, for emit
+    const int cap = po.bt_stride < R::kStageMax / kBlock ? static_cast<int>(po.bt_stride) : R::kStageMax / kBlock;
     const int pages = min((n + kBlock - 1) / kBlock, cap);
-    for (int p = tid; p < pages; p += kRowThreads) bts[p] = __ldg(o.bt_row + p);
+    for (int p = tid; p < pages; p += NT) bts[p] = __ldg(o.bt_row + p);
     o.bt_row = bts;
   }
   pdl_wait();  // the scores come from the previous kernel
@@ -119,72 +136,93 @@ __global__ void __launch_bounds__(kRowThreads) topk_kernel(const float* __restri
   const bool have_hist = hist_g != nullptr && t < hist_rows;
   if (have_hist) {
     const uint4* hrow = reinterpret_cast<const uint4*>(hist_g + static_cast<int64_t>(t) * kSelBins);
-    for (int b = tid; b < kSelBins / 4; b += kRowThreads) reinterpret_cast<uint4*>(hist)[b] = __ldcg(hrow + b);
+    for (int b = tid; b < kSelBins / 4; b += NT) reinterpret_cast<uint4*>(hist)[b] = __ldcg(hrow + b);
   } else {
-    for (int b = tid; b < kSelBins; b += kRowThreads) hist[b] = 0;
+    for (int b = tid; b < kSelBins; b += NT) hist[b] = 0;
   }
-  if constexpr (kStaged) {
-    // rows are 16-byte aligned (ld is a multiple of 4): float4 loads, up to twelve in flight per thread
-    const float4* l4 = reinterpret_cast<const float4*>(lrow);
-    const int n4 = (n + 3) >> 2;
-    for (int base = 0; base < n4; base += 12 * kRowThreads) {
-      float4 v[12];
+  // rows are 16-byte aligned (ld is a multiple of 4): float4 loads, several in flight per thread
+  const float4* l4 = reinterpret_cast<const float4*>(lrow);
+  const int n4 = (n + 3) >> 2;
+  if (staged) {
+    constexpr int U = R::kLoads;
+    for (int base = 0; base < n4; base += U * NT) {
+      float4 v[U];
 #pragma unroll
-      for (int u = 0; u < 12; ++u) {
-        const int i4 = base + u * kRowThreads + tid;
+      for (int u = 0; u < U; ++u) {
+        const int i4 = base + u * NT + tid;
         v[u] = i4 < n4 ? __ldcg(l4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
-      for (int u = 0; u < 12; ++u) {
-        const int i4 = base + u * kRowThreads + tid;
+      for (int u = 0; u < U; ++u) {
+        const int i4 = base + u * NT + tid;
         if (i4 < n4) reinterpret_cast<uint4*>(keys)[i4] =
             make_uint4(f32_key(v[u].x), f32_key(v[u].y), f32_key(v[u].z), f32_key(v[u].w));
       }
     }
-  }
-  __syncthreads();
-  auto key_at = [&](int i) -> uint32_t {
-    if constexpr (kStaged) return keys[i];
-    else return f32_key(__ldcg(lrow + i));
-  };
-  if (!have_hist) {
-    for (int i = tid; i < n; i += kRowThreads) atomicAdd(&hist[key_at(i) >> kHistShift], 1u);
     __syncthreads();
-  }
-  if constexpr (kStaged) {
-    select_row_staged<kRowThreads>(keys, n, hist, ckey, cidx, oid, topk, static_cast<uint32_t>(cap), o, s, &bad);
-  } else {
-    select_row<kRowThreads>(key_at, n, hist, ckey, cidx, oid, topk, static_cast<uint32_t>(cap), o, s, &bad);
+    if (!have_hist) {
+      for (int i = tid; i < n; i += NT) atomicAdd(&hist[keys[i] >> kHistShift], 1u);
+      __syncthreads();
+    }
+    select_row_staged<NT>(keys, n, hist, sh + kSelBins, sh + kSelBins + R::kCand, oid, topk, R::kCand, o, s, &bad);
+  } else if constexpr (NT <= 512) {  // (the 1024-thread launch stages every row: stage_cap >= ld)
+    __syncthreads();
+    if (!have_hist) {  // pass 1 from L2, eight float4 loads in flight per thread
+      for (int base = 0; base < n4; base += 8 * NT) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i4 = base + u * NT + tid;
+          v[u] = i4 < n4 ? __ldcg(l4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = 4 * (base + u * NT + tid);
+          if (i < n) atomicAdd(&hist[f32_key(v[u].x) >> kHistShift], 1u);
+          if (i + 1 < n) atomicAdd(&hist[f32_key(v[u].y) >> kHistShift], 1u);
+          if (i + 2 < n) atomicAdd(&hist[f32_key(v[u].z) >> kHistShift], 1u);
+          if (i + 3 < n) atomicAdd(&hist[f32_key(v[u].w) >> kHistShift], 1u);
+        }
+      }
+      __syncthreads();
+    }
+    // the staging area holds the boundary bin's candidates instead
+    const int cap = stage_cap / 2;
+    select_row<NT>([&](int i) -> uint32_t { return f32_key(__ldcg(lrow + i)); }, n, hist, keys, keys + cap, oid,
+                   topk, static_cast<uint32_t>(cap), o, s, &bad);
   }
   if (bad) flag_error(po.err, DSA_DEVERR_ID_RANGE);
+}
+
+// Keys staged per row by the 256-thread launch: the whole row when the score
+// rows fit kTopkRowCap, else 8192 (four CTAs per SM at k = 2048); longer rows
+// are re-read from L2.
+constexpr int kLongRowStage = 8192;
+
+template <int NT>
+static cudaError_t launch_topk_rows(const float* logits, int64_t ld, const int32_t* qsl, const int32_t* seq_lens,
+                                    const int32_t* req_id, int num_reqs, int row_begin, int n_tokens, int topk,
+                                    int32_t* out, const TopkPhys* phys, const uint32_t* hist, int hist_rows,
+                                    int stage_cap, cudaStream_t stream) {
+  using R = RowCfg<NT>;
+  const int rows = n_tokens - row_begin;
+  if (rows <= 0) return cudaSuccess;
+  const int ids = (topk + 3) & ~3;
+  const int smem = (kSelBins + 2 * R::kCand + ids + stage_cap) * 4;
+  static uint64_t configured = 0;  // the largest layout: k = kMaxTopk, stage_cap = kStageMax
+  cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(topk_kernel<NT>),
+                                   (kSelBins + 2 * R::kCand + kMaxTopk + R::kStageMax) * 4, &configured);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(topk_kernel<NT>, dim3(rows), dim3(NT), smem, stream, logits, ld, qsl, seq_lens, req_id, num_reqs,
+                    row_begin, topk, out, phys_out(phys), hist, hist_rows, stage_cap);
 }
 
 cudaError_t launch_topk(const float* logits, int64_t ld, const int32_t* qsl, const int32_t* seq_lens,
                         const int32_t* req_id, int num_reqs, int row_begin, int n_tokens, int topk, int32_t* out,
                         const TopkPhys* phys, const uint32_t* hist, int hist_rows, cudaStream_t stream) {
-  const int rows = n_tokens - row_begin;
-  if (rows <= 0) return cudaSuccess;
-  const PhysOut po = phys_out(phys);
-  const int ids = (topk + 3) & ~3;
-  if (ld <= kTopkRowCap) {
-    const int cap = kStagedCandCap;
-    const int smem = (kSelBins + 2 * cap + ids + static_cast<int>((ld + 3) & ~3)) * 4;
-    static uint64_t configured = 0;  // the largest layout: k = kMaxTopk, ld = kTopkRowCap
-    cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(topk_kernel<true>),
-                                     (kSelBins + 2 * kStagedCandCap + kMaxTopk + kTopkRowCap) * 4, &configured);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(topk_kernel<true>, dim3(rows), dim3(kRowThreads), smem, stream, logits, ld, qsl, seq_lens,
-                      req_id, num_reqs, row_begin, topk, out, po, hist, hist_rows, cap);
-  } else {
-    const int cap = kCandCap;
-    const int smem = (kSelBins + 2 * cap + ids) * 4;
-    static uint64_t configured = 0;
-    cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(topk_kernel<false>),
-                                     (kSelBins + 2 * kCandCap + kMaxTopk) * 4, &configured);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(topk_kernel<false>, dim3(rows), dim3(kRowThreads), smem, stream, logits, ld, qsl, seq_lens,
-                      req_id, num_reqs, row_begin, topk, out, po, hist, hist_rows, cap);
-  }
+  const int stage_cap = ld <= kTopkRowCap ? static_cast<int>((ld + 3) & ~3) : kLongRowStage;
+  return launch_topk_rows<kRowThreads>(logits, ld, qsl, seq_lens, req_id, num_reqs, row_begin, n_tokens, topk, out,
+                                       phys, hist, hist_rows, stage_cap, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -342,6 +380,14 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(SelectArgs a, Ph
 
 cudaError_t launch_select(const SelectArgs& a, const TopkPhys* phys, int num_sms, cudaStream_t stream) {
   if (a.n_rows <= 0) return cudaSuccess;
+  // rows of up to 32768 scores: one 1024-thread CTA per row stages the whole
+  // row; cross-CTA exchanges (global reservations, or a thread-block cluster's
+  // distributed shared memory) measured slower for these (decode32 step 27.6
+  // and 24.6 against 22.7 us)
+  if (a.ld <= RowCfg<1024>::kStageMax)
+    return launch_topk_rows<1024>(a.logits, a.ld, a.qsl, a.seq_lens, a.req_id, a.num_reqs, 0, a.n_rows, a.topk, a.out,
+                                  phys, a.hist, a.n_rows, static_cast<int>((a.ld + 3) & ~3), stream);
+  // longer rows: chunks of the row in independent CTAs
   // chunks of 1024..8192 scores, the smallest that keeps every row's chunks
   // within about two CTAs per SM
   int chunk = 1024;

@@ -204,3 +204,18 @@ def test_k_quant_write_strided_view_bit_exact():
         assert oracle.k_quant_write(hb.k_new, hb.slot_mapping, want) == 0
         assert dsa.check_device_error(err) == 0
         assert np.array_equal(cache.cpu().numpy(), want), fmt
+
+
+def test_decode_row_longer_than_one_cta_stages():
+    # a decode row past 32768 scores takes the select of independent chunk
+    # CTAs; the other rows of the batch share its launch
+    hb = synth.make_batch(16, [140000, 3000, 2049], [], 2048)
+    check_batch(hb)
+
+
+def test_decode_rows_ragged_lengths_one_cta_per_row():
+    # decode rows staged whole by one CTA each, ragged lengths and tails,
+    # k from 512 to 2048, rows up to the 32768-score staging limit
+    for seed, lens, k in ((17, [1000, 700, 600], 512), (18, [1500, 900], 1024), (19, [5000, 4097, 2100], 1024),
+                          (20, [8000, 1100], 1024), (21, [32768, 20000, 7000, 64], 2048)):
+        check_batch(synth.make_batch(seed, lens, [], k))
