@@ -466,41 +466,49 @@ __global__ void __launch_bounds__(LogitsCfg<NTOK, FP4>::kThreads, 1)
         if (lane == 0) mbar_arrive(&empty[stage]);
         const int key = (meta.kt0 + e) * 128 + row;
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * C::N;
+        // the warpgroup's tokens in halves of 32 heads: each half's TMEM load
+        // is in flight while the previous half is reduced (columns of tokens
+        // past the block's end are read too, and not stored)
+        auto reduce32 = [&](const uint32_t (&r)[32], const float4* w, uint64_t& s01, uint64_t& s23) {
+#pragma unroll
+          for (int h = 0; h < 32; h += 4) {
+            const float4 w4 = w[h / 4];  // the same address across the warp: one broadcast load
+            s01 = fma_f32x2(pack_f32x2(w4.x, w4.y),
+                            pack_f32x2(fmaxf(__uint_as_float(r[h]), 0.f), fmaxf(__uint_as_float(r[h + 1]), 0.f)), s01);
+            s23 = fma_f32x2(pack_f32x2(w4.z, w4.w),
+                            pack_f32x2(fmaxf(__uint_as_float(r[h + 2]), 0.f), fmaxf(__uint_as_float(r[h + 3]), 0.f)),
+                            s23);
+          }
+        };
+        uint32_t ra[32], rb[32];
+        tmem_ld32(tbase + tok0 * kHeads, ra);
+        tmem_wait32(ra);
 #pragma unroll
         for (int tt = 0; tt < C::kTokPerWG; ++tt) {
           const int tok = tok0 + tt;
-          if (tok < qb.ntok) {
-            const float4* wt = reinterpret_cast<const float4*>(wq + tok * kHeads);
-            float v[kHeads];
-            tmem_ld64_sync(tbase + tok * kHeads, v);
-            if (tt == C::kTokPerWG - 1) {
-              // the accumulator's last columns this warp reads are in registers:
-              // hand it back to the MMA before reducing them
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&tempty[acc]);
-            }
-            // four chains (heads h mod 4), two per packed fma (one issue slot
-            // for two chains' steps)
-            uint64_t s01 = 0, s23 = 0;
-#pragma unroll
-            for (int h = 0; h < kHeads; h += 4) {
-              const float4 w4 = wt[h / 4];  // the same address across the warp: one broadcast load
-              s01 = fma_f32x2(pack_f32x2(w4.x, w4.y), pack_f32x2(fmaxf(v[h], 0.f), fmaxf(v[h + 1], 0.f)), s01);
-              s23 = fma_f32x2(pack_f32x2(w4.z, w4.w), pack_f32x2(fmaxf(v[h + 2], 0.f), fmaxf(v[h + 3], 0.f)), s23);
-            }
-            if (key <= qb.p0 + tok && key < a.ld) {
-              const float2 p01 = unpack_f32x2(s01), p23 = unpack_f32x2(s23);
-              const float score = ((p01.x + p01.y) + (p23.x + p23.y)) * kscale;
-              a.logits[static_cast<int64_t>(qb.t0 + tok) * a.ld + key] = score;
-              if constexpr (NTOK == 1) {
-                if (use_hist) atomicAdd(&ghist[f32_key(score) >> kHistShift], 1u);
-              }
-            }
-          } else if (tt == C::kTokPerWG - 1) {  // a short block: nothing to read from the last columns
+          const float4* wt = reinterpret_cast<const float4*>(wq + tok * kHeads);
+          uint64_t s01 = 0, s23 = 0;
+          tmem_ld32(tbase + tok * kHeads + 32, rb);
+          reduce32(ra, wt, s01, s23);
+          tmem_wait32(rb);
+          if (tt + 1 < C::kTokPerWG) {
+            tmem_ld32(tbase + (tok + 1) * kHeads, ra);
+          } else {
+            // this warp's last columns are in registers: hand the accumulator
+            // back to the MMA before reducing them
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
+          }
+          reduce32(rb, wt + 8, s01, s23);
+          if (tt + 1 < C::kTokPerWG) tmem_wait32(ra);
+          if (tok < qb.ntok && key <= qb.p0 + tok && key < a.ld) {
+            const float2 p01 = unpack_f32x2(s01), p23 = unpack_f32x2(s23);
+            const float score = ((p01.x + p01.y) + (p23.x + p23.y)) * kscale;
+            a.logits[static_cast<int64_t>(qb.t0 + tok) * a.ld + key] = score;
+            if constexpr (NTOK == 1) {
+              if (use_hist) atomicAdd(&ghist[f32_key(score) >> kHistShift], 1u);
+            }
           }
         }
       }
