@@ -340,9 +340,12 @@ def workload_config(name: str, hb, args, world: int) -> dict:
         "rope": "q and new K rotated (RoPE) in the layer prologue" if args.rope else "inputs arrive rotated",
     }
     if name == "stack61":
+        if args.stack_layers != STACK_LAYERS:
+            cfg["workload"] += f" [profiling case: the first {args.stack_layers} layers]"
         slot_bytes = 68 if fp4 else 132
-        cfg.update({"layers": STACK_LAYERS, "freq": STACK_FREQ, "f_layers": 16,
-                    "pairs_per_step": 16 * hb.num_pairs(),
+        n_f = sum(1 for l in range(args.stack_layers) if max(l - 1, 0) % STACK_FREQ == 0)
+        cfg.update({"layers": args.stack_layers, "freq": STACK_FREQ, "f_layers": n_f,
+                    "pairs_per_step": n_f * hb.num_pairs(),
                     "l2": f"inputs larger than L2: every F layer reads its own "
                           f"{hb.num_blocks * 64 * slot_bytes / 1e6:.0f} MB K cache"})
     else:
@@ -725,11 +728,12 @@ def run_stack(args, ranks: Ranks, with_cpu: bool):
     T, k = meta.num_tokens, meta.topk
     batch = dsa.Batch.from_host(meta, dev)
     slots = torch.from_numpy(meta.slot_mapping).to(dev)
-    fs4, _ = dsa.schedule_build(STACK_LAYERS, True, STACK_FREQ)
-    fs1, _ = dsa.schedule_build(STACK_LAYERS, True, 1)
+    n_layers = args.stack_layers
+    fs4, _ = dsa.schedule_build(n_layers, True, STACK_FREQ)
+    fs1, _ = dsa.schedule_build(n_layers, True, 1)
     n_f = fs4.count("F")
-    layers = stack_inputs(meta, STACK_LAYERS, dev, dsa, torch, args.kcache)
-    l4 = [layers[l] if fs4[l] == "F" else None for l in range(STACK_LAYERS)]
+    layers = stack_inputs(meta, n_layers, dev, dsa, torch, args.kcache)
+    l4 = [layers[l] if fs4[l] == "F" else None for l in range(n_layers)]
     ws = torch.empty(dsa.layer_stack_workspace_size(batch, k), dtype=torch.uint8, device=dev)
     topk = torch.empty((T, k), dtype=torch.int32, device=dev)
     phys = torch.empty((T, k), dtype=torch.int32, device=dev)
@@ -762,7 +766,7 @@ def run_stack(args, ranks: Ranks, with_cpu: bool):
     cap.wait_stream(stream)
     g4 = capture_graph(torch, cap, lambda: run(fs4, l4))
     g1 = capture_graph(torch, cap, lambda: run(fs1, layers))
-    one = [capture_graph(torch, cap, lambda i=i: run("F", [layers[i % STACK_LAYERS]], kev[i]))
+    one = [capture_graph(torch, cap, lambda i=i: run("F", [layers[i % n_layers]], kev[i]))
            for i in range(args.steps)]
     stream.wait_stream(cap)
     torch.cuda.synchronize()
@@ -848,11 +852,14 @@ def run_stack(args, ranks: Ranks, with_cpu: bool):
     ms = {kname: float(per_kernel[:, j].mean()) for j, kname in enumerate(kernels)}
     slot_bytes = 68 if args.kcache == "fp4" else 132
     mma = "tcgen05 kind::f8f6f4 E2M1 K x E4M3 q" if args.kcache == "fp4" else "tcgen05 FP8"
+    fp4_tag = "_fp4" if args.kcache == "fp4" else ""
     phases = {
         "decode_scores": hbm_roofline(f"dsa::logits_kernel<1> (decode scores, {mma})",
-                                      decode_score_bytes(dec_pairs, n_dec, slot_bytes), ms["logits<1>"], peaks),
+                                      decode_score_bytes(dec_pairs, n_dec, slot_bytes), ms["logits<1>"], peaks,
+                                      traffic=profiled_traffic(f"logits_kernel_decode_stack61{fp4_tag}.md")),
         "prefill_scores": tensor_roofline(f"dsa::logits_kernel<4> (prefill scores, {mma})",
-                                          pre_pairs * FLOP_PER_PAIR, ms["logits<4>"], peaks),
+                                          pre_pairs * FLOP_PER_PAIR, ms["logits<4>"], peaks,
+                                          traffic=profiled_traffic(f"logits_kernel_prefill_stack61{fp4_tag}.md")),
         "decode_topk": {"kernel": "dsa::select_kernel", "bound": "latency", "avg_launch_ms": ms["select"],
                         "rows": n_dec, "rows_per_s": n_dec / (ms["select"] / 1e3)},
         "prefill_topk": {"kernel": "dsa::topk_kernel", "bound": "latency", "avg_launch_ms": ms["topk"],
@@ -1105,6 +1112,8 @@ def main(argv=None):
                     help="single-layer workloads measured after stack61 and reported under `workloads` "
                          "('' for none)")
     ap.add_argument("--replicas", type=int, default=0)
+    ap.add_argument("--stack-layers", type=int, default=STACK_LAYERS,
+                    help="layers of the stack61 workload (fewer only to profile a small case)")
     ap.add_argument("--clock-window", type=float, default=1.0, help="seconds of untimed steps while sampling clocks")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
