@@ -13,7 +13,7 @@
 namespace dsa {
 
 constexpr int kPlanStage = 2048;  // requests per segment staged in shared memory
-constexpr int kBlockCost = 2;     // cost of a query block's q / w' load, in tiles
+constexpr int kBlockCost = 1;     // cost of a query block's q / w' load, in tiles
 
 struct PlanSmem {
   int scan[33];
