@@ -410,7 +410,12 @@ def run_layer(args, name: str, ranks: Ranks, with_cpu: bool):
     has_pre = hb.num_reqs > hb.num_decodes
     kernels = ["prologue"] + (["logits<1>"] if has_dec else []) + (["logits<4>"] if has_pre else []) + \
         (["select"] if has_dec else []) + (["topk"] if has_pre else [])
-    launches_per_step = len(kernels)
+    launches_per_step = len(kernels)  # timeline marks per step
+    # decode rows that one CTA stages (up to 32768 scores) take one top-k
+    # launch; longer ones a chunk launch and a resolving launch, timed together
+    # as "select"
+    long_rows = has_dec and (batch.max_seq_len + 3) // 4 * 4 > 32768
+    kernel_launches = launches_per_step + (1 if long_rows else 0)
 
     # --rope: q and the new K rows arrive un-rotated and the layer's prologue
     # applies RoPE (positions + cos/sin table) before quantising them
@@ -549,7 +554,7 @@ def run_layer(args, name: str, ranks: Ranks, with_cpu: bool):
         "roofline": roofline,
         "breakdown_us": breakdown,
         "e2e": e2e,
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": kernel_launches * args.steps,
         "clocks": clocks.summary(),
         "wall_s_timed_region": wall1 - wall0,
     }

@@ -157,6 +157,7 @@ struct IndexerWs {
   SegmentPlan pre;
   float* logits;
   uint32_t* hist;
+  uint32_t* hist2;
   uint32_t* counters;
   uint2* cand;
   int hist_rows;
@@ -185,6 +186,7 @@ IndexerWs carve(const DsaBatch* b, void* base) {
   w.pre.max_qb = static_cast<int32_t>(max_pre);
   w.logits = static_cast<float*>(take(T * ld * 4));
   w.hist = static_cast<uint32_t*>(take(Td * kHistBins * 4));
+  w.hist2 = static_cast<uint32_t*>(take(Td * kHistBins * 4));
   w.counters = static_cast<uint32_t*>(take(Td * kRowCounters * 4));
   w.cand = static_cast<uint2*>(take(Td * ld * sizeof(uint2)));
   w.hist_rows = static_cast<int>(Td);
@@ -213,6 +215,7 @@ PrologueArgs plan_only(const DsaBatch* b, const IndexerWs& ws, int sms, const vo
   pa.plan = b->num_reqs > b->num_decodes;
   pa.p = plan_args(b, ws, sms, dev_err);
   pa.hist = ws.hist;
+  pa.hist2 = ws.hist2;
   pa.counters = ws.counters;
   pa.hist_rows = ws.hist_rows;
   pa.err = dev_err;
@@ -270,7 +273,7 @@ int run_logits(const DsaBatch* b, const uint8_t* q_fp8, const float* w_folded, c
 int run_topk(const DsaBatch* b, const IndexerWs& ws, int64_t ld, int32_t topk, int32_t* out, const TopkPhys* phys,
              int sms, cudaStream_t stream) {
   SelectArgs sa{ws.logits, ld, b->query_start_loc, b->seq_lens, b->req_id_per_token, b->num_reqs,
-                ws.hist_rows, topk, out, ws.hist, ws.counters, ws.cand};
+                ws.hist_rows, topk, out, ws.hist, ws.counters, ws.cand, ws.hist2};
   int st = DSA_OK;
   if (ws.hist_rows > 0 && (st = launched(launch_select(sa, phys, sms, stream), stream)) != DSA_OK) return st;
   if (b->num_tokens > ws.hist_rows)

@@ -107,6 +107,7 @@ struct PrologueArgs {
   bool plan;
   PlanArgs p;
   uint32_t* hist;      // zeroed here for the score kernel: [hist_rows][kHistBins]
+  uint32_t* hist2;     // zeroed here for the select: [hist_rows][kHistBins]
   uint32_t* counters;  // [hist_rows][kRowCounters]
   int hist_rows;
   int32_t* err;
@@ -129,8 +130,8 @@ struct TopkPhys {
   int32_t* err;
 };
 
-// Per decode row (multi-CTA select): ids out, boundary-bin candidates,
-// finished chunks, spare.
+// Per decode row (multi-CTA select): ids placed, boundary-bin candidates,
+// the boundary bin, the count above it.
 constexpr int kRowCounters = 4;
 
 // Rows up to this many scores are staged in shared memory by the top-k.
@@ -166,8 +167,9 @@ struct SelectArgs {
   int topk;
   int32_t* out;             // [T, topk]
   const uint32_t* hist;     // [n_rows][kHistBins]
-  uint32_t* counters;       // [n_rows][kRowCounters], zeroed before
+  uint32_t* counters;       // [n_rows][kRowCounters], zeroed before: ids placed, candidates, b1, count above b1
   uint2* cand;              // [n_rows][ld]: (key, id) of the boundary bin
+  uint32_t* hist2;          // [n_rows][kHistBins], zeroed before: the boundary bin's next 11 bits
 };
 
 // ntok_per_block = 1 (decode segment: the kernel plans its slice from the
@@ -184,8 +186,9 @@ cudaError_t launch_topk(const float* logits, int64_t ld, const int32_t* qsl, con
                         const TopkPhys* phys, const uint32_t* hist, int hist_rows, cudaStream_t stream);
 
 // Decode rows [0, a.n_rows) whose score histograms the score kernel built:
-// each row in chunks sized so that all rows' chunks run at once, one CTA per
-// chunk; the last CTA of a row resolves its boundary bin.
+// one CTA per row when the rows fit one CTA's shared memory; else each row in
+// chunks (one CTA per chunk) and a second launch, one CTA per row, resolving
+// the boundary bin.
 cudaError_t launch_select(const SelectArgs& a, const TopkPhys* phys, int num_sms, cudaStream_t stream);
 
 // The consumer's gather: out[i] = row physical[i] (row_bytes, a multiple of

@@ -227,8 +227,12 @@ __global__ void __launch_bounds__(kPrologueThreads, 6) prologue_kernel(PrologueA
     } else {
       const int64_t t = j - q_groups - k_rows;
       uint4* h = reinterpret_cast<uint4*>(a.hist + t * kHistBins);
+      uint4* h2 = reinterpret_cast<uint4*>(a.hist2 + t * kHistBins);
 #pragma unroll 4
-      for (int b = lane; b < kHistBins / 4; b += 32) h[b] = make_uint4(0, 0, 0, 0);
+      for (int b = lane; b < kHistBins / 4; b += 32) {
+        h[b] = make_uint4(0, 0, 0, 0);
+        h2[b] = make_uint4(0, 0, 0, 0);
+      }
       if (lane == 0) reinterpret_cast<uint4*>(a.counters)[t] = make_uint4(0, 0, 0, 0);
     }
   }

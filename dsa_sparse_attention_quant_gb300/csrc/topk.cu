@@ -16,10 +16,10 @@
 //    that fit the launch's staging area are staged once in shared memory;
 //    longer rows are re-read from L2. Prefill rows run in 256-thread CTAs,
 //    several per SM; decode rows of up to 32768 scores in 1024-thread CTAs.
-//  * select_kernel: decode rows longer than that. Several CTAs per row place
-//    the keys above the boundary bin and collect the boundary bin's keys; the
-//    last CTA of the row to finish resolves the boundary bin on those
-//    candidates only.
+//  * select_kernel + resolve_kernel: decode rows longer than that. Several
+//    CTAs per row place the keys above the boundary bin and collect the
+//    boundary bin's keys with their next-level histogram; a second launch,
+//    one CTA per row, resolves the boundary bin on those candidates only.
 #include "select.cuh"
 
 namespace dsa {
@@ -226,11 +226,16 @@ cudaError_t launch_topk(const float* logits, int64_t ld, const int32_t* qsl, con
 }
 
 // ---------------------------------------------------------------------------
-// Multi-CTA select for decode rows: CTA (c, t) takes scores [c*chunk,
-// (c+1)*chunk) of row t. Pass 1 is the score kernel's histogram of the row,
-// so every chunk knows the boundary bin at once: it places its keys above the
-// bin (one global reservation per CTA) and its boundary-bin keys (as
-// candidates in global memory); the row's last CTA resolves the candidates.
+// Decode rows longer than one CTA stages: two launches. select_kernel: CTA
+// (c, t) takes scores [c*chunk, (c+1)*chunk) of row t. Pass 1 is the score
+// kernel's histogram of the row, so every chunk knows the boundary bin b1 at
+// once: it places its keys above b1 (one global reservation per CTA), appends
+// its b1 keys to the row's candidate list (another), and adds their next 11
+// bits to the row's second-level histogram. resolve_kernel, one CTA per row,
+// then finds the k-th key from that histogram (and, when its sub-bin is not
+// taken whole, a third level over the sub-bin's candidates) and places the
+// boundary keys. The kernel boundary replaces a completion counter and the
+// row's last CTA resolving on its own.
 // 1024 threads: the chain of dependent loads, scans and reservations is
 // latency-bound, and more threads per CTA keep more of each chunk's loads in
 // flight (decode8x128k step 49.8 us at 512, 47.3 at 1024, 56.1 at 256).
@@ -238,13 +243,11 @@ constexpr int kSelectThreads = 1024;
 
 __global__ void __launch_bounds__(kSelectThreads) select_kernel(SelectArgs a, PhysOut po, int chunk) {
   extern __shared__ __align__(16) uint32_t sh[];
-  uint32_t* hist = sh;              // kSelBins
+  uint32_t* hist = sh;              // kSelBins: pass 1, then this chunk's second-level histogram
   uint32_t* keys = sh + kSelBins;   // chunk: the chunk's keys
   uint32_t* ids = keys + chunk;     // chunk: its ids above the boundary bin, in order
-  uint2* cands = reinterpret_cast<uint2*>(keys);  // the finishing CTA: up to `chunk` candidates
   __shared__ SelState s;
   __shared__ uint32_t s_base_up, s_base_eq;
-  __shared__ int s_last;
 
   const int t = blockIdx.y;
   const int c = blockIdx.x;
@@ -299,7 +302,13 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(SelectArgs a, Ph
   __syncthreads();
   find_bin<kSelectThreads>(hist, static_cast<uint32_t>(a.topk), s);
   const uint32_t b1 = static_cast<uint32_t>(s.bin);
-  const uint32_t above = s.above;
+  if (c == 0 && tid == 0) {  // the boundary for the resolving launch
+    cnt[2] = b1;
+    cnt[3] = s.above;
+  }
+  // pass 1 is read (find_bin ends with a barrier): the array takes this
+  // chunk's second-level histogram
+  for (int b = tid; b < kSelBins; b += kSelectThreads) hist[b] = 0;
 
   // thread ranges of 4*q keys (q odd), one packed scan for the offsets
   int q4 = ((len + kSelectThreads - 1) / kSelectThreads + 3) >> 2;
@@ -339,6 +348,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(SelectArgs a, Ph
         if (bin > b1) {
           ids[p_up++] = static_cast<uint32_t>(lo + i + u);
         } else if (bin == b1) {
+          atomicAdd(&hist[(kk[u] >> 10) & (kSelBins - 1)], 1u);
           if (base_eq + p_eq < static_cast<uint32_t>(a.ld))
             crow[base_eq + p_eq] = make_uint2(kk[u], static_cast<uint32_t>(lo + i + u));
           ++p_eq;
@@ -347,33 +357,93 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(SelectArgs a, Ph
     }
   }
   __syncthreads();
-  // this chunk's ids above the bin, coalesced, at its reserved positions of the row
+  // this chunk's ids above the bin, coalesced, at its reserved positions of the
+  // row; its second-level counts added to the row's
   const uint32_t base_up = s_base_up;
   for (uint32_t j = tid; j < total_up; j += kSelectThreads)
     if (base_up + j < static_cast<uint32_t>(a.topk)) emit(o, base_up + j, static_cast<int>(ids[j]), &bad);
+  if (total_eq > 0) {
+    uint32_t* h2 = a.hist2 + static_cast<int64_t>(t) * kSelBins;
+    for (int b = tid; b < kSelBins; b += kSelectThreads)
+      if (hist[b]) atomicAdd(h2 + b, hist[b]);
+  }
+  if (bad) flag_error(po.err, DSA_DEVERR_ID_RANGE);
+}
 
-  // the last CTA of the row to finish resolves the boundary bin
-  __syncthreads();
+// One CTA per long decode row: the boundary keys, from the candidates and the
+// second-level histogram the chunk CTAs left. The row's candidates are staged
+// in shared memory when they fit (kCandCap), else read from the list.
+__global__ void __launch_bounds__(kSelectThreads) resolve_kernel(SelectArgs a, PhysOut po) {
+  __shared__ __align__(16) uint32_t hist[kSelBins];
+  __shared__ uint2 cands[kCandCap];
+  __shared__ SelState s;
+  const int t = blockIdx.x;
+  const int tid = threadIdx.x;
+  int r;
+  const int n = row_length(t, a.qsl, a.seq_lens, a.req_id, a.num_reqs, a.ld, &r);
+  const RowOut o = row_out(po, a.out, a.topk, t, r, a.num_reqs);
+  pdl_wait();  // the chunk CTAs' placements, candidates and counts
+  pdl_launch_dependents();
+  if (n <= a.topk) return;  // written whole by the row's first chunk
+  bool bad = false;
+  const uint32_t* cnt = a.counters + static_cast<int64_t>(t) * kRowCounters;
+  const uint2* crow = a.cand + static_cast<int64_t>(t) * a.ld;
+  const uint32_t b1 = __ldcg(cnt + 2), above = __ldcg(cnt + 3);
+  const uint32_t m = min(__ldcg(cnt + 1), static_cast<uint32_t>(a.ld));
+  const uint32_t need = static_cast<uint32_t>(a.topk) - above;  // 1 <= need <= m
+  const bool staged = m <= static_cast<uint32_t>(kCandCap);
+  const uint4* h2 = reinterpret_cast<const uint4*>(a.hist2 + static_cast<int64_t>(t) * kSelBins);
+  for (int b = tid; b < kSelBins / 4; b += kSelectThreads) reinterpret_cast<uint4*>(hist)[b] = __ldcg(h2 + b);
+  if (staged)
+    for (uint32_t j = tid; j < m; j += kSelectThreads) cands[j] = __ldcg(crow + j);
   if (tid == 0) {
-    __threadfence();
-    s_last = atomicAdd(&cnt[2], 1u) == static_cast<uint32_t>(chunks - 1);
-    if (s_last) __threadfence();
+    s.bin = 0;
+    s.above = 0;
+    s.cnt = above;
+    s.eq = 0;
   }
   __syncthreads();
-  if (s_last) {
-    const uint32_t m = min(__ldcg(&cnt[1]), static_cast<uint32_t>(a.ld));
-    const bool staged = m <= static_cast<uint32_t>(chunk);
-    if (staged) {
-      for (uint32_t j = tid; j < m; j += kSelectThreads) cands[j] = __ldcg(crow + j);
+  auto cand_at = [&](uint32_t j) -> uint2 { return staged ? cands[j] : __ldcg(crow + j); };
+  // take every candidate (level 1), every candidate whose next 11 bits are
+  // >= b2 (level 2), or every candidate above T and need3 equal to T (level 3)
+  int level = 1;
+  uint32_t lo2 = 0, T = 0, need3 = 0;
+  if (m != need) {
+    find_bin<kSelectThreads>(hist, need, s);
+    const uint32_t b2 = static_cast<uint32_t>(s.bin);
+    const uint32_t need2 = need - s.above;
+    const uint32_t p2 = (b1 << 11) | b2;  // the top 22 bits of the k-th key
+    lo2 = p2 << 10;
+    level = 2;
+    if (hist[b2] != need2) {
       __syncthreads();
+      for (int b = tid; b < kSelBins; b += kSelectThreads) hist[b] = 0;
+      if (tid == 0) {
+        s.bin = 0;
+        s.above = 0;
+      }
+      __syncthreads();
+      for (uint32_t j = tid; j < m; j += kSelectThreads) {
+        const uint32_t k = cand_at(j).x;
+        if ((k >> 10) == p2) atomicAdd(&hist[k & 1023u], 1u);
+      }
+      __syncthreads();
+      find_bin<kSelectThreads>(hist, need2, s);
+      T = lo2 | static_cast<uint32_t>(s.bin);
+      need3 = need2 - s.above;
+      level = 3;
     }
-    auto cand_at = [&](uint32_t j) -> uint2 { return staged ? cands[j] : __ldcg(crow + j); };
-    // hist still holds the row's pass 1: 1 <= need <= m
-    resolve_boundary<kSelectThreads>([&](uint32_t j) -> uint32_t { return cand_at(j).x; },
-                                     [&](uint32_t j) -> uint32_t { return cand_at(j).y; }, m, b1,
-                                     static_cast<uint32_t>(a.topk) - above, above, hist,
-                                     [&](uint32_t pos, uint32_t id) { emit(o, pos, static_cast<int>(id), &bad); },
-                                     a.topk, s);
+  }
+  for (uint32_t j0 = 0; j0 < m; j0 += kSelectThreads) {
+    const uint32_t j = j0 + tid;
+    const uint2 kv = j < m ? cand_at(j) : make_uint2(0u, 0u);
+    const bool in = j < m && (kv.x >> kHistShift) == b1;
+    const bool up = in && (level == 1 || (level == 2 ? kv.x >= lo2 : kv.x > T));
+    const bool tie = in && level == 3 && kv.x == T;
+    const uint32_t tq = warp_reserve(tie, &s.eq);
+    const bool take = up || (tie && tq < need3);
+    const uint32_t pos = warp_reserve(take, &s.cnt);
+    if (take && pos < static_cast<uint32_t>(a.topk)) emit(o, pos, static_cast<int>(kv.y), &bad);
   }
   if (bad) flag_error(po.err, DSA_DEVERR_ID_RANGE);
 }
@@ -387,9 +457,9 @@ cudaError_t launch_select(const SelectArgs& a, const TopkPhys* phys, int num_sms
   if (a.ld <= RowCfg<1024>::kStageMax)
     return launch_topk_rows<1024>(a.logits, a.ld, a.qsl, a.seq_lens, a.req_id, a.num_reqs, 0, a.n_rows, a.topk, a.out,
                                   phys, a.hist, a.n_rows, static_cast<int>((a.ld + 3) & ~3), stream);
-  // longer rows: chunks of the row in independent CTAs
-  // chunks of 1024..8192 scores, the smallest that keeps every row's chunks
-  // within about two CTAs per SM
+  // longer rows: chunks of the row in independent CTAs, then one CTA per row
+  // for the boundary; chunks of 1024..8192 scores, the smallest that keeps
+  // every row's chunks within about two CTAs per SM
   int chunk = 1024;
   while (chunk < 8192 && static_cast<int64_t>(a.n_rows) * a.ld / chunk > 2 * static_cast<int64_t>(num_sms)) chunk *= 2;
   const int max_smem = (kSelBins + 2 * 8192) * 4;
@@ -398,8 +468,10 @@ cudaError_t launch_select(const SelectArgs& a, const TopkPhys* phys, int num_sms
   if (e != cudaSuccess) return e;
   const int64_t chunks = (a.ld + chunk - 1) / chunk;
   dim3 grid(static_cast<unsigned>(chunks < 1 ? 1 : chunks), static_cast<unsigned>(a.n_rows));
-  return launch_pdl(select_kernel, grid, dim3(kSelectThreads), (kSelBins + 2 * chunk) * 4, stream, a, phys_out(phys),
-                    chunk);
+  const PhysOut po = phys_out(phys);
+  e = launch_pdl(select_kernel, grid, dim3(kSelectThreads), (kSelBins + 2 * chunk) * 4, stream, a, po, chunk);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(resolve_kernel, dim3(a.n_rows), dim3(kSelectThreads), 0, stream, a, po);
 }
 
 }  // namespace dsa

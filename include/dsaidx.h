@@ -268,7 +268,7 @@ DSA_API int dsa_set_launch_events(void *const *events, int32_t n_events);
  * allocating library call.
  *  - A batch whose dsa_indexer_workspace_size() exceeds
  *    DSA_STATIC_WORKSPACE_BYTES is rejected with DSA_ENOSPACE before any
- *    launch (32 MiB holds, e.g., 83 decode tokens at 32K context or 310 at
+ *    launch (32 MiB holds, e.g., 81 decode tokens at 32K context or 292 at
  *    8K: their score rows, histograms and boundary candidates).
  *  - The first call on a device looks up the array's device address (with
  *    that device current); make that first call before any stream capture.

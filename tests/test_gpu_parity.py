@@ -219,3 +219,17 @@ def test_decode_rows_ragged_lengths_one_cta_per_row():
     for seed, lens, k in ((17, [1000, 700, 600], 512), (18, [1500, 900], 1024), (19, [5000, 4097, 2100], 1024),
                           (20, [8000, 1100], 1024), (21, [32768, 20000, 7000, 64], 2048)):
         check_batch(synth.make_batch(seed, lens, [], k))
+
+
+def test_long_decode_rows_every_score_ties():
+    # decode rows past 32768 scores whose keys are all identical: the boundary
+    # bin holds the whole row, past the resolving CTA's staged candidates
+    hb = synth.make_batch(23, [40000, 33000], [], 2048)
+    first = {}
+    for i in range(hb.ctx_k.shape[0]):
+        r = 0 if i < 39999 else 1
+        first.setdefault(r, hb.ctx_k[i].copy())
+        hb.ctx_k[i] = first[r]
+    for t in range(hb.num_tokens):
+        hb.k_new[t] = first[t]
+    check_batch(hb)
