@@ -218,6 +218,7 @@ PrologueArgs plan_only(const DsaBatch* b, const IndexerWs& ws, int sms, const vo
   pa.hist2 = ws.hist2;
   pa.counters = ws.counters;
   pa.hist_rows = ws.hist_rows;
+  pa.num_sms = sms;
   pa.err = dev_err;
   return pa;
 }
@@ -267,19 +268,78 @@ int run_logits(const DsaBatch* b, const uint8_t* q_fp8, const float* w_folded, c
   return DSA_OK;
 }
 
+// A second stream of this host thread on one device, with its fork and join
+// events: the decode rows' select runs on it beside the prefill rows' top-k.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+thread_local SideStream t_side[kMaxDevices];
+
+// The side stream of the current device, created on first use (highest
+// priority, so the short select's CTAs are placed first), or nullptr: the
+// caller then launches both top-k kernels on its own stream. Not used while a
+// launch timeline is set (it times every kernel alone), and never created
+// while `stream` is being captured.
+SideStream* side_stream(cudaStream_t stream) {
+  if (t_count > 0) return nullptr;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  SideStream& ss = t_side[dev];
+  if (ss.stream != nullptr) return &ss;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  int least = 0, greatest = 0;
+  SideStream n;
+  if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
+      cudaStreamCreateWithPriority(&n.stream, cudaStreamNonBlocking, greatest) != cudaSuccess ||
+      cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&n.join, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();  // not sticky: fall back to one stream
+    if (n.join) cudaEventDestroy(n.join);
+    if (n.fork) cudaEventDestroy(n.fork);
+    if (n.stream) cudaStreamDestroy(n.stream);
+    return nullptr;
+  }
+  ss = n;
+  return &ss;
+}
+
 // Top-k of every row from scores built with the decode rows' histograms:
-// the decode rows by the multi-CTA select (chunks of each row in parallel,
-// pass 1 from the histograms), the others by one CTA per row.
+// the decode rows by the select (one CTA per row that fits its shared memory,
+// else chunk CTAs and a resolving CTA, pass 1 from the histograms), the
+// others by one CTA per row. The two read and write disjoint rows; with
+// `side`, when both are present, the select runs on the side stream (forked
+// from `stream` after the scores, joined back before return), beside the
+// prefill rows' top-k: its CTAs fill only as many SMs as there are decode rows.
 int run_topk(const DsaBatch* b, const IndexerWs& ws, int64_t ld, int32_t topk, int32_t* out, const TopkPhys* phys,
-             int sms, cudaStream_t stream) {
+             int sms, bool side, cudaStream_t stream) {
   SelectArgs sa{ws.logits, ld, b->query_start_loc, b->seq_lens, b->req_id_per_token, b->num_reqs,
                 ws.hist_rows, topk, out, ws.hist, ws.counters, ws.cand, ws.hist2};
+  const bool dec = ws.hist_rows > 0, pre = b->num_tokens > ws.hist_rows;
+  SideStream* ss = side && dec && pre ? side_stream(stream) : nullptr;
   int st = DSA_OK;
-  if (ws.hist_rows > 0 && (st = launched(launch_select(sa, phys, sms, stream), stream)) != DSA_OK) return st;
-  if (b->num_tokens > ws.hist_rows)
+  if (ss != nullptr) {
+    if ((st = from_cuda(cudaEventRecord(ss->fork, stream))) != DSA_OK) return st;
+    if ((st = from_cuda(cudaStreamWaitEvent(ss->stream, ss->fork, 0))) != DSA_OK) return st;
+    // from here on the side stream is joined back whatever fails
+    st = from_cuda(launch_select(sa, phys, sms, ss->stream));
+    const int r = from_cuda(cudaEventRecord(ss->join, ss->stream));
+    if (st == DSA_OK) st = r;
+  } else if (dec) {
+    st = launched(launch_select(sa, phys, sms, stream), stream);
+  }
+  if (pre && st == DSA_OK)
     st = launched(launch_topk(ws.logits, ld, b->query_start_loc, b->seq_lens, b->req_id_per_token, b->num_reqs,
                               ws.hist_rows, b->num_tokens, topk, out, phys, nullptr, 0, stream),
                   stream);
+  if (ss != nullptr) {
+    const int j = from_cuda(cudaStreamWaitEvent(stream, ss->join, 0));
+    if (st == DSA_OK) st = j;
+  }
   return st;
 }
 
@@ -487,7 +547,7 @@ int dsa_indexer_logits_topk(const DsaBatch* batch, const uint8_t* q_fp8, const f
   const int64_t ld = logits_ld(batch);
   st = run_logits(batch, q_fp8, w_folded, k_cache, w.logits, ld, w, true, dev_err, stream);
   if (st != DSA_OK) return st;
-  return run_topk(batch, w, ld, topk, topk_out, nullptr, sms, stream);
+  return run_topk(batch, w, ld, topk, topk_out, nullptr, sms, false, stream);
 }
 
 int dsa_topk_logical_to_physical(const int32_t* logical, int64_t n_tokens, int32_t topk,
@@ -615,7 +675,7 @@ int dsa_layer_stack_run(const DsaStackPlan* plan, const DsaBatch* batch, const i
                     plan->block_stride_rows > 0 ? plan->block_stride_rows : kBlock, phys_buf, valid_buf, dev_err};
         st = run_logits(batch, q8, wf, L.k_cache, w.logits, ld, w, true, dev_err, stream);
         if (st != DSA_OK) return st;
-        st = run_topk(batch, w, ld, plan->topk, topk_buf, &tp, sms, stream);
+        st = run_topk(batch, w, ld, plan->topk, topk_buf, &tp, sms, true, stream);
         if (st != DSA_OK) return st;
       }
     }

@@ -122,6 +122,31 @@ __device__ __forceinline__ uint32_t quant_row_lane(uint2 raw, float* scale_out) 
   return e4m3x4(f0.x * inv, f0.y * inv, f1.x * inv, f1.y * inv);
 }
 
+// The same quantiser on half a warp: lanes 16h..16h+15 hold one row, lane i of
+// the half values 8i..8i+7 (one 16-byte load), so a warp load moves two rows.
+// Returns this lane's 8 codes (first value in the lowest byte) and the row's
+// scale.
+__device__ __forceinline__ uint2 quant_row_half(uint4 raw, float* scale_out) {
+  const uint32_t wd[4] = {raw.x, raw.y, raw.z, raw.w};
+  float f[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wd[k]));
+    f[2 * k] = p.x;
+    f[2 * k + 1] = p.y;
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(f[k]));
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));  // within the half
+  const float s = ue8m0_scale(amax);
+  const float inv = pow2_reciprocal(s);
+  *scale_out = s;
+  return make_uint2(e4m3x4(f[0] * inv, f[1] * inv, f[2] * inv, f[3] * inv),
+                    e4m3x4(f[4] * inv, f[5] * inv, f[6] * inv, f[7] * inv));
+}
+
 // Four fp32 values -> four E2M1 codes (nearest-even, saturating), first value
 // in the lowest nibble.
 __device__ __forceinline__ uint32_t e2m1x4(float a, float b, float c, float d) {
@@ -190,6 +215,39 @@ __device__ __forceinline__ uint2 rope_row_lane(uint2 raw, const float* cs) {
   }
   const __nv_bfloat162 lo = __floats2bfloat162_rn(r[0], r[1]), hi = __floats2bfloat162_rn(r[2], r[3]);
   return make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+}
+
+// rope_row_lane for the half-warp layout of quant_row_half: dim i < 32 sits on
+// lane i/8 of the half and pairs with dim i + 32 on lane i/8 + 4; the same
+// rounding (each product and sum in fp32, the result to bf16). All lanes must
+// call.
+__device__ __forceinline__ uint4 rope_row_half(uint4 raw, const float* cs) {
+  const int hl = threadIdx.x & 15;
+  const uint32_t ow[4] = {__shfl_xor_sync(0xffffffffu, raw.x, 4), __shfl_xor_sync(0xffffffffu, raw.y, 4),
+                          __shfl_xor_sync(0xffffffffu, raw.z, 4), __shfl_xor_sync(0xffffffffu, raw.w, 4)};
+  if (hl >= 8) return raw;  // dims 64..127 are not rotated
+  const int i0 = 8 * (hl & 3);
+  const float4 c0 = __ldg(reinterpret_cast<const float4*>(cs + i0));
+  const float4 c1 = __ldg(reinterpret_cast<const float4*>(cs + i0 + 4));
+  const float4 s0 = __ldg(reinterpret_cast<const float4*>(cs + 32 + i0));
+  const float4 s1 = __ldg(reinterpret_cast<const float4*>(cs + 36 + i0));
+  const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+  const uint32_t wd[4] = {raw.x, raw.y, raw.z, raw.w};
+  uint32_t out[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    // lanes 0-3 hold x[i] (partner x[i+32]); lanes 4-7 hold x[i+32] (partner x[i])
+    const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wd[k]));
+    const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[k]));
+    const float a0 = __fmul_rn(x.x, cc[2 * k]), b0 = __fmul_rn(y.x, ss[2 * k]);
+    const float a1 = __fmul_rn(x.y, cc[2 * k + 1]), b1 = __fmul_rn(y.y, ss[2 * k + 1]);
+    const float r0 = hl < 4 ? __fsub_rn(a0, b0) : __fadd_rn(a0, b0);
+    const float r1 = hl < 4 ? __fsub_rn(a1, b1) : __fadd_rn(a1, b1);
+    const __nv_bfloat162 p = __floats2bfloat162_rn(r0, r1);
+    out[k] = *reinterpret_cast<const uint32_t*>(&p);
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
 // The row of the cos/sin table for a position, or nullptr (no rotation:

@@ -110,6 +110,7 @@ struct PrologueArgs {
   uint32_t* hist2;     // zeroed here for the select: [hist_rows][kHistBins]
   uint32_t* counters;  // [hist_rows][kRowCounters]
   int hist_rows;
+  int num_sms;         // SMs of the device: the grid is one wave
   int32_t* err;
 };
 

@@ -147,18 +147,21 @@ __device__ void plan_batch(const PlanArgs& p, PlanSmem& S) {
 // ---------------------------------------------------------------------------
 // One launch per F layer before the scores: CTA 0 plans (first layer of a
 // step only; being first it is dispatched first and overlaps the rest); the
-// others quantise the step's K into the cache and the q rows with the weight
-// fold, one warp per 128-value row, and zero the decode rows' score
-// histograms and top-k counters.
-// 256 threads and at most 40 registers a thread, and the plan's staging in
-// dynamic shared memory (requested only when there is a plan), so prologue
-// CTAs fit beside a score-kernel CTA that starts early on the same SM.
+// others quantise the q rows with the weight fold (half a warp per 128-value
+// row: 16-byte loads, eight rows per warp in flight), the step's K into the
+// cache (a warp per row), and zero the decode rows' score histograms and
+// top-k counters. One wave: the grid is the CTAs that fit on the GPU at once
+// (five per SM at 256 threads and at most 48 registers), each looping over its
+// share. Against a warp per q row (8-byte loads, four rows per warp) and two
+// waves, prefill4x8k's prologue took 219 -> 136 us (HBM-bound: 837 MB moved,
+// 0.91 of the measured copy bandwidth).
 constexpr int kPrologueThreads = 256;
+constexpr int kPrologueMinCtas = 5;
 
 // FP4: the K cache has FP4 pages (a.k_fp4), fixed per instance so that the
 // K store of the other format costs no registers.
 template <bool FP4>
-__global__ void __launch_bounds__(kPrologueThreads, 6) prologue_kernel(PrologueArgs a) {
+__global__ void __launch_bounds__(kPrologueThreads, kPrologueMinCtas) prologue_kernel(PrologueArgs a) {
   extern __shared__ __align__(16) uint8_t plan_smem[];
   pdl_launch_dependents();  // the score kernel may start its set-up now
   if (a.plan && blockIdx.x == 0) {
@@ -172,43 +175,46 @@ __global__ void __launch_bounds__(kPrologueThreads, 6) prologue_kernel(PrologueA
   const int64_t q_rows = a.q != nullptr ? static_cast<int64_t>(a.n_tokens) * kHeads : 0;
   const int64_t k_rows = a.k_new != nullptr ? a.n_tokens : 0;
   const int64_t z_rows = a.hist != nullptr ? a.hist_rows : 0;
-  // jobs: groups of 4 q rows (their loads are issued together), then K rows, then zeroing
-  constexpr int kGroup = 4;
+  // jobs: groups of 8 q rows (two rows per 16-byte load of the warp, four
+  // loads issued together), then K rows, then zeroing
+  constexpr int kGroup = 8;
+  const int half = lane >> 4, hl = lane & 15;
   static_assert(kHeads % kGroup == 0, "a group of q rows belongs to one token");
   const int64_t q_groups = (q_rows + kGroup - 1) / kGroup;
   const int64_t jobs = q_groups + k_rows + z_rows;
   for (int64_t j = static_cast<int64_t>(blockIdx.x - first) * (kPrologueThreads / 32) + (threadIdx.x >> 5); j < jobs;
        j += warps) {
     if (j < q_groups) {
+      // q_rows is a multiple of 64: every group is whole and heads of one token
       const int64_t r0 = j * kGroup;
-      uint2 raw[kGroup];
-      float wv[kGroup];
+      constexpr int kLoads = kGroup / 2;
+      uint4 raw[kLoads];
+      float wv[kLoads];
 #pragma unroll
-      for (int u = 0; u < kGroup; ++u) {
-        const int64_t r = r0 + u;
-        raw[u] = r < q_rows ? __ldg(reinterpret_cast<const uint2*>(a.q + r * kDim) + lane) : make_uint2(0, 0);
+      for (int u = 0; u < kLoads; ++u) {
+        const int64_t r = r0 + 2 * u + half;
+        raw[u] = __ldg(reinterpret_cast<const uint4*>(a.q + r * kDim) + hl);
         wv[u] = 0.0f;
-        if (lane == 0 && r < q_rows) {  // w[token][head]: row r is head r % 64 of token r / 64
+        if (hl == 0) {  // w[token][head]: row r is head r % 64 of token r / 64
           const int64_t wi = (r / kHeads) * a.w_row_stride + (r % kHeads);
           wv[u] = a.w_bf16 ? __bfloat162float(__ldg(static_cast<const __nv_bfloat16*>(a.w) + wi))
                            : __ldg(static_cast<const float*>(a.w) + wi);
         }
       }
-      if (a.rope.cos_sin != nullptr) {  // the group's rows are heads of one token (64 % kGroup == 0)
+      if (a.rope.cos_sin != nullptr) {
         const float* cs = rope_row(a.rope, r0 / kHeads, a.err, lane);
         if (cs != nullptr) {
 #pragma unroll
-          for (int u = 0; u < kGroup; ++u) raw[u] = rope_row_lane(raw[u], cs);
+          for (int u = 0; u < kLoads; ++u) raw[u] = rope_row_half(raw[u], cs);
         }
       }
 #pragma unroll
-      for (int u = 0; u < kGroup; ++u) {
-        const int64_t r = r0 + u;
-        if (r >= q_rows) break;  // warp-uniform
+      for (int u = 0; u < kLoads; ++u) {
+        const int64_t r = r0 + 2 * u + half;
         float s;
-        const uint32_t codes = quant_row_lane(raw[u], &s);
-        reinterpret_cast<uint32_t*>(a.q_fp8 + r * kDim)[lane] = codes;
-        if (lane == 0) a.w_folded[r] = __fmul_rn(__fmul_rn(__fmul_rn(wv[u], s), a.softmax_scale), 0.125f);
+        const uint2 codes = quant_row_half(raw[u], &s);
+        reinterpret_cast<uint2*>(a.q_fp8 + r * kDim)[hl] = codes;
+        if (hl == 0) a.w_folded[r] = __fmul_rn(__fmul_rn(__fmul_rn(wv[u], s), a.softmax_scale), 0.125f);
       }
     } else if (j < q_groups + k_rows) {
       const int64_t t = j - q_groups;
@@ -238,13 +244,31 @@ __global__ void __launch_bounds__(kPrologueThreads, 6) prologue_kernel(PrologueA
   }
 }
 
+// Prologue CTAs resident on one SM (the occupancy of the instance, with the
+// plan's shared memory), found once.
+template <bool FP4>
+int prologue_resident() {
+  static const int n = [] {
+    int r = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r, prologue_kernel<FP4>, kPrologueThreads, sizeof(PlanSmem)) !=
+        cudaSuccess) {
+      cudaGetLastError();  // not sticky; leave no error for the launch check
+      r = 0;
+    }
+    return r < 1 ? kPrologueMinCtas : r;
+  }();
+  return n;
+}
+
 cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t stream) {
   if (a.plan && (a.p.grid < 1 || a.p.grid > kMaxCtas)) return cudaErrorInvalidValue;
-  const int64_t q_groups = a.q != nullptr ? (static_cast<int64_t>(a.n_tokens) * kHeads + 3) / 4 : 0;
+  const int64_t q_groups = a.q != nullptr ? (static_cast<int64_t>(a.n_tokens) * kHeads + 7) / 8 : 0;
   const int64_t jobs = q_groups + (a.k_new != nullptr ? a.n_tokens : 0) + (a.hist != nullptr ? a.hist_rows : 0);
   int64_t quant = (jobs + kPrologueThreads / 32 - 1) / (kPrologueThreads / 32);  // one job per warp, if it fits
   if (quant < 1) quant = 1;
-  if (quant > 1216) quant = 1216;  // one wave of 8 CTAs per SM; the rest loops
+  const int64_t wave = static_cast<int64_t>(a.num_sms > 0 ? a.num_sms : 1) *
+                           (a.k_fp4 ? prologue_resident<true>() : prologue_resident<false>()) - (a.plan ? 1 : 0);
+  if (quant > wave) quant = wave > 1 ? wave : 1;  // every CTA resident at once; the rest loops
   const size_t smem = a.plan ? sizeof(PlanSmem) : 0;
   static_assert(sizeof(PlanSmem) <= 48 * 1024, "plan staging fits the default dynamic shared memory");
   const unsigned grid = static_cast<unsigned>(quant + (a.plan ? 1 : 0));

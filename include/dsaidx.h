@@ -348,7 +348,15 @@ DSA_API int dsa_gather_rows(const uint8_t *rows, int64_t num_rows, int64_t row_b
  * the group's buffers, in layer order, after that layer's device work is
  * queued on `stream`; it may enqueue its own work on the stream (the sparse
  * attention that reads the indices). 'S' layers own no indexer inputs: their
- * entries of `layers` are ignored and may be zero. */
+ * entries of `layers` are ignored and may be zero.
+ * Streams: with decode and prefill rows in the batch, the decode rows' top-k
+ * runs on a second stream of the calling host thread (created on the first
+ * such call, outside stream capture; highest priority), forked from `stream`
+ * after the scores and joined back to it before the layer's consumer call,
+ * so every later operation on `stream` sees the layer's complete output. In
+ * stream capture the fork and join become graph edges. Without that second
+ * stream (capture before the first such call, or a launch timeline set by
+ * dsa_set_launch_events) both run on `stream`. */
 #define DSA_W_FP32 0
 #define DSA_W_BF16 1
 typedef struct DsaLayerInputs {
