@@ -112,11 +112,19 @@ struct QMeta {
 // *first_new = position of the request's first token of this step: pages
 // below first_new / 64 hold no slot written in this step.
 __device__ __forceinline__ int decode_block(const LogitsArgs& a, int t, QBlock* out, int* first_new = nullptr) {
+  // one token per decode request is the common case (request t): its
+  // metadata is loaded beside req_id[t] instead of after it
   const int r = __ldg(a.req_id + t);
+  const bool spec = t < a.num_decodes;
+  int q0 = spec ? __ldg(a.qsl + t) : 0, q1 = spec ? __ldg(a.qsl + t + 1) : 0, sl = spec ? __ldg(a.seq_lens + t) : 0;
   QBlock b{r, t, 1, 0};
   int tiles = 0, fn = 0;
   if (r >= 0 && r < a.num_decodes) {
-    const int q0 = __ldg(a.qsl + r), q1 = __ldg(a.qsl + r + 1), sl = __ldg(a.seq_lens + r);
+    if (r != t) {
+      q0 = __ldg(a.qsl + r);
+      q1 = __ldg(a.qsl + r + 1);
+      sl = __ldg(a.seq_lens + r);
+    }
     if (t >= q0 && t < q1 && sl >= q1 - q0 && static_cast<int64_t>(sl) <= a.bt_stride * kBlock) {
       fn = sl - (q1 - q0);
       b.p0 = fn + (t - q0);
