@@ -744,6 +744,10 @@ def run_stack(args, ranks: Ranks, with_cpu: bool):
     phys = torch.empty((T, k), dtype=torch.int32, device=dev)
     valid = torch.empty(T, dtype=torch.int32, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
+    # the batch carries its work (decode keys, prefill pairs) from the host
+    # metadata: in the step, each F layer scores the decode rows on this many
+    # SMs beside the prefill rows on the rest
+    dec_sms = dsa.LayerStack(batch, fs4, l4, k, topk_buf=topk, phys_buf=phys, valid_buf=valid, ws=ws).decode_sms()
 
     def run(fs, L, ev=None):
         if ev is not None:
@@ -874,7 +878,8 @@ def run_stack(args, ranks: Ranks, with_cpu: bool):
     roofline = dict(phases[dom])
     roofline.update({"phases": phases, "dominant_phase": dom,
                      "timing": "CUDA events on the launching stream around each kernel of one F layer (a one-layer "
-                               "stack replayed alone), averaged over K layers"})
+                               "stack replayed alone), averaged over K layers; each kernel alone on the whole GPU "
+                               "(the launch timeline turns the decode/prefill SM split off)"})
     line = {
         "metric": METRIC,
         "value": whole_job_rate(pairs, world, ms4 / 1e3),
@@ -892,6 +897,10 @@ def run_stack(args, ranks: Ranks, with_cpu: bool):
         "config": workload_config("stack61", meta, args, world),
         "indexcache": {"freq4_ms_per_step": ms4, "freq1_ms_per_step": ms1, "freq4_speedup_vs_freq1": ms1 / ms4,
                        "f_layer_ms_in_step": ms4 / n_f},
+        "sm_split": {"decode_score_sms": dec_sms, "prefill_score_sms": torch.cuda.get_device_properties(dev)
+                     .multi_processor_count - dec_sms if dec_sms else None,
+                     "note": "in the step each F layer scores its decode rows on decode_score_sms SMs beside its "
+                             "prefill rows on the rest (two streams), each segment's top-k after its scores"},
         "roofline": roofline,
         "breakdown_us": {kname: v * 1e3 for kname, v in ms.items()},
         "e2e": {"value": whole_job_rate(pairs, world, e2e_s), "unit": "pairs/s", "h2d_bytes_per_step": h2d,

@@ -13,6 +13,8 @@ import math
 import os
 import threading
 
+import numpy as np
+
 import torch
 
 from . import build as _build
@@ -37,7 +39,7 @@ SYMBOLS = [
     "dsa_indexer_workspace_size", "dsa_indexer_logits_topk",
     "dsa_indexer_plan", "dsa_indexer_logits", "dsa_indexer_topk",
     "dsa_topk_logical_to_physical", "dsa_schedule_build",
-    "dsa_layer_stack_workspace_size", "dsa_layer_stack_run",
+    "dsa_layer_stack_workspace_size", "dsa_layer_stack_run", "dsa_layer_stack_decode_sms",
     "dsa_indexer_logits_topk_static", "dsa_set_launch_events",
     "dsa_indexer_k_rope_quant_write", "dsa_indexer_q_rope_quant_fold", "dsa_gather_rows",
     "dsa_indexer_k_quant_write_fp4", "dsa_selftest_wait_timeout",
@@ -93,6 +95,8 @@ class DsaStackPlanC(ctypes.Structure):
         ("positions", ctypes.c_void_p),
         ("rope_cos_sin", ctypes.c_void_p),
         ("rope_max_pos", ctypes.c_int64),
+        ("decode_keys", ctypes.c_int64),
+        ("prefill_pairs", ctypes.c_int64),
     ]
 
 
@@ -132,6 +136,7 @@ def load(build_if_missing: bool = True):
             "dsa_layer_stack_run": (ctypes.c_int, [ctypes.POINTER(DsaStackPlanC), BP, P, P, P, P, CONSUMER_FN, P, P,
                                                    SZ, P, P]),
             "dsa_indexer_logits_topk_static": (ctypes.c_int, [BP, P, P, P, I32, P, P, P, P, P]),
+            "dsa_layer_stack_decode_sms": (ctypes.c_int, [ctypes.POINTER(DsaStackPlanC), BP, P]),
             "dsa_set_launch_events": (ctypes.c_int, [P, I32]),
             "dsa_indexer_k_rope_quant_write": (ctypes.c_int, [P, I64, I64, P, P, I64, P, P, I64, P, P]),
             "dsa_indexer_k_quant_write_fp4": (ctypes.c_int, [P, I64, I64, P, P, I64, P, P, I64, P, P]),
@@ -197,19 +202,34 @@ class Batch:
         if num_decode_tokens is None:
             num_decode_tokens = int(query_start_loc[self.num_decodes].item()) if self.num_reqs else 0
         self.num_decode_tokens = int(num_decode_tokens)
+        self.work = (0, 0)  # (decode_keys, prefill_pairs) when known on the host; see work_from_host
         self.c = DsaBatchC(self.num_reqs, self.num_decodes, self.num_decode_tokens, self.num_tokens, self.max_seq_len,
                            int(block_table.shape[1]) if block_table.dim() == 2 else 1, self.num_blocks,
                            query_start_loc.data_ptr(), seq_lens.data_ptr(), block_table.data_ptr(),
                            req_id_per_token.data_ptr())
+
+    @staticmethod
+    def work_from_host(query_start_loc, seq_lens, num_decodes: int):
+        """(decode_keys, prefill_pairs) of a step from host copies of its
+        metadata: the sums over the decode and the prefill tokens of the keys
+        each token sees (position + 1), as ``DsaStackPlan`` takes them."""
+        qsl = np.asarray(query_start_loc, dtype=np.int64)
+        sl = np.asarray(seq_lens, dtype=np.int64)
+        ql = qsl[1:] - qsl[:-1]
+        # a request of ql tokens ending at length sl: its tokens see sl - ql + 1 .. sl keys
+        per_req = ql * (sl - ql) + ql * (ql + 1) // 2
+        return int(per_req[:num_decodes].sum()), int(per_req[num_decodes:].sum())
 
     @classmethod
     def from_host(cls, hb, device="cuda"):
         """From a ``synth.Batch`` (numpy metadata) to device tensors."""
         def d(a):
             return torch.from_numpy(a.astype("int32")).to(device)
-        return cls(d(hb.query_start_loc), d(hb.seq_lens), d(hb.block_table), d(hb.req_id_per_token),
-                   hb.num_decodes, hb.num_blocks, int(hb.seq_lens.max()) if hb.num_reqs else 1,
-                   int(hb.query_start_loc[hb.num_decodes]) if hb.num_reqs else 0)
+        b = cls(d(hb.query_start_loc), d(hb.seq_lens), d(hb.block_table), d(hb.req_id_per_token),
+                hb.num_decodes, hb.num_blocks, int(hb.seq_lens.max()) if hb.num_reqs else 1,
+                int(hb.query_start_loc[hb.num_decodes]) if hb.num_reqs else 0)
+        b.work = cls.work_from_host(hb.query_start_loc, hb.seq_lens, hb.num_decodes)
+        return b
 
 
 def selftest_wait_timeout(dev_err, stream=None):
@@ -500,11 +520,18 @@ class LayerStack:
     launches). The graph reads and writes the same buffers, so a step's new
     inputs go into them before ``run()``; metadata that sizes the launch (the
     batch's lengths) must not change. A graphed stack takes no consumer (a
-    host callback would run at capture only)."""
+    host callback would run at capture only).
+
+    ``work`` = (decode_keys, prefill_pairs), the step's keys seen by its decode
+    tokens and by its prefill tokens (``Batch.work_from_host``); by default the
+    batch's own, known when it was built from host metadata. With both given,
+    each F layer scores the decode rows on a share of the SMs beside the
+    prefill rows (``DsaStackPlan.decode_keys``); (0, 0) keeps one after the
+    other."""
 
     def __init__(self, batch: Batch, fs: str, layers, topk: int, slot_mapping=None, topk_buf=None, phys_buf=None,
                  valid_buf=None, consumer=None, ws=None, softmax_scale: float = 0.0, block_stride_rows: int = 0,
-                 dev_err=None, positions=None, rope_cos_sin=None, graphed: bool = False):
+                 dev_err=None, positions=None, rope_cos_sin=None, graphed: bool = False, work=None):
         if graphed and consumer is not None:
             raise DsaError("a graphed LayerStack takes no consumer: a host callback runs only at capture")
         self._graphed = bool(graphed)
@@ -527,9 +554,10 @@ class LayerStack:
             max_pos = _rope_table(rope_cos_sin)
             _need(positions, torch.int64, "positions")
         self._fs = fs.encode()
+        decode_keys, prefill_pairs = batch.work if work is None else work
         self._plan = DsaStackPlanC(n, self._fs, self._arr, int(topk), float(softmax_scale), int(block_stride_rows),
                                    _ptr(positions) if rope_cos_sin is not None else None, _ptr(rope_cos_sin),
-                                   max_pos)
+                                   max_pos, int(decode_keys), int(prefill_pairs))
         dev = torch.device("cuda", torch.cuda.current_device())
         T = batch.num_tokens
         self.topk_buf = topk_buf if topk_buf is not None else torch.empty((T, int(topk)), dtype=torch.int32,
@@ -546,6 +574,14 @@ class LayerStack:
         self._args = (ctypes.byref(self._plan), ctypes.byref(batch.c), _ptr(slot_mapping), _ptr(self.topk_buf),
                       _ptr(self.phys_buf), _ptr(self.valid_buf), self._cb, None, _ptr(self.ws), self.ws.numel(),
                       _ptr(dev_err))
+
+    def decode_sms(self) -> int:
+        """SMs each F layer gives the decode rows' scores beside the prefill
+        rows' (0: one after the other)."""
+        out = ctypes.c_int32(0)
+        _check(load().dsa_layer_stack_decode_sms(ctypes.byref(self._plan), self._args[1], ctypes.byref(out)),
+               "dsa_layer_stack_decode_sms")
+        return int(out.value)
 
     def run(self, stream=None):
         s = stream if stream is not None else torch.cuda.current_stream()
@@ -569,7 +605,7 @@ class LayerStack:
 
 def layer_stack_run(batch: Batch, fs: str, layers, topk: int, slot_mapping=None, topk_buf=None, phys_buf=None,
                     valid_buf=None, consumer=None, ws=None, softmax_scale: float = 0.0, block_stride_rows: int = 0,
-                    dev_err=None, stream=None, positions=None, rope_cos_sin=None):
+                    dev_err=None, stream=None, positions=None, rope_cos_sin=None, work=None):
     """Run a stack of layers once (see ``LayerStack`` for the arguments)."""
     return LayerStack(batch, fs, layers, topk, slot_mapping, topk_buf, phys_buf, valid_buf, consumer, ws,
-                      softmax_scale, block_stride_rows, dev_err, positions, rope_cos_sin).run(stream)
+                      softmax_scale, block_stride_rows, dev_err, positions, rope_cos_sin, work=work).run(stream)

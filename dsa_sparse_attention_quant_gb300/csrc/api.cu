@@ -194,14 +194,16 @@ IndexerWs carve(const DsaBatch* b, void* base) {
   return w;
 }
 
-PlanArgs plan_args(const DsaBatch* b, const IndexerWs& ws, int sms, int32_t* dev_err) {
-  return PlanArgs{b->query_start_loc, b->seq_lens,    b->num_reqs,    b->num_decodes, b->num_decode_tokens,
-                  b->num_tokens,      b->bt_stride,   grid_ctas(sms), ws.pre,         dev_err};
+// The prefill plan for a score kernel of pre_grid CTAs.
+PlanArgs plan_args(const DsaBatch* b, const IndexerWs& ws, int pre_grid, int32_t* dev_err) {
+  return PlanArgs{b->query_start_loc, b->seq_lens,    b->num_reqs, b->num_decodes, b->num_decode_tokens,
+                  b->num_tokens,      b->bt_stride,   pre_grid,    ws.pre,         dev_err};
 }
 
 // Prologue with no q: (optional) K quant + cache write, the prefill plan (when
-// the batch has prefill requests), and zeroed decode-row histograms and counters.
-PrologueArgs plan_only(const DsaBatch* b, const IndexerWs& ws, int sms, const void* k_new,
+// the batch has prefill requests) for a prefill score kernel of pre_grid CTAs,
+// and zeroed decode-row histograms and counters.
+PrologueArgs plan_only(const DsaBatch* b, const IndexerWs& ws, int sms, int pre_grid, const void* k_new,
                        const int64_t* slot_mapping, uint8_t* k_cache, int32_t* dev_err) {
   PrologueArgs pa{};
   pa.k_new = static_cast<const __nv_bfloat16*>(k_new);
@@ -213,7 +215,7 @@ PrologueArgs plan_only(const DsaBatch* b, const IndexerWs& ws, int sms, const vo
   pa.k_fp4 = kcache_fp4(b);
   pa.n_tokens = b->num_tokens;
   pa.plan = b->num_reqs > b->num_decodes;
-  pa.p = plan_args(b, ws, sms, dev_err);
+  pa.p = plan_args(b, ws, pre_grid, dev_err);
   pa.hist = ws.hist;
   pa.hist2 = ws.hist2;
   pa.counters = ws.counters;
@@ -336,6 +338,75 @@ int run_topk(const DsaBatch* b, const IndexerWs& ws, int64_t ld, int32_t topk, i
     st = launched(launch_topk(ws.logits, ld, b->query_start_loc, b->seq_lens, b->req_id_per_token, b->num_reqs,
                               ws.hist_rows, b->num_tokens, topk, out, phys, nullptr, 0, stream),
                   stream);
+  if (ss != nullptr) {
+    const int j = from_cuda(cudaStreamWaitEvent(stream, ss->join, 0));
+    if (st == DSA_OK) st = j;
+  }
+  return st;
+}
+
+// Per-SM rates of the score kernels on GB300, measured: a decode CTA's K-tile
+// pipeline takes about 0.34 us per 128-key tile whatever the number of CTAs
+// (decode8x128k on 40 to 100 SMs: 47-50 GB/s per SM), and on the whole GPU
+// the shared HBM holds it to about 0.40 us; the prefill kernel scores about
+// 730-890 pairs per us per SM (stack61, prefill4x8k).
+constexpr double kDecodeKeysPerSmUs = 376.0;
+constexpr double kPrefillPairsPerSmUs = 800.0;
+constexpr int kMinSplitSms = 16;
+
+// SMs for the decode rows' scores when they run beside the prefill rows'
+// scores, or 0 (one after the other): the share that makes both take the same
+// time at the rates above. The decode kernel on the whole GPU is bound by HBM
+// at about 35 GB/s per SM, so a share streams K at nearly the HBM rate of the
+// whole GPU's while the other SMs compute the prefill: stack61 (64 decodes at
+// 32768 keys, a 4096-token prefill, 53 of 152 SMs) 211 -> 193 us per F layer.
+int decode_split(const DsaStackPlan* plan, const DsaBatch* b, int sms) {
+  if (t_count > 0) return 0;  // a launch timeline times every kernel alone, on the whole GPU
+  if (plan->decode_keys <= 0 || plan->prefill_pairs <= 0 || b->num_decodes == 0 || b->num_reqs == b->num_decodes)
+    return 0;
+  const double wd = static_cast<double>(plan->decode_keys) / kDecodeKeysPerSmUs;
+  const double wp = static_cast<double>(plan->prefill_pairs) / kPrefillPairsPerSmUs;
+  const int s = static_cast<int>(sms * wd / (wd + wp) + 0.5);
+  return (s < kMinSplitSms || s > sms - kMinSplitSms || sms - s > kMaxCtas) ? 0 : s;
+}
+
+// One F layer's scores and top-k with the SMs split: the decode rows' scores
+// (split CTAs) and select on the side stream, the prefill rows' scores (the
+// rest, as planned) and top-k on `stream`, joined back before return. Without
+// a side stream (stream capture before its first use) the same launches run
+// one after the other on `stream`.
+int run_split(const DsaBatch* b, const uint8_t* q_fp8, const float* w_folded, const uint8_t* k_cache,
+              const IndexerWs& ws, int64_t ld, int32_t topk, int32_t* out, const TopkPhys* phys, int sms, int split,
+              int32_t* dev_err, cudaStream_t stream) {
+  CUtensorMap mk, mq1, mq4;
+  const bool fp4 = kcache_fp4(b);
+  int st;
+  if ((st = make_kcache_map(&mk, k_cache, b->num_blocks, fp4)) != DSA_OK) return st;
+  if ((st = make_q_map(&mq1, q_fp8, b->num_tokens, kHeads)) != DSA_OK) return st;
+  if ((st = make_q_map(&mq4, q_fp8, b->num_tokens, kPrefillTok * kHeads)) != DSA_OK) return st;
+  LogitsArgs a{w_folded,          k_cache,     b->block_table,       b->bt_stride,   b->num_blocks,
+               ws.logits,         ld,          ws.hist,              ws.hist_rows,
+               b->query_start_loc, b->seq_lens, b->req_id_per_token, b->num_decodes, b->num_decode_tokens,
+               dev_err};
+  SelectArgs sa{ws.logits, ld, b->query_start_loc, b->seq_lens, b->req_id_per_token, b->num_reqs,
+                ws.hist_rows, topk, out, ws.hist, ws.counters, ws.cand, ws.hist2};
+  SideStream* ss = side_stream(stream);
+  cudaStream_t ds = ss != nullptr ? ss->stream : stream;
+  if (ss != nullptr) {
+    if ((st = from_cuda(cudaEventRecord(ss->fork, stream))) != DSA_OK) return st;
+    if ((st = from_cuda(cudaStreamWaitEvent(ss->stream, ss->fork, 0))) != DSA_OK) return st;
+  }
+  // from here on the side stream is joined back whatever fails
+  st = from_cuda(launch_logits(1, fp4, &mk, &mq1, SegmentPlan{}, a, split, ds));
+  if (st == DSA_OK) st = from_cuda(launch_select(sa, phys, sms, ds));
+  if (ss != nullptr) {
+    const int r = from_cuda(cudaEventRecord(ss->join, ss->stream));
+    if (st == DSA_OK) st = r;
+  }
+  if (st == DSA_OK) st = from_cuda(launch_logits(kPrefillTok, fp4, &mk, &mq4, ws.pre, a, sms - split, stream));
+  if (st == DSA_OK)
+    st = from_cuda(launch_topk(ws.logits, ld, b->query_start_loc, b->seq_lens, b->req_id_per_token, b->num_reqs,
+                               ws.hist_rows, b->num_tokens, topk, out, phys, nullptr, 0, stream));
   if (ss != nullptr) {
     const int j = from_cuda(cudaStreamWaitEvent(stream, ss->join, 0));
     if (st == DSA_OK) st = j;
@@ -483,7 +554,7 @@ int dsa_indexer_plan(const DsaBatch* batch, void* ws, size_t ws_bytes, int32_t* 
   if (ws_bytes < w.bytes) return DSA_ENOSPACE;
   int sms;
   if ((st = device_sms(&sms)) != DSA_OK) return st;
-  return from_cuda(launch_prologue(plan_only(batch, w, sms, nullptr, nullptr, nullptr, dev_err), stream));
+  return from_cuda(launch_prologue(plan_only(batch, w, sms, grid_ctas(sms), nullptr, nullptr, nullptr, dev_err), stream));
 }
 
 int dsa_set_launch_events(void* const* events, int32_t n_events) {
@@ -542,7 +613,8 @@ int dsa_indexer_logits_topk(const DsaBatch* batch, const uint8_t* q_fp8, const f
   if ((st = device_sms(&sms)) != DSA_OK) return st;
   // one launch: this step's K into the cache (if given), the plan, zeroed histograms
   if ((st = mark(stream)) != DSA_OK) return st;
-  st = launched(launch_prologue(plan_only(batch, w, sms, k_new, slot_mapping, k_cache, dev_err), stream), stream);
+  st = launched(launch_prologue(plan_only(batch, w, sms, grid_ctas(sms), k_new, slot_mapping, k_cache, dev_err), stream),
+                stream);
   if (st != DSA_OK) return st;
   const int64_t ld = logits_ld(batch);
   st = run_logits(batch, q_fp8, w_folded, k_cache, w.logits, ld, w, true, dev_err, stream);
@@ -607,6 +679,16 @@ size_t dsa_layer_stack_workspace_size(const DsaBatch* batch, int32_t topk) {
   return bytes + dsa_indexer_workspace_size(batch, topk);
 }
 
+int dsa_layer_stack_decode_sms(const DsaStackPlan* plan, const DsaBatch* batch, int32_t* decode_sms) {
+  if (plan == nullptr || decode_sms == nullptr) return DSA_EINVAL;
+  int st = check_batch(batch);
+  if (st != DSA_OK) return st;
+  int sms = 0;
+  if ((st = device_sms(&sms)) != DSA_OK) return st;
+  *decode_sms = batch->num_tokens > 0 ? decode_split(plan, batch, sms) : 0;
+  return DSA_OK;
+}
+
 int dsa_layer_stack_run(const DsaStackPlan* plan, const DsaBatch* batch, const int64_t* slot_mapping,
                         int32_t* topk_buf, int32_t* phys_buf, int32_t* valid_buf, dsa_layer_consumer_fn consumer,
                         void* user, void* ws, size_t ws_bytes, int32_t* dev_err, dsa_stream_t stream) {
@@ -644,6 +726,8 @@ int dsa_layer_stack_run(const DsaStackPlan* plan, const DsaBatch* batch, const i
   int sms = 0;
   if (batch->num_tokens > 0 && (st = device_sms(&sms)) != DSA_OK) return st;
   const float softmax_scale = plan->softmax_scale > 0.0f ? plan->softmax_scale : 0.08838834764831845f;
+  // decode and prefill scores side by side on split SMs, when the caller gave the work
+  const int split = batch->num_tokens > 0 ? decode_split(plan, batch, sms) : 0;
   bool planned = false;
   int32_t producer = 0;
   for (int32_t l = 0; l < plan->n_layers; ++l) {
@@ -655,7 +739,8 @@ int dsa_layer_stack_run(const DsaStackPlan* plan, const DsaBatch* batch, const i
         // (first F layer only: the batch layout is the same for every layer) the
         // prefill plan
         // (histograms and counters of the decode rows zeroed for this layer's top-k)
-        PrologueArgs pa = plan_only(batch, w, sms, L.k_new, slot_mapping, L.k_cache, dev_err);
+        PrologueArgs pa = plan_only(batch, w, sms, split > 0 ? sms - split : grid_ctas(sms), L.k_new, slot_mapping,
+                                    L.k_cache, dev_err);
         pa.q = static_cast<const __nv_bfloat16*>(L.q);
         pa.w = L.w;
         pa.w_bf16 = L.w_dtype == DSA_W_BF16;
@@ -673,9 +758,12 @@ int dsa_layer_stack_run(const DsaStackPlan* plan, const DsaBatch* batch, const i
         // S3 with S5 fused into its output pass: logical ids, physical ids, valid counts
         TopkPhys tp{batch->block_table, batch->bt_stride,
                     plan->block_stride_rows > 0 ? plan->block_stride_rows : kBlock, phys_buf, valid_buf, dev_err};
-        st = run_logits(batch, q8, wf, L.k_cache, w.logits, ld, w, true, dev_err, stream);
-        if (st != DSA_OK) return st;
-        st = run_topk(batch, w, ld, plan->topk, topk_buf, &tp, sms, true, stream);
+        if (split > 0) {
+          st = run_split(batch, q8, wf, L.k_cache, w, ld, plan->topk, topk_buf, &tp, sms, split, dev_err, stream);
+        } else {
+          st = run_logits(batch, q8, wf, L.k_cache, w.logits, ld, w, true, dev_err, stream);
+          if (st == DSA_OK) st = run_topk(batch, w, ld, plan->topk, topk_buf, &tp, sms, true, stream);
+        }
         if (st != DSA_OK) return st;
       }
     }

@@ -391,9 +391,26 @@ typedef struct DsaStackPlan {
   const int64_t *positions;       /* device int64 [T] */
   const float *rope_cos_sin;      /* device fp32 [rope_max_pos, 64] or NULL */
   int64_t rope_max_pos;
+  /* The step's work per segment, counted by the caller from its host copy of
+   * the metadata (0 = not given): decode_keys = the sum over the decode
+   * tokens of the keys each sees (its position + 1), prefill_pairs = the
+   * same sum over the prefill tokens. With both given and neither side too
+   * small, every F layer scores the decode rows on a share of the SMs while
+   * the prefill rows are scored on the rest (the decode scores are bound by
+   * HBM on the whole GPU, the prefill scores by the tensor cores), each
+   * segment's top-k following its scores; the share balances the two at
+   * per-SM rates measured on GB300. Not used while a launch timeline is set
+   * (dsa_set_launch_events times every kernel alone on the whole GPU). */
+  int64_t decode_keys;
+  int64_t prefill_pairs;
 } DsaStackPlan;
 
 DSA_API size_t dsa_layer_stack_workspace_size(const DsaBatch *batch, int32_t topk);
+/* The SMs dsa_layer_stack_run would give the decode rows' scores on this
+ * device (plan->decode_keys, plan->prefill_pairs and the batch; a launch
+ * timeline set on this thread counts), written to *decode_sms; 0 = decode and
+ * prefill scores one after the other. Host only, no launch. */
+DSA_API int dsa_layer_stack_decode_sms(const DsaStackPlan *plan, const DsaBatch *batch, int32_t *decode_sms);
 DSA_API int dsa_layer_stack_run(const DsaStackPlan *plan, const DsaBatch *batch,
                         const int64_t *slot_mapping, int32_t *topk_buf,
                         int32_t *phys_buf, int32_t *valid_buf,

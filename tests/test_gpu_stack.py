@@ -28,7 +28,7 @@ def fused_projection(hb):
 
 
 def run_stack(n_layers, freq, scale, n_decode, pattern=None, check_rows=None, fmt="fp8", strided=False,
-              block_stride_rows=0):
+              block_stride_rows=0, work=None, want_split=None):
     fs, prod = dsa.schedule_build(n_layers, True, freq, 2, pattern)
     fs_o, prod_o = oracle.schedule(n_layers, True, freq, 2, pattern)
     assert fs == fs_o and prod == prod_o.tolist()
@@ -64,8 +64,12 @@ def run_stack(n_layers, freq, scale, n_decode, pattern=None, check_rows=None, fm
         assert phys_ptr == phys_buf.data_ptr() and valid_ptr == valid_buf.data_ptr()
         seen.append((layer, producer, phys_buf.clone(), valid_buf.clone(), topk_buf.clone()))
 
-    dsa.layer_stack_run(batch, fs, layers, k, slot_mapping=slots, topk_buf=topk_buf, phys_buf=phys_buf,
-                        valid_buf=valid_buf, consumer=consumer, dev_err=err, block_stride_rows=block_stride_rows)
+    stack = dsa.LayerStack(batch, fs, layers, k, slot_mapping=slots, topk_buf=topk_buf, phys_buf=phys_buf,
+                           valid_buf=valid_buf, consumer=consumer, dev_err=err, block_stride_rows=block_stride_rows,
+                           work=work)
+    if want_split is not None:  # decode scores on a share of the SMs beside the prefill scores, or not
+        assert (stack.decode_sms() > 0) == want_split
+    stack.run()
     torch.cuda.synchronize()
     assert dsa.check_device_error(err) == 0
     assert [s[0] for s in seen] == list(range(n_layers))
@@ -96,8 +100,15 @@ def run_stack(n_layers, freq, scale, n_decode, pattern=None, check_rows=None, fm
 
 
 def test_stack_freq4_scaled():
-    fs = run_stack(9, 4, scale=0.05, n_decode=6)
+    # the batch's work is known from its host metadata: decode and prefill
+    # scores run side by side on split SMs
+    fs = run_stack(9, 4, scale=0.05, n_decode=6, want_split=True)
     assert fs == "FFSSSFSSS"
+
+
+def test_stack_freq4_scaled_one_after_the_other():
+    # no work given: decode scores, then prefill scores, each on the whole GPU
+    run_stack(5, 4, scale=0.05, n_decode=6, work=(0, 0), want_split=False)
 
 
 def test_stack_pattern_scaled():

@@ -201,3 +201,30 @@ def test_layer_inputs_strides_and_weight_dtype_checked_on_the_host():
         assert run(**bad) == binding.DSA_EINVAL, bad
     if not torch.cuda.is_available():  # on a GPU these placeholder pointers would reach the kernels
         assert run(k_row_stride=192, w_row_stride=192, w=256 + 256, w_dtype=1) == binding.DSA_ENODEV
+
+
+def test_step_work_from_host_metadata_matches_per_token_sum():
+    # decode_keys / prefill_pairs of DsaStackPlan: the keys each token sees
+    # (position + 1), summed per segment; here against the synthetic batches'
+    # own per-token positions
+    from dsa_sparse_attention_quant_gb300 import synth
+    for hb in (synth.make_batch(3, [900, 2500, 64], [(700, 500), (40, 3)], 256, with_data=False),
+               synth.stack_layer(0, scale=0.05, n_decode=6, with_data=False),
+               synth.make_batch(4, [], [(300, 300)], 64, with_data=False)):
+        dk, pp = binding.Batch.work_from_host(hb.query_start_loc, hb.seq_lens, hb.num_decodes)
+        td = int(hb.query_start_loc[hb.num_decodes])
+        keys = hb.positions.astype(np.int64) + 1
+        assert dk == int(keys[:td].sum()) and pp == int(keys[td:].sum())
+
+
+def test_decode_sms_query_needs_a_device():
+    if torch.cuda.is_available():
+        pytest.skip("checked on the GPU by the stack tests")
+    from dsa_sparse_attention_quant_gb300 import synth
+    hb = synth.make_batch(3, [900, 2500], [(700, 500)], 256, with_data=False)
+    lib = binding.load()
+    plan = binding.DsaStackPlanC()
+    plan.decode_keys, plan.prefill_pairs = binding.Batch.work_from_host(hb.query_start_loc, hb.seq_lens, hb.num_decodes)
+    out = ctypes.c_int32(-1)
+    assert lib.dsa_layer_stack_decode_sms(ctypes.byref(plan), None, ctypes.byref(out)) != 0  # no batch
+    assert lib.dsa_layer_stack_decode_sms(None, None, ctypes.byref(out)) != 0
