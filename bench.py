@@ -807,7 +807,12 @@ def run_stack(args, ranks: Ranks, with_cpu: bool):
         per_kernel = np.array([[evs[j].elapsed_time(evs[j + 1]) for j in range(len(kernels))] for evs in kev])
 
         # end to end: the F layers' q, w and new K and the step's metadata from
-        # pinned host memory, the stack, the physical ids back
+        # pinned host memory, the stack, the physical ids back. Consecutive
+        # steps alternate between two streams, each with its own device copy
+        # of the inputs and metadata and its own outputs: a step's uploads
+        # overlap the previous step's kernels, while its kernels start only
+        # after the previous step's kernels (an event). The host waits for
+        # step i's result before it enqueues step i + 2.
         host = [dict(q=L["q"].cpu().pin_memory(), w=L["w"].cpu().pin_memory(), k_new=L["k_new"].cpu().pin_memory())
                 if L is not None else None for L in l4]
         meta_host = {
@@ -817,34 +822,62 @@ def run_stack(args, ranks: Ranks, with_cpu: bool):
             "bt": torch.from_numpy(meta.block_table.astype(np.int32)).pin_memory(),
             "req": torch.from_numpy(meta.req_id_per_token.astype(np.int32)).pin_memory(),
         }
-        out_phys = torch.empty((T, k), dtype=torch.int32).pin_memory()
-        out_valid = torch.empty(T, dtype=torch.int32).pin_memory()
         h2d = sum(t.numel() * t.element_size() for h in host if h is not None for t in h.values()) + \
             sum(t.numel() * t.element_size() for t in meta_host.values())
-        d2h = out_phys.numel() * 4 + out_valid.numel() * 4
+        d2h = T * k * 4 + T * 4
+        lanes = []
+        for ln in range(2):
+            mdev = {n_: t.to(dev) for n_, t in meta_host.items()}
+            lb = dsa.Batch(mdev["qsl"], mdev["seq"], mdev["bt"], mdev["req"], meta.num_decodes, meta.num_blocks,
+                           batch.max_seq_len, batch.num_decode_tokens)
+            lb.work = batch.work
+            ll = [dict(q=torch.empty_like(L["q"]), w=torch.empty_like(L["w"]), k_new=torch.empty_like(L["k_new"]),
+                       k_cache=L["k_cache"]) if L is not None else None for L in l4]
+            o_t, o_p = torch.empty_like(topk), torch.empty_like(phys)
+            o_v = torch.empty_like(valid)
+            lanes.append(dict(
+                meta=mdev, layers=ll, phys=o_p, valid=o_v,
+                stack=dsa.LayerStack(lb, fs4, ll, k, slot_mapping=mdev["slots"], topk_buf=o_t, phys_buf=o_p,
+                                     valid_buf=o_v, ws=ws if ln == 0 else torch.empty_like(ws), dev_err=err),
+                out_phys=torch.empty((T, k), dtype=torch.int32).pin_memory(),
+                out_valid=torch.empty(T, dtype=torch.int32).pin_memory(),
+                stream=stream if ln == 0 else torch.cuda.Stream(), done=torch.cuda.Event(), ready=torch.cuda.Event()))
+        issued = []
 
         def e2e_step():
-            for L, h in zip(l4, host):
-                if L is None:
-                    continue
-                for pname in ("q", "w", "k_new"):
-                    L[pname].copy_(h[pname], non_blocking=True)
-            slots.copy_(meta_host["slots"], non_blocking=True)
-            batch.query_start_loc.copy_(meta_host["qsl"], non_blocking=True)
-            batch.seq_lens.copy_(meta_host["seq"], non_blocking=True)
-            batch.block_table.copy_(meta_host["bt"], non_blocking=True)
-            batch.req_id_per_token.copy_(meta_host["req"], non_blocking=True)
-            run(fs4, l4)
-            out_phys.copy_(phys, non_blocking=True)
-            out_valid.copy_(valid, non_blocking=True)
-            torch.cuda.current_stream().synchronize()
+            i = len(issued)
+            lane = lanes[i % 2]
+            st = lane["stream"]
+            with torch.cuda.stream(st):
+                for L, h in zip(lane["layers"], host):
+                    if L is None:
+                        continue
+                    for pname in ("q", "w", "k_new"):
+                        L[pname].copy_(h[pname], non_blocking=True)
+                for n_, t in meta_host.items():
+                    lane["meta"][n_].copy_(t, non_blocking=True)
+                if issued:
+                    st.wait_event(lanes[(i - 1) % 2]["done"])  # one step's kernels at a time
+                lane["stack"].run(st)
+                lane["done"].record(st)
+                lane["out_phys"].copy_(lane["phys"], non_blocking=True)
+                lane["out_valid"].copy_(lane["valid"], non_blocking=True)
+                lane["ready"].record(st)
+            issued.append(i)
+            if i >= 1:
+                lanes[(i - 1) % 2]["ready"].synchronize()  # step i - 1's result is on the host
+
+        def e2e_drain():
+            lanes[(len(issued) - 1) % 2]["ready"].synchronize()
 
         for _ in range(args.warmup):
             e2e_step()
+        e2e_drain()
         barrier(ranks)
         e0 = time.perf_counter()
         for _ in range(args.steps):
             e2e_step()
+        e2e_drain()
         e2e_s = max_over_ranks((time.perf_counter() - e0) / args.steps, dev)
     torch.cuda.synchronize()
     if dsa.check_device_error(err):
@@ -906,8 +939,10 @@ def run_stack(args, ranks: Ranks, with_cpu: bool):
         "e2e": {"value": whole_job_rate(pairs, world, e2e_s), "unit": "pairs/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
                 "path": "per step: the F layers' q, w and new K and the step's metadata copied from pinned host "
-                        "memory, the 61-layer stack (one C call), physical ids and valid counts copied back, "
-                        "synchronised"},
+                        "memory, the 61-layer stack (one C call), physical ids and valid counts copied back; "
+                        "steps alternate between two streams with their own device inputs and outputs (a step's "
+                        "uploads overlap the previous step's kernels, its kernels follow them), the host waits for "
+                        "each step's result before it enqueues the step after next"},
         "gpu_launches": args.steps * len(kernels) * n_f,
         "clocks": clocks.summary(),
         "wall_s_timed_region": wall1 - wall0,
