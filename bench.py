@@ -732,6 +732,8 @@ def run_stack(args, ranks: Ranks, with_cpu: bool):
     meta = synth.stack_layer(0, with_data=False)
     T, k = meta.num_tokens, meta.topk
     batch = dsa.Batch.from_host(meta, dev)
+    if args.sm_split == "off":
+        batch.work = (0, 0)  # no work given: decode and prefill scores one after the other
     slots = torch.from_numpy(meta.slot_mapping).to(dev)
     n_layers = args.stack_layers
     fs4, _ = dsa.schedule_build(n_layers, True, STACK_FREQ)
@@ -1170,6 +1172,9 @@ def main(argv=None):
                     help="indexer K cache: FP8 (132 B/slot) or FP4 E2M1 (68 B/slot)")
     ap.add_argument("--rope", action="store_true",
                     help="q and new K arrive un-rotated; the layer prologue applies RoPE before quantising")
+    ap.add_argument("--sm-split", choices=["auto", "off"], default="auto",
+                    help="stack61: score each F layer's decode rows on a share of the SMs beside its prefill rows "
+                         "(auto, from the step's work) or one after the other on the whole GPU (off)")
     ap.add_argument("--dry-run", action="store_true",
                     help="no GPU: exercise the rank launcher and the slowest-rank timing on CPU (gloo)")
     argv = sys.argv[1:] if argv is None else argv
