@@ -19,8 +19,12 @@ from tests.gpu_harness import DEV, bf16_tensor
 pytestmark = pytest.mark.gpu
 
 
-def test_captured_layer_run_replays_on_new_inputs():
-    shape = ([900, 2500, 64], [(700, 500)])
+@pytest.mark.parametrize("split", [False, True])
+def test_captured_layer_run_replays_on_new_inputs(split):
+    # split: decode rows heavy enough that the runner scores them on a share of
+    # the SMs beside the prefill rows, so the capture holds the side stream's
+    # fork and join
+    shape = ([3000] * 8, [(300, 300)]) if split else ([900, 2500, 64], [(700, 500)])
     first = synth.make_batch(41, *shape, 256, table_seed=40)
     second = synth.make_batch(42, *shape, 256, table_seed=40)  # same metadata and pages, other values
     assert np.array_equal(first.block_table, second.block_table)
@@ -33,6 +37,7 @@ def test_captured_layer_run_replays_on_new_inputs():
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     stack = dsa.LayerStack(batch, "F", [dict(q=q, w=w, k_new=kn, k_cache=cache)], first.topk, slot_mapping=slots,
                            dev_err=err)
+    assert (stack.decode_sms() > 0) == split
     stack.run()  # first call on the device outside the capture
     torch.cuda.synchronize()
 
