@@ -35,17 +35,36 @@ struct SelState {
 };
 
 // Bin b, scanning from the top, at which the running count reaches `need`;
-// s.above = the count in bins above b. Ends with __syncthreads().
+// s.above = the count in bins above b. Ends with __syncthreads(). Each
+// thread reads its kPer bins with vector loads (hist 16-byte aligned) and
+// searches them in registers (prefill4x8k top-k 546 -> 486 us against one
+// scalar load per bin, read twice).
 template <int NT>
 __device__ void find_bin(const uint32_t* hist, uint32_t need, SelState& s) {
   static_assert(NT % 32 == 0 && NT / 32 <= 32, "block size");
   constexpr int kPer = (kSelBins + NT - 1) / NT;  // bins per thread; thread 0 holds the top bins
   const int tid = threadIdx.x;
   const int lane = tid & 31, wid = tid >> 5;
-  const int hi = kSelBins - kPer * tid;  // bins [hi - kPer, hi), clipped at 0
+  const int hi = kSelBins - kPer * tid;  // bins [hi - kPer, hi)
+  static_assert(kPer * NT == kSelBins && (kPer % 4 == 0 || kPer == 2), "vector loads of the thread's bins");
+  uint32_t v[kPer];  // v[b] = hist[hi - 1 - b]
+  if constexpr (kPer % 4 == 0) {
+#pragma unroll
+    for (int q = 0; q < kPer / 4; ++q) {
+      const uint4 w = reinterpret_cast<const uint4*>(hist + hi - kPer)[q];
+      v[kPer - 1 - 4 * q] = w.x;
+      v[kPer - 2 - 4 * q] = w.y;
+      v[kPer - 3 - 4 * q] = w.z;
+      v[kPer - 4 - 4 * q] = w.w;
+    }
+  } else {
+    const uint2 w = *reinterpret_cast<const uint2*>(hist + hi - 2);
+    v[1] = w.x;
+    v[0] = w.y;
+  }
   uint32_t local = 0;
 #pragma unroll
-  for (int b = 0; b < kPer; ++b) local += hi - 1 - b >= 0 ? hist[hi - 1 - b] : 0u;
+  for (int b = 0; b < kPer; ++b) local += v[b];
   uint32_t incl = local;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -67,8 +86,9 @@ __device__ void find_bin(const uint32_t* hist, uint32_t need, SelState& s) {
   incl += wid > 0 ? s.sm[wid - 1] : 0u;
   uint32_t above = incl - local;
   if (above < need && need <= incl) {
+#pragma unroll
     for (int b = 0; b < kPer; ++b) {
-      const uint32_t c = hi - 1 - b >= 0 ? hist[hi - 1 - b] : 0u;
+      const uint32_t c = v[b];
       if (above + c >= need) {
         s.bin = hi - 1 - b;
         s.above = above;
