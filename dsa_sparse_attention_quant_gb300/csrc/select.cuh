@@ -175,7 +175,7 @@ __device__ void resolve_boundary(CandKey cand_key, CandId cand_id, uint32_t m, u
     for (int lvl = 0; lvl < 2; ++lvl) {
       const uint32_t mask = (1u << kWidths[lvl]) - 1u;
       __syncthreads();
-      for (int b = tid; b < kSelBins; b += NT) hist[b] = 0;
+      for (int b = tid; b < kSelBins / 4; b += NT) reinterpret_cast<uint4*>(hist)[b] = make_uint4(0, 0, 0, 0);
       if (tid == 0) {
         s.bin = 0;
         s.above = 0;
@@ -305,7 +305,7 @@ __device__ void select_row_staged(const uint32_t* keys, int n, uint32_t* hist, u
     s.bin = 0;
     s.above = 0;
   }
-  for (int i = tid; i < topk; i += NT) oid[i] = 0xffffffffu;
+  for (int i = tid; i < topk / 4; i += NT) reinterpret_cast<uint4*>(oid)[i] = make_uint4(~0u, ~0u, ~0u, ~0u);
   __syncthreads();
   find_bin<NT>(hist, static_cast<uint32_t>(topk), s);
   const uint32_t b1 = static_cast<uint32_t>(s.bin);

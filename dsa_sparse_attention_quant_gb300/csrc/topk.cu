@@ -140,12 +140,13 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 4) topk_kernel(const floa
     const uint4* hrow = reinterpret_cast<const uint4*>(hist_g + static_cast<int64_t>(t) * kSelBins);
     for (int b = tid; b < kSelBins / 4; b += NT) reinterpret_cast<uint4*>(hist)[b] = __ldcg(hrow + b);
   } else {
-    for (int b = tid; b < kSelBins; b += NT) hist[b] = 0;
+    for (int b = tid; b < kSelBins / 4; b += NT) reinterpret_cast<uint4*>(hist)[b] = make_uint4(0, 0, 0, 0);
   }
   // rows are 16-byte aligned (ld is a multiple of 4): float4 loads, several in flight per thread
   const float4* l4 = reinterpret_cast<const float4*>(lrow);
   const int n4 = (n + 3) >> 2;
   if (staged) {
+    if (!have_hist) __syncthreads();  // the zeroed histogram, before the staging pass counts into it
     constexpr int U = R::kLoads;
     for (int base = 0; base < n4; base += U * NT) {
       float4 v[U];
@@ -157,15 +158,20 @@ __global__ void __launch_bounds__(NT, NT == 1024 ? 1 : 4) topk_kernel(const floa
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int i4 = base + u * NT + tid;
-        if (i4 < n4) reinterpret_cast<uint4*>(keys)[i4] =
-            make_uint4(f32_key(v[u].x), f32_key(v[u].y), f32_key(v[u].z), f32_key(v[u].w));
+        if (i4 < n4) {
+          const uint4 k = make_uint4(f32_key(v[u].x), f32_key(v[u].y), f32_key(v[u].z), f32_key(v[u].w));
+          reinterpret_cast<uint4*>(keys)[i4] = k;
+          if (!have_hist) {  // pass 1 while staging: the row's keys below n
+            const int i = 4 * i4;
+            atomicAdd(&hist[k.x >> kHistShift], 1u);
+            if (i + 1 < n) atomicAdd(&hist[k.y >> kHistShift], 1u);
+            if (i + 2 < n) atomicAdd(&hist[k.z >> kHistShift], 1u);
+            if (i + 3 < n) atomicAdd(&hist[k.w >> kHistShift], 1u);
+          }
+        }
       }
     }
     __syncthreads();
-    if (!have_hist) {
-      for (int i = tid; i < n; i += NT) atomicAdd(&hist[keys[i] >> kHistShift], 1u);
-      __syncthreads();
-    }
     select_row_staged<NT>(keys, n, hist, sh + kSelBins, sh + kSelBins + R::kCand, oid, topk, R::kCand, o, s, &bad);
   } else if constexpr (NT <= 512) {  // (the 1024-thread launch stages every row: stage_cap >= ld)
     __syncthreads();
