@@ -50,8 +50,11 @@ MUTANTS = {
     "fp4_nibbles_swapped": [("(ora_e2m1_encode(x[i] / s) | (ora_e2m1_encode(x[i + 1] / s) << 4))",
                              "(ora_e2m1_encode(x[i + 1] / s) | (ora_e2m1_encode(x[i] / s) << 4))")],
     "fp4_decode_high_nibble_first": [("(4 * (d & 1))", "(4 * (1 - (d & 1)))")],
-    "fp4_fp8_page_size": [("int64_t page_bytes = (fmt == ORA_FMT_FP4) ? ORA_FP4_PAGE_BYTES : ORA_PAGE_BYTES;",
-                           "int64_t page_bytes = ORA_PAGE_BYTES;")],
+    # FP4 pages pitched without their scale block (4096 instead of 4352 bytes);
+    # a smaller pitch keeps every write inside the cache
+    "fp4_page_pitch_without_scales": [
+        ("int64_t page_bytes = (fmt == ORA_FMT_FP4) ? ORA_FP4_PAGE_BYTES : ORA_PAGE_BYTES;",
+         "int64_t page_bytes = (fmt == ORA_FMT_FP4) ? ORA_BLOCK * ORA_DIM / 2 : ORA_PAGE_BYTES;")],
     "fp4_row_read_as_fp8": [("double v = (fmt == ORA_FMT_FP4) ?", "double v = 0 ?")],
     "convert_counts_padding": [("        ++valid;\n", ""), ("        physical[t * topk + j] = -1;\n",
                                                         "        physical[t * topk + j] = -1;\n        ++valid;\n")],
