@@ -130,3 +130,41 @@ def test_stack_block_stride_rows_128():
 
 def test_stack_fused_projection_views_fp4_stride_1000():
     run_stack(5, 4, scale=0.03, n_decode=3, fmt="fp4", strided=True, block_stride_rows=1000)
+
+
+def run_layer(hb, want_split, fmt="fp8"):
+    """One F layer of ``hb`` through the runner, top-k, physical ids and valid
+    counts against the oracle."""
+    batch = dsa.Batch.from_host(hb, DEV)
+    cache = dsa.new_k_cache(hb.num_blocks, fmt, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    dsa.indexer_k_quant_write(bf16_tensor(hb.ctx_k), torch.from_numpy(hb.ctx_slots).to(DEV), cache, err)
+    layers = [dict(q=bf16_tensor(hb.q), w=torch.from_numpy(hb.w).to(DEV), k_new=bf16_tensor(hb.k_new),
+                   k_cache=cache)]
+    stack = dsa.LayerStack(batch, "F", layers, hb.topk, slot_mapping=torch.from_numpy(hb.slot_mapping).to(DEV),
+                           dev_err=err)
+    assert (stack.decode_sms() > 0) == want_split
+    topk, phys, valid = stack.run()
+    torch.cuda.synchronize()
+    assert dsa.check_device_error(err) == 0
+    ref_cache = oracle.fill_cache(hb, fmt=fmt)
+    assert np.array_equal(cache.cpu().numpy(), ref_cache)
+    rows = np.arange(hb.num_tokens)
+    _, scores = oracle.indexer(hb, ref_cache, rows=rows, with_scores=True)
+    lens = hb.positions + 1
+    topk = topk.cpu().numpy()
+    assert not compare.check_topk(topk, scores, lens, hb.topk)
+    phys, valid = phys.cpu().numpy(), valid.cpu().numpy()
+    assert np.array_equal(valid, (topk >= 0).sum(axis=1))
+    for t in rows:
+        table, _ = oracle.convert(np.arange(int(lens[t]), dtype=np.int32)[None, :], hb.req_id_per_token[t:t + 1],
+                                  hb.block_table, 64, 0)
+        assert np.array_equal(phys[t], np.where(topk[t] >= 0, table[0][np.clip(topk[t], 0, None)], -1))
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "fp4"])
+def test_split_layer_with_decode_rows_past_one_cta(fmt):
+    # decode rows longer than one CTA stages (chunk CTAs and a resolving CTA
+    # per row) on the decode share of the SMs, beside a prefill on the rest
+    hb = synth.make_batch(31, [40000, 36000, 35000, 2500], [(600, 600)], 2048)
+    run_layer(hb, want_split=True, fmt=fmt)
