@@ -751,6 +751,7 @@ int dsa_layer_stack_run(const DsaStackPlan* plan, const DsaBatch* batch, const i
         pa.q_fp8 = q8;
         pa.w_folded = wf;
         pa.plan = pa.plan && !planned;
+        pa.pdl = planned && consumer == nullptr;  // the previous kernel is then this library's top-k
         if ((st = mark(stream)) != DSA_OK) return st;
         st = launched(launch_prologue(pa, stream), stream);
         if (st != DSA_OK) return st;

@@ -111,6 +111,7 @@ struct PrologueArgs {
   uint32_t* counters;  // [hist_rows][kRowCounters]
   int hist_rows;
   int num_sms;         // SMs of the device: the grid is one wave
+  bool pdl;            // launched as a programmatic dependent of the previous kernel
   int32_t* err;
 };
 

@@ -155,6 +155,9 @@ __device__ void plan_batch(const PlanArgs& p, PlanSmem& S) {
 // share. Against a warp per q row (8-byte loads, four rows per warp) and two
 // waves, prefill4x8k's prologue took 219 -> 136 us (HBM-bound: 837 MB moved,
 // 0.91 of the measured copy bandwidth).
+// Launched as a programmatic dependent of the previous layer's top-k (pdl), it
+// quantises while that top-k's last CTAs run, and waits for it only before
+// clearing the decode rows' histograms and counters, which the top-k reads.
 constexpr int kPrologueThreads = 256;
 constexpr int kPrologueMinCtas = 5;
 
@@ -231,6 +234,9 @@ __global__ void __launch_bounds__(kPrologueThreads, kPrologueMinCtas) prologue_k
       }
       quant_store_k_row(a.k_cache, slot, raw, FP4, lane);
     } else {
+      // the previous layer's top-k may still read these rows: wait for it
+      // (the q codes, the cache rows and the plan above are not read by it)
+      pdl_wait();
       const int64_t t = j - q_groups - k_rows;
       uint4* h = reinterpret_cast<uint4*>(a.hist + t * kHistBins);
       uint4* h2 = reinterpret_cast<uint4*>(a.hist2 + t * kHistBins);
@@ -272,6 +278,9 @@ cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t stream) {
   const size_t smem = a.plan ? sizeof(PlanSmem) : 0;
   static_assert(sizeof(PlanSmem) <= 48 * 1024, "plan staging fits the default dynamic shared memory");
   const unsigned grid = static_cast<unsigned>(quant + (a.plan ? 1 : 0));
+  if (a.pdl)
+    return a.k_fp4 ? launch_pdl(prologue_kernel<true>, dim3(grid), dim3(kPrologueThreads), smem, stream, a)
+                   : launch_pdl(prologue_kernel<false>, dim3(grid), dim3(kPrologueThreads), smem, stream, a);
   if (a.k_fp4)
     prologue_kernel<true><<<grid, kPrologueThreads, smem, stream>>>(a);
   else

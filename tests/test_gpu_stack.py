@@ -168,3 +168,41 @@ def test_split_layer_with_decode_rows_past_one_cta(fmt):
     # per row) on the decode share of the SMs, beside a prefill on the rest
     hb = synth.make_batch(31, [40000, 36000, 35000, 2500], [(600, 600)], 2048)
     run_layer(hb, want_split=True, fmt=fmt)
+
+
+@pytest.mark.parametrize("work", [None, (0, 0)])
+def test_stack_without_consumer(work):
+    # no consumer: every F layer after the first starts its prologue as a
+    # programmatic dependent of the previous layer's top-k; every cache and the
+    # last F layer's ids (left in the buffers) against the oracle
+    n_layers, freq = 9, 4
+    fs, _ = dsa.schedule_build(n_layers, True, freq, 2)
+    hbs = {l: synth.stack_layer(l, 0.05, 6) for l in range(n_layers) if fs[l] == "F"}
+    meta = hbs[0]
+    batch = dsa.Batch.from_host(meta, DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    layers = []
+    for l in range(n_layers):
+        if fs[l] != "F":
+            layers.append(None)
+            continue
+        hb = hbs[l]
+        cache = dsa.new_k_cache(hb.num_blocks, device=DEV)
+        dsa.indexer_k_quant_write(bf16_tensor(hb.ctx_k), torch.from_numpy(hb.ctx_slots).to(DEV), cache, err)
+        layers.append(dict(q=bf16_tensor(hb.q), w=torch.from_numpy(hb.w).to(DEV), k_new=bf16_tensor(hb.k_new),
+                           k_cache=cache))
+    stack = dsa.LayerStack(batch, fs, layers, meta.topk, slot_mapping=torch.from_numpy(meta.slot_mapping).to(DEV),
+                           dev_err=err, work=work)
+    topk, phys, valid = stack.run()
+    torch.cuda.synchronize()
+    assert dsa.check_device_error(err) == 0
+    for l, hb in hbs.items():
+        assert np.array_equal(layers[l]["k_cache"].cpu().numpy(), oracle.fill_cache(hb)), f"layer {l}: cache bytes"
+    last = max(hbs)
+    hb = hbs[last]
+    rows = np.arange(hb.num_tokens)
+    _, scores = oracle.indexer(hb, oracle.fill_cache(hb), rows=rows, with_scores=True)
+    lens = hb.positions + 1
+    topk = topk.cpu().numpy()
+    assert not compare.check_topk(topk, scores, lens, hb.topk)
+    assert np.array_equal(valid.cpu().numpy(), (topk >= 0).sum(axis=1))
