@@ -349,14 +349,20 @@ DSA_API int dsa_gather_rows(const uint8_t *rows, int64_t num_rows, int64_t row_b
  * queued on `stream`; it may enqueue its own work on the stream (the sparse
  * attention that reads the indices). 'S' layers own no indexer inputs: their
  * entries of `layers` are ignored and may be zero.
- * Streams: with decode and prefill rows in the batch, the decode rows' top-k
+ * Streams: with decode and prefill rows in the batch, part of each F layer
  * runs on a second stream of the calling host thread (created on the first
- * such call, outside stream capture; highest priority), forked from `stream`
- * after the scores and joined back to it before the layer's consumer call,
- * so every later operation on `stream` sees the layer's complete output. In
+ * such call, outside stream capture, and kept with two events for the life of
+ * the thread; highest priority): with the step's work given (decode_keys,
+ * prefill_pairs below) the decode rows' scores and top-k, forked after the
+ * layer's prologue; without it the decode rows' top-k, forked after the
+ * scores. It is joined back to `stream` before the layer's consumer call, so
+ * every later operation on `stream` sees the layer's complete output. In
  * stream capture the fork and join become graph edges. Without that second
  * stream (capture before the first such call, or a launch timeline set by
- * dsa_set_launch_events) both run on `stream`. */
+ * dsa_set_launch_events) the same kernels run on `stream` one after another.
+ * After the first F layer of a call without a consumer, each F layer's first
+ * kernel starts as a programmatic dependent of the previous layer's top-k
+ * (the inputs of every layer are the caller's, fixed for the call). */
 #define DSA_W_FP32 0
 #define DSA_W_BF16 1
 typedef struct DsaLayerInputs {
