@@ -39,16 +39,18 @@ struct SelState {
 // thread reads its kPer bins with vector loads (hist 16-byte aligned) and
 // searches them in registers (prefill4x8k top-k 546 -> 486 us against one
 // scalar load per bin, read twice).
-template <int NT>
+template <int NT, int BINS = kSelBins>
 __device__ void find_bin(const uint32_t* hist, uint32_t need, SelState& s) {
   static_assert(NT % 32 == 0 && NT / 32 <= 32, "block size");
-  constexpr int kPer = (kSelBins + NT - 1) / NT;  // bins per thread; thread 0 holds the top bins
+  constexpr int kPer = BINS / NT;  // bins per thread; thread 0 holds the top bins
   const int tid = threadIdx.x;
   const int lane = tid & 31, wid = tid >> 5;
-  const int hi = kSelBins - kPer * tid;  // bins [hi - kPer, hi)
-  static_assert(kPer * NT == kSelBins && (kPer % 4 == 0 || kPer == 2), "vector loads of the thread's bins");
+  const int hi = BINS - kPer * tid;  // bins [hi - kPer, hi)
+  static_assert(kPer * NT == BINS && (kPer % 4 == 0 || kPer <= 2), "vector loads of the thread's bins");
   uint32_t v[kPer];  // v[b] = hist[hi - 1 - b]
-  if constexpr (kPer % 4 == 0) {
+  if constexpr (kPer == 1) {
+    v[0] = hist[hi - 1];
+  } else if constexpr (kPer % 4 == 0) {
 #pragma unroll
     for (int q = 0; q < kPer / 4; ++q) {
       const uint4 w = reinterpret_cast<const uint4*>(hist + hi - kPer)[q];
@@ -169,13 +171,20 @@ __device__ void resolve_boundary(CandKey cand_key, CandId cand_id, uint32_t m, u
   const int tid = threadIdx.x;
   uint32_t prefix = b1;
   int shift = kHistShift;
-  constexpr int kShifts[2] = {10, 0};
-  constexpr int kWidths[2] = {11, 10};
+  // the key's last 21 bits: 11 + 10 with 2048 bins for 1024-thread rows;
+  // 8 + 8 + 5 with 256 bins (one per thread) for 256-thread rows, whose
+  // boundary bins hold a few hundred keys (prefill4x8k top-k 455 -> 441 us:
+  // a 256-bin search costs a fraction of a 2048-bin one)
+  constexpr bool kWide = NT >= 1024;
+  constexpr int kLevels = kWide ? 2 : 3;
+  constexpr int kBins = kWide ? kSelBins : 256;
+  constexpr int kShifts[3] = {kWide ? 10 : 13, kWide ? 0 : 5, 0};
+  constexpr int kWidths[3] = {kWide ? 11 : 8, kWide ? 10 : 8, 5};
   if (hist[b1] != need) {  // else the whole bin is taken
-    for (int lvl = 0; lvl < 2; ++lvl) {
+    for (int lvl = 0; lvl < kLevels; ++lvl) {
       const uint32_t mask = (1u << kWidths[lvl]) - 1u;
       __syncthreads();
-      for (int b = tid; b < kSelBins / 4; b += NT) reinterpret_cast<uint4*>(hist)[b] = make_uint4(0, 0, 0, 0);
+      for (int b = tid; b < kBins / 4; b += NT) reinterpret_cast<uint4*>(hist)[b] = make_uint4(0, 0, 0, 0);
       if (tid == 0) {
         s.bin = 0;
         s.above = 0;
@@ -186,7 +195,7 @@ __device__ void resolve_boundary(CandKey cand_key, CandId cand_id, uint32_t m, u
         if ((k >> shift) == prefix) atomicAdd(&hist[(k >> kShifts[lvl]) & mask], 1u);
       }
       __syncthreads();
-      find_bin<NT>(hist, need, s);
+      find_bin<NT, kBins>(hist, need, s);
       const int b = s.bin;
       need -= s.above;
       prefix = (prefix << kWidths[lvl]) | static_cast<uint32_t>(b);
