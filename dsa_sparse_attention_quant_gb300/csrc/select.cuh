@@ -32,10 +32,12 @@ struct SelState {
   uint32_t sm[33];  // scan scratch
   int bin;
   uint32_t above, cnt, eq;
+  uint32_t binc;  // the count in bin `bin`
 };
 
 // Bin b, scanning from the top, at which the running count reaches `need`;
-// s.above = the count in bins above b. Ends with __syncthreads(). Each
+// s.above = the count in bins above b, s.binc = the count in b. Ends with
+// __syncthreads(), after which hist is no longer read. Each
 // thread reads its kPer bins with vector loads (hist 16-byte aligned) and
 // searches them in registers (prefill4x8k top-k 546 -> 486 us against one
 // scalar load per bin, read twice).
@@ -75,17 +77,8 @@ __device__ void find_bin(const uint32_t* hist, uint32_t need, SelState& s) {
   }
   if (lane == 31) s.sm[wid] = incl;
   __syncthreads();
-  if (wid == 0) {
-    uint32_t x = lane < NT / 32 ? s.sm[lane] : 0u;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t v = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += v;
-    }
-    if (lane < NT / 32) s.sm[lane] = x;
-  }
-  __syncthreads();
-  incl += wid > 0 ? s.sm[wid - 1] : 0u;
+  // every warp sums the totals of the warps before it (one barrier, not two)
+  incl += __reduce_add_sync(0xffffffffu, lane < wid ? s.sm[lane] : 0u);
   uint32_t above = incl - local;
   if (above < need && need <= incl) {
 #pragma unroll
@@ -94,12 +87,32 @@ __device__ void find_bin(const uint32_t* hist, uint32_t need, SelState& s) {
       if (above + c >= need) {
         s.bin = hi - 1 - b;
         s.above = above;
+        s.binc = c;
         break;
       }
       above += c;
     }
   }
   __syncthreads();
+}
+
+// Exclusive prefix sum of v over the block and the block's total, with one
+// barrier: every warp sums the totals of the warps before it. sm (NT/32
+// words) must not be rewritten before a later barrier.
+template <int NT>
+__device__ __forceinline__ uint32_t block_excl_sum(uint32_t v, uint32_t* sm, uint32_t* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  if (lane == 31) sm[wid] = incl;
+  __syncthreads();
+  const uint32_t w = lane < NT / 32 ? sm[lane] : 0u;
+  *total = __reduce_add_sync(0xffffffffu, w);
+  return incl - v + __reduce_add_sync(0xffffffffu, lane < wid ? w : 0u);
 }
 
 // Where a row's ids go: logical ids, and optionally physical slots.
@@ -160,55 +173,72 @@ __device__ void write_ids(const uint32_t* oid, int topk, const RowOut& o, bool* 
   }
 }
 
+// Levels that resolve the key's last 21 bits inside the boundary bin: 11 + 10
+// bits with 2048 bins for 1024-thread rows; 8 + 8 + 5 bits with 256 bins (one
+// per thread) for 256-thread rows, whose boundary bins hold a few hundred keys
+// (prefill4x8k top-k 455 -> 441 us: a 256-bin search costs a fraction of a
+// 2048-bin one). Level l bins a key by its kWidth<l> bits from bit kShift<l> up.
+template <int NT>
+struct Levels {
+  static constexpr bool kWide = NT >= 1024;
+  static constexpr int kCount = kWide ? 2 : 3;
+  static constexpr int kBins = kWide ? kSelBins : 256;
+  static constexpr int kShift0 = kWide ? 10 : 13, kShift1 = kWide ? 0 : 5, kShift2 = 0;
+  static constexpr int kWidth0 = kWide ? 11 : 8, kWidth1 = kWide ? 10 : 8, kWidth2 = 5;
+  __device__ static __forceinline__ uint32_t first_bin(uint32_t key) {
+    return (key >> kShift0) & ((1u << kWidth0) - 1u);
+  }
+};
+
 // Passes 2 and 3 on the boundary bin b1's keys cand_key(0..m) (ids cand_id),
-// of which `need` are still to be taken after the n_up keys above the bin;
-// the keys above the k-th and as many ties as needed go to put(position, id)
-// at positions n_up, n_up + 1, ... (below topk). hist holds pass 1 of the
-// row on entry and is reused.
-template <int NT, typename CandKey, typename CandId, typename Put>
-__device__ void resolve_boundary(CandKey cand_key, CandId cand_id, uint32_t m, uint32_t b1, uint32_t need,
-                                 uint32_t n_up, uint32_t* hist, Put put, int topk, SelState& s) {
+// bin_count of them, of which `need` are still to be taken after the n_up keys
+// above the bin; the keys above the k-th and as many ties as needed go to
+// put(position, id) at positions n_up, n_up + 1, ... (below topk). hist is
+// reused for the levels' histograms. With kFirstBuilt the caller has already
+// binned the bin's keys by Levels<NT>::first_bin into hist, reset s.bin,
+// s.above, s.cnt = n_up and s.eq = 0, and synchronised; else hist holds pass 1
+// on entry.
+template <int NT, bool kFirstBuilt, typename CandKey, typename CandId, typename Put>
+__device__ void resolve_boundary(CandKey cand_key, CandId cand_id, uint32_t m, uint32_t b1, uint32_t bin_count,
+                                 uint32_t need, uint32_t n_up, uint32_t* hist, Put put, int topk, SelState& s) {
+  using L = Levels<NT>;
+  constexpr int kShifts[3] = {L::kShift0, L::kShift1, L::kShift2};
+  constexpr int kWidths[3] = {L::kWidth0, L::kWidth1, L::kWidth2};
   const int tid = threadIdx.x;
   uint32_t prefix = b1;
   int shift = kHistShift;
-  // the key's last 21 bits: 11 + 10 with 2048 bins for 1024-thread rows;
-  // 8 + 8 + 5 with 256 bins (one per thread) for 256-thread rows, whose
-  // boundary bins hold a few hundred keys (prefill4x8k top-k 455 -> 441 us:
-  // a 256-bin search costs a fraction of a 2048-bin one)
-  constexpr bool kWide = NT >= 1024;
-  constexpr int kLevels = kWide ? 2 : 3;
-  constexpr int kBins = kWide ? kSelBins : 256;
-  constexpr int kShifts[3] = {kWide ? 10 : 13, kWide ? 0 : 5, 0};
-  constexpr int kWidths[3] = {kWide ? 11 : 8, kWide ? 10 : 8, 5};
-  if (hist[b1] != need) {  // else the whole bin is taken
-    for (int lvl = 0; lvl < kLevels; ++lvl) {
+  if (!kFirstBuilt && tid == 0) {  // ordered before the placement below by the syncs that follow
+    s.cnt = n_up;
+    s.eq = 0;
+  }
+  bool synced = kFirstBuilt;
+  if (bin_count != need) {  // else the whole bin is taken
+    for (int lvl = 0; lvl < L::kCount; ++lvl) {
       const uint32_t mask = (1u << kWidths[lvl]) - 1u;
-      __syncthreads();
-      for (int b = tid; b < kBins / 4; b += NT) reinterpret_cast<uint4*>(hist)[b] = make_uint4(0, 0, 0, 0);
-      if (tid == 0) {
-        s.bin = 0;
-        s.above = 0;
+      if (!kFirstBuilt || lvl > 0) {
+        __syncthreads();
+        for (int b = tid; b < L::kBins / 4; b += NT) reinterpret_cast<uint4*>(hist)[b] = make_uint4(0, 0, 0, 0);
+        if (tid == 0) {
+          s.bin = 0;
+          s.above = 0;
+        }
+        __syncthreads();
+        for (uint32_t j = tid; j < m; j += NT) {
+          const uint32_t k = cand_key(j);
+          if ((k >> shift) == prefix) atomicAdd(&hist[(k >> kShifts[lvl]) & mask], 1u);
+        }
+        __syncthreads();
       }
-      __syncthreads();
-      for (uint32_t j = tid; j < m; j += NT) {
-        const uint32_t k = cand_key(j);
-        if ((k >> shift) == prefix) atomicAdd(&hist[(k >> kShifts[lvl]) & mask], 1u);
-      }
-      __syncthreads();
-      find_bin<NT, kBins>(hist, need, s);
+      find_bin<NT, L::kBins>(hist, need, s);
+      synced = true;
       const int b = s.bin;
       need -= s.above;
       prefix = (prefix << kWidths[lvl]) | static_cast<uint32_t>(b);
       shift = kShifts[lvl];
-      if (hist[b] == need) break;
+      if (s.binc == need) break;
     }
   }
-  __syncthreads();
-  if (tid == 0) {
-    s.cnt = n_up;
-    s.eq = 0;
-  }
-  __syncthreads();
+  if (!synced) __syncthreads();
   for (uint32_t j0 = 0; j0 < m; j0 += NT) {
     const uint32_t j = j0 + tid;
     const uint32_t k = j < m ? cand_key(j) : 0u;
@@ -246,8 +276,8 @@ __device__ void select_row(KeyAt key_at, int n, uint32_t* hist, uint32_t* ckey, 
   __syncthreads();
   find_bin<NT>(hist, static_cast<uint32_t>(topk), s);
   const uint32_t b1 = static_cast<uint32_t>(s.bin);
-  const uint32_t n_up = s.above;
-  const bool gather = hist[b1] <= cap;
+  const uint32_t n_up = s.above, bin_count = s.binc;
+  const bool gather = bin_count <= cap;
 
   const int per = ((n + kWarps - 1) / kWarps + 31) & ~31;
   const int lo = wid * per, hi = min(n, lo + per);
@@ -294,32 +324,50 @@ __device__ void select_row(KeyAt key_at, int n, uint32_t* hist, uint32_t* ckey, 
   __syncthreads();
   // the boundary bin: candidates j < m (or, past cap, the row filtered to the bin)
   const uint32_t m = gather ? min(total_eq, cap) : static_cast<uint32_t>(n);
-  resolve_boundary<NT>([&](uint32_t j) -> uint32_t { return gather ? ckey[j] : key_at(static_cast<int>(j)); },
-                       [&](uint32_t j) -> uint32_t { return gather ? cidx[j] : j; }, m, b1,
-                       static_cast<uint32_t>(topk) - n_up, n_up, hist,
-                       [&](uint32_t pos, uint32_t id) { oid[pos] = id; }, topk, s);
+  resolve_boundary<NT, false>([&](uint32_t j) -> uint32_t { return gather ? ckey[j] : key_at(static_cast<int>(j)); },
+                              [&](uint32_t j) -> uint32_t { return gather ? cidx[j] : j; }, m, b1, bin_count,
+                              static_cast<uint32_t>(topk) - n_up, n_up, hist,
+                              [&](uint32_t pos, uint32_t id) { oid[pos] = id; }, topk, s);
   write_ids<NT>(oid, topk, o, bad);
   __syncthreads();
 }
 
-// Top `topk` of the kTopkRowCap >= n > topk keys staged in shared memory
-// (keys, 16-byte aligned), written through o. Thread i owns a contiguous
-// range of 4*q keys (q odd: the 16-byte loads of a warp hit distinct banks);
-// one block scan of the packed counts gives every thread its offsets.
+// Before the staging pass's closing __syncthreads() of a row that
+// select_row_staged will take: the ids' slots emptied, the scan state reset.
 template <int NT>
-__device__ void select_row_staged(const uint32_t* keys, int n, uint32_t* hist, uint32_t* ckey, uint32_t* cidx,
-                                  uint32_t* oid, int topk, uint32_t cap, const RowOut& o, SelState& s, bool* bad) {
-  const int tid = threadIdx.x;
-  if (tid == 0) {
+__device__ __forceinline__ void select_staged_init(uint32_t* oid, int topk, SelState& s) {
+  if (threadIdx.x == 0) {
     s.bin = 0;
     s.above = 0;
   }
-  for (int i = tid; i < topk / 4; i += NT) reinterpret_cast<uint4*>(oid)[i] = make_uint4(~0u, ~0u, ~0u, ~0u);
-  __syncthreads();
+  for (int i = threadIdx.x; i < topk / 4; i += NT) reinterpret_cast<uint4*>(oid)[i] = make_uint4(~0u, ~0u, ~0u, ~0u);
+}
+
+// Top `topk` of the kTopkRowCap >= n > topk keys staged in shared memory
+// (keys, 16-byte aligned), written through o; select_staged_init ran before
+// the sync that ended the staging. Thread i owns a contiguous range of 4*q
+// keys (q odd: the 16-byte loads of a warp hit distinct banks); one block
+// scan of the packed counts gives every thread its offsets. In 1024-thread
+// rows the placement pass also bins the boundary bin's keys for the first
+// resolving level, into hist, which pass 1 no longer needs once the boundary
+// bin is known: one pass and three barriers fewer (decode32 top-k 11.8 ->
+// 11.2 us). 256-thread rows gather a few hundred candidates, and a pass over
+// them costs less than the counts in the placement (prefill4x8k top-k 430
+// against 433 us).
+template <int NT>
+__device__ void select_row_staged(const uint32_t* keys, int n, uint32_t* hist, uint32_t* ckey, uint32_t* cidx,
+                                  uint32_t* oid, int topk, uint32_t cap, const RowOut& o, SelState& s, bool* bad) {
+  using L = Levels<NT>;
+  constexpr bool kFuse = L::kWide;
+  const int tid = threadIdx.x;
   find_bin<NT>(hist, static_cast<uint32_t>(topk), s);
   const uint32_t b1 = static_cast<uint32_t>(s.bin);
-  const uint32_t n_up = s.above;
-  const bool gather = hist[b1] <= cap;
+  const uint32_t n_up = s.above, bin_count = s.binc;
+  const bool gather = bin_count <= cap;
+  // hist is no longer read: clear it for the first level (ordered before the
+  // placement's counts by the scan's barrier)
+  if constexpr (kFuse)
+    for (int b = tid; b < L::kBins / 4; b += NT) reinterpret_cast<uint4*>(hist)[b] = make_uint4(0, 0, 0, 0);
 
   int q4 = ((n + NT - 1) / NT + 3) >> 2;
   q4 += (q4 & 1) ^ 1;  // odd
@@ -338,11 +386,16 @@ __device__ void select_row_staged(const uint32_t* keys, int n, uint32_t* hist, u
     }
   }
   // counts <= kTopkRowCap < 2^16: up in the high half, boundary-bin keys in the low
-  int total;
-  const int packed = (c_up << 16) | c_eq;
-  const int excl = block_scan_incl(packed, reinterpret_cast<int*>(s.sm), &total) - packed;
-  uint32_t p_up = static_cast<uint32_t>(excl) >> 16, p_eq = static_cast<uint32_t>(excl) & 0xffffu;
-  const uint32_t total_eq = static_cast<uint32_t>(total) & 0xffffu;
+  uint32_t total;
+  const uint32_t excl = block_excl_sum<NT>((static_cast<uint32_t>(c_up) << 16) | static_cast<uint32_t>(c_eq), s.sm, &total);
+  uint32_t p_up = excl >> 16, p_eq = excl & 0xffffu;
+  const uint32_t total_eq = total & 0xffffu;
+  if (tid == 0) {  // every thread read s.bin, s.above and s.binc before the scan's barrier
+    s.bin = 0;
+    s.above = 0;
+    s.cnt = n_up;
+    s.eq = 0;
+  }
   for (int i = lo; i < hi; i += 4) {
     const uint4 v = k4[i >> 2];
     const uint32_t kk[4] = {v.x, v.y, v.z, v.w};
@@ -351,8 +404,10 @@ __device__ void select_row_staged(const uint32_t* keys, int n, uint32_t* hist, u
       const uint32_t bin = kk[c] >> kHistShift;
       const bool in = i + c < hi;
       const bool up = in && bin > b1;
-      const bool eq = in && gather && bin == b1;
+      const bool in_bin = in && bin == b1;
+      const bool eq = in_bin && gather;
       if (up && p_up < static_cast<uint32_t>(topk)) oid[p_up] = static_cast<uint32_t>(i + c);
+      if (kFuse && in_bin) atomicAdd(&hist[L::first_bin(kk[c])], 1u);
       if (eq && p_eq < cap) {
         ckey[p_eq] = kk[c];
         cidx[p_eq] = static_cast<uint32_t>(i + c);
@@ -363,10 +418,10 @@ __device__ void select_row_staged(const uint32_t* keys, int n, uint32_t* hist, u
   }
   __syncthreads();
   const uint32_t m = gather ? min(total_eq, cap) : static_cast<uint32_t>(n);
-  resolve_boundary<NT>([&](uint32_t j) -> uint32_t { return gather ? ckey[j] : keys[j]; },
-                       [&](uint32_t j) -> uint32_t { return gather ? cidx[j] : j; }, m, b1,
-                       static_cast<uint32_t>(topk) - n_up, n_up, hist,
-                       [&](uint32_t pos, uint32_t id) { oid[pos] = id; }, topk, s);
+  resolve_boundary<NT, kFuse>([&](uint32_t j) -> uint32_t { return gather ? ckey[j] : keys[j]; },
+                              [&](uint32_t j) -> uint32_t { return gather ? cidx[j] : j; }, m, b1, bin_count,
+                              static_cast<uint32_t>(topk) - n_up, n_up, hist,
+                              [&](uint32_t pos, uint32_t id) { oid[pos] = id; }, topk, s);
   write_ids<NT>(oid, topk, o, bad);
   __syncthreads();
 }
