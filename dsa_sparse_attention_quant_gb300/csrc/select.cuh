@@ -124,18 +124,55 @@ struct RowOut {
   int stride_rows;
 };
 
-__device__ __forceinline__ void emit(const RowOut& o, uint32_t pos, int id, bool* bad) {
-  o.orow[pos] = id;
-  if (o.prow != nullptr) {
-    const int64_t page = id / kBlock;
-    const int32_t blk = page < o.bt_stride ? o.bt_row[page] : -1;
-    if (blk < 0) *bad = true;
-    o.prow[pos] = blk < 0 ? -1 : blk * o.stride_rows + id % kBlock;
-  }
+// Physical slot of logical id `id` >= 0 through the row's block table; -1,
+// flagged, when its page has no block.
+__device__ __forceinline__ int32_t phys_of(const RowOut& o, int id, bool* bad) {
+  const int64_t page = id / kBlock;
+  const int32_t blk = page < o.bt_stride ? o.bt_row[page] : -1;
+  if (blk < 0) *bad = true;
+  return blk < 0 ? -1 : blk * o.stride_rows + id % kBlock;
 }
 
-// Rows with at most k visible keys: every key, then -1.
+__device__ __forceinline__ void emit(const RowOut& o, uint32_t pos, int id, bool* bad) {
+  o.orow[pos] = id;
+  if (o.prow != nullptr) o.prow[pos] = phys_of(o, id, bad);
+}
+
+// Whether a row's ids can go out in 16-byte stores: k a multiple of 4 (the
+// library requires it) and both output rows 16-byte aligned (required of the
+// caller's buffers, checked here as well).
+__device__ __forceinline__ bool rows_vec4(const RowOut& o, int topk) {
+  return (topk & 3) == 0 && ((reinterpret_cast<uintptr_t>(o.orow) | reinterpret_cast<uintptr_t>(o.prow)) & 15u) == 0;
+}
+
+// Rows with at most k visible keys: every key, then -1. Four consecutive ids
+// per thread and 16-byte stores: the four lie in one page, so they take one
+// block-table entry (prefill4x8k, whose 32768 rows hold 8192 short ones:
+// top-k 417 -> 413 us). The same 16-byte stores for the selected ids, four
+// block-table lookups per thread, spilled registers in the 256-thread kernel
+// and ran slower (425 us).
 __device__ __forceinline__ void write_short_row(int n, int topk, const RowOut& o, bool* bad) {
+  if (rows_vec4(o, topk)) {
+#pragma unroll 2
+    for (int i = 4 * static_cast<int>(threadIdx.x); i < topk; i += 4 * static_cast<int>(blockDim.x)) {
+      reinterpret_cast<int4*>(o.orow)[i >> 2] =
+          make_int4(i < n ? i : -1, i + 1 < n ? i + 1 : -1, i + 2 < n ? i + 2 : -1, i + 3 < n ? i + 3 : -1);
+      if (o.prow != nullptr) {
+        int4 p = make_int4(-1, -1, -1, -1);
+        if (i < n) {
+          const int64_t page = i / kBlock;
+          const int32_t blk = page < o.bt_stride ? o.bt_row[page] : -1;
+          if (blk < 0) *bad = true;
+          if (blk >= 0) {
+            const int b = blk * o.stride_rows + i % kBlock;
+            p = make_int4(b, i + 1 < n ? b + 1 : -1, i + 2 < n ? b + 2 : -1, i + 3 < n ? b + 3 : -1);
+          }
+        }
+        reinterpret_cast<int4*>(o.prow)[i >> 2] = p;
+      }
+    }
+    return;
+  }
   for (int i = threadIdx.x; i < topk; i += blockDim.x) {
     if (i < n) {
       emit(o, i, i, bad);
