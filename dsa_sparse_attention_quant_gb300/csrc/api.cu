@@ -105,6 +105,23 @@ int make_kcache_map(CUtensorMap* m, const uint8_t* cache, int64_t num_blocks, bo
   return r == CUDA_SUCCESS ? DSA_OK : DSA_ECUDA;
 }
 
+// The K cache's scale rows as a 2-D fp32 tensor {64, num_blocks}: row p is
+// page p's 64 scales (after its codes); one-row boxes, for the score kernel's
+// tile::gather4 of a tile's two rows.
+int make_kscale_map(CUtensorMap* m, const uint8_t* cache, int64_t num_blocks, bool fp4) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  int st = tensor_map_encoder(&enc);
+  if (st != DSA_OK) return st;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kBlock), static_cast<cuuint64_t>(num_blocks)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(fp4 ? kFp4PageBytes : kPageBytes)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlock), 1};
+  cuuint32_t estr[2] = {1, 1};
+  uint8_t* scales = const_cast<uint8_t*>(cache) + (fp4 ? kFp4ScaleOffset : kScaleOffset);
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, scales, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DSA_OK : DSA_ECUDA;
+}
+
 // q codes as a 2-D byte tensor {128, T*64}: one box is `rows` head rows.
 int make_q_map(CUtensorMap* m, const uint8_t* q, int64_t n_tokens, int rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc;
@@ -251,20 +268,24 @@ int run_logits(const DsaBatch* b, const uint8_t* q_fp8, const float* w_folded, c
   int sms = 0;
   int st = device_sms(&sms);
   if (st != DSA_OK) return st;
-  CUtensorMap mk, mq1, mq4;
+  CUtensorMap mk, ms, mq1, mq4;
   const bool fp4 = kcache_fp4(b);
   if ((st = make_kcache_map(&mk, k_cache, b->num_blocks, fp4)) != DSA_OK) return st;
+  if ((st = make_kscale_map(&ms, k_cache, b->num_blocks, fp4)) != DSA_OK) return st;
   LogitsArgs a{w_folded,          k_cache,    b->block_table,   b->bt_stride,   b->num_blocks,
                logits,            ld,         hist ? ws.hist : nullptr,          hist ? ws.hist_rows : 0,
                b->query_start_loc, b->seq_lens, b->req_id_per_token, b->num_decodes, b->num_decode_tokens,
                dev_err};
   if (b->num_decodes > 0) {
     if ((st = make_q_map(&mq1, q_fp8, b->num_tokens, kHeads)) != DSA_OK) return st;
-    if ((st = launched(launch_logits(1, fp4, &mk, &mq1, SegmentPlan{}, a, grid_ctas(sms), stream), stream)) != DSA_OK) return st;
+    if ((st = launched(launch_logits(1, fp4, &mk, &ms, &mq1, SegmentPlan{}, a, grid_ctas(sms), stream), stream)) !=
+        DSA_OK)
+      return st;
   }
   if (b->num_reqs > b->num_decodes) {
     if ((st = make_q_map(&mq4, q_fp8, b->num_tokens, kPrefillTok * kHeads)) != DSA_OK) return st;
-    if ((st = launched(launch_logits(kPrefillTok, fp4, &mk, &mq4, ws.pre, a, grid_ctas(sms), stream), stream)) != DSA_OK)
+    if ((st = launched(launch_logits(kPrefillTok, fp4, &mk, &ms, &mq4, ws.pre, a, grid_ctas(sms), stream), stream)) !=
+        DSA_OK)
       return st;
   }
   return DSA_OK;
@@ -346,11 +367,14 @@ int run_topk(const DsaBatch* b, const IndexerWs& ws, int64_t ld, int32_t topk, i
 }
 
 // Per-SM rates of the score kernels on GB300, measured: a decode CTA's K-tile
-// pipeline takes about 0.34 us per 128-key tile whatever the number of CTAs
-// (decode8x128k on 40 to 100 SMs: 47-50 GB/s per SM), and on the whole GPU
-// the shared HBM holds it to about 0.40 us; the prefill kernel scores about
-// 730-890 pairs per us per SM (stack61, prefill4x8k).
-constexpr double kDecodeKeysPerSmUs = 376.0;
+// pipeline took about 0.34 us per 128-key tile whatever the number of CTAs
+// (decode8x128k on 40 to 100 SMs: 47-50 GB/s per SM) with four copies a
+// tile, and about 13% less with three (the scale rows by one gather4); on the
+// whole GPU the shared HBM holds it to about 0.40 us. The prefill kernel
+// scores about 730-890 pairs per us per SM (stack61, prefill4x8k). With these,
+// stack61's share is 49 SMs (sweep with three copies a tile: 44 / 47 / 50 / 53
+// SMs, 174.6 / 173.0 / 173.0 / 175.6 us per F layer).
+constexpr double kDecodeKeysPerSmUs = 425.0;
 constexpr double kPrefillPairsPerSmUs = 800.0;
 constexpr int kMinSplitSms = 16;
 
@@ -359,7 +383,7 @@ constexpr int kMinSplitSms = 16;
 // time at the rates above. The decode kernel on the whole GPU is bound by HBM
 // at about 35 GB/s per SM, so a share streams K at nearly the HBM rate of the
 // whole GPU's while the other SMs compute the prefill: stack61 (64 decodes at
-// 32768 keys, a 4096-token prefill, 53 of 152 SMs) 211 -> 193 us per F layer.
+// 32768 keys, a 4096-token prefill, 53 of 152 SMs at four copies a tile) 211 -> 193 us per F layer.
 int decode_split(const DsaStackPlan* plan, const DsaBatch* b, int sms) {
   if (t_count > 0) return 0;  // a launch timeline times every kernel alone, on the whole GPU
   if (plan->decode_keys <= 0 || plan->prefill_pairs <= 0 || b->num_decodes == 0 || b->num_reqs == b->num_decodes)
@@ -378,10 +402,11 @@ int decode_split(const DsaStackPlan* plan, const DsaBatch* b, int sms) {
 int run_split(const DsaBatch* b, const uint8_t* q_fp8, const float* w_folded, const uint8_t* k_cache,
               const IndexerWs& ws, int64_t ld, int32_t topk, int32_t* out, const TopkPhys* phys, int sms, int split,
               int32_t* dev_err, cudaStream_t stream) {
-  CUtensorMap mk, mq1, mq4;
+  CUtensorMap mk, ms, mq1, mq4;
   const bool fp4 = kcache_fp4(b);
   int st;
   if ((st = make_kcache_map(&mk, k_cache, b->num_blocks, fp4)) != DSA_OK) return st;
+  if ((st = make_kscale_map(&ms, k_cache, b->num_blocks, fp4)) != DSA_OK) return st;
   if ((st = make_q_map(&mq1, q_fp8, b->num_tokens, kHeads)) != DSA_OK) return st;
   if ((st = make_q_map(&mq4, q_fp8, b->num_tokens, kPrefillTok * kHeads)) != DSA_OK) return st;
   LogitsArgs a{w_folded,          k_cache,     b->block_table,       b->bt_stride,   b->num_blocks,
@@ -397,13 +422,13 @@ int run_split(const DsaBatch* b, const uint8_t* q_fp8, const float* w_folded, co
     if ((st = from_cuda(cudaStreamWaitEvent(ss->stream, ss->fork, 0))) != DSA_OK) return st;
   }
   // from here on the side stream is joined back whatever fails
-  st = from_cuda(launch_logits(1, fp4, &mk, &mq1, SegmentPlan{}, a, split, ds));
+  st = from_cuda(launch_logits(1, fp4, &mk, &ms, &mq1, SegmentPlan{}, a, split, ds));
   if (st == DSA_OK) st = from_cuda(launch_select(sa, phys, sms, ds));
   if (ss != nullptr) {
     const int r = from_cuda(cudaEventRecord(ss->join, ss->stream));
     if (st == DSA_OK) st = r;
   }
-  if (st == DSA_OK) st = from_cuda(launch_logits(kPrefillTok, fp4, &mk, &mq4, ws.pre, a, sms - split, stream));
+  if (st == DSA_OK) st = from_cuda(launch_logits(kPrefillTok, fp4, &mk, &ms, &mq4, ws.pre, a, sms - split, stream));
   if (st == DSA_OK)
     st = from_cuda(launch_topk(ws.logits, ld, b->query_start_loc, b->seq_lens, b->req_id_per_token, b->num_reqs,
                                ws.hist_rows, b->num_tokens, topk, out, phys, nullptr, 0, stream));

@@ -342,6 +342,17 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, uint64_
       : "memory");
 }
 
+// Four one-row boxes of a 2-D tensor map at rows y0..y3 (column 0), landing
+// one after the other in shared memory (tile::gather4).
+__device__ __forceinline__ void tma_gather4_2d(void* dst, const void* tmap, uint64_t* bar, int32_t y0, int32_t y1,
+                                               int32_t y2, int32_t y3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(smem_u32(bar)), "r"(0), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
+      : "memory");
+}
+
 // Untiled bulk copy global -> shared (both 16-byte aligned, size multiple of 16).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(

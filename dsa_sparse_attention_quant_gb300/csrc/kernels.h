@@ -177,9 +177,11 @@ struct SelectArgs {
 // ntok_per_block = 1 (decode segment: the kernel plans its slice from the
 // request metadata in `a`, `plan` is unused) or kPrefillTok (prefill segment,
 // `plan` written by the prologue). fp4: the K cache has FP4 pages and tmap_k
-// describes them (make_kcache_map with fp4).
-cudaError_t launch_logits(int ntok_per_block, bool fp4, const CUtensorMap* tmap_k, const CUtensorMap* tmap_q,
-                          SegmentPlan plan, const LogitsArgs& a, int num_sms, cudaStream_t stream);
+// describes them (make_kcache_map with fp4); tmap_s is the pages' scale rows
+// (make_kscale_map).
+cudaError_t launch_logits(int ntok_per_block, bool fp4, const CUtensorMap* tmap_k, const CUtensorMap* tmap_s,
+                          const CUtensorMap* tmap_q, SegmentPlan plan, const LogitsArgs& a, int num_sms,
+                          cudaStream_t stream);
 
 // Rows [row_begin, n_tokens): one CTA per row. Rows t < hist_rows take their
 // first radix pass from hist (the score kernel's histograms; may be nullptr).
