@@ -151,15 +151,18 @@ __device__ void plan_batch(const PlanArgs& p, PlanSmem& S) {
 // row: 16-byte loads, eight rows per warp in flight), the step's K into the
 // cache (a warp per row), and zero the decode rows' score histograms and
 // top-k counters. One wave: the grid is the CTAs that fit on the GPU at once
-// (five per SM at 256 threads and at most 48 registers), each looping over its
+// (four per SM at 256 threads and at most 64 registers), each looping over its
 // share. Against a warp per q row (8-byte loads, four rows per warp) and two
 // waves, prefill4x8k's prologue took 219 -> 136 us (HBM-bound: 837 MB moved,
-// 0.91 of the measured copy bandwidth).
+// 0.91 of the measured copy bandwidth). Four CTAs of up to 64 registers ran
+// 143 -> 137 us against five of 48 (stack61 unchanged); issuing the next
+// group's loads before quantising the current one ran 140 us, and 3 us slower
+// per stack61 F layer.
 // Launched as a programmatic dependent of the previous layer's top-k (pdl), it
 // quantises while that top-k's last CTAs run, and waits for it only before
 // clearing the decode rows' histograms and counters, which the top-k reads.
 constexpr int kPrologueThreads = 256;
-constexpr int kPrologueMinCtas = 5;
+constexpr int kPrologueMinCtas = 4;
 
 // FP4: the K cache has FP4 pages (a.k_fp4), fixed per instance so that the
 // K store of the other format costs no registers.
