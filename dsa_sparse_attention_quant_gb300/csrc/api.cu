@@ -383,7 +383,8 @@ constexpr int kMinSplitSms = 16;
 // time at the rates above. The decode kernel on the whole GPU is bound by HBM
 // at about 35 GB/s per SM, so a share streams K at nearly the HBM rate of the
 // whole GPU's while the other SMs compute the prefill: stack61 (64 decodes at
-// 32768 keys, a 4096-token prefill, 53 of 152 SMs at four copies a tile) 211 -> 193 us per F layer.
+// 32768 keys, a 4096-token prefill; 53 of 152 SMs at four copies a tile)
+// 211 -> 193 us per F layer.
 int decode_split(const DsaStackPlan* plan, const DsaBatch* b, int sms) {
   if (t_count > 0) return 0;  // a launch timeline times every kernel alone, on the whole GPU
   if (plan->decode_keys <= 0 || plan->prefill_pairs <= 0 || b->num_decodes == 0 || b->num_reqs == b->num_decodes)

@@ -68,7 +68,7 @@ struct LogitsCfg {
   static constexpr int kEpiWarp0 = kProducers + kMmaWarps;
   static constexpr int kThreads = 32 * kEpiWarp0 + 32 * kEpiWarps;
   static constexpr uint32_t kTmemCols = N * kAcc;         // 256 (decode) or 512 (prefill)
-  static constexpr int kStageBytes = 17 * 1024;           // 2 x 8 KB K pages, 2 x 256 B scales, 1 KB aligned
+  static constexpr int kStageBytes = 17 * 1024;           // 2 x 8 KB K pages, 4 x 256 B scale rows (gather4)
   static constexpr int kScaleOff = 16384;
   static constexpr int kQBytes = N * kDim;
   static constexpr int kWBytes = NTOK * kHeads * 4;
