@@ -233,3 +233,30 @@ def test_long_decode_rows_every_score_ties():
     for t in range(hb.num_tokens):
         hb.k_new[t] = first[t]
     check_batch(hb)
+
+
+def test_topk_output_rows_not_16_byte_aligned():
+    # the per-row top-k writes ids four at a time with 16-byte stores only when
+    # the output rows allow it; an output starting 4 bytes into a buffer takes
+    # the scalar stores, with the same result
+    hb = synth.make_batch(24, [3000, 40], [(600, 600)], 256)
+    db = DeviceBatch(hb)
+    res = db.run()  # writes this step's K into the cache
+    assert res["dev_err"] == 0
+    q8, _, wf = db.quant_fold()
+    scores = dsa.indexer_logits(db.batch, q8, wf, db.k_cache)
+    T, k = hb.num_tokens, hb.topk
+    big = torch.full((T * k + 1,), -7, dtype=torch.int32, device=DEV)
+    shifted = big[1:].view(T, k)
+    assert shifted.data_ptr() % 16 == 4
+    dsa.indexer_topk(db.batch, scores, k, topk_out=shifted)
+    torch.cuda.synchronize()
+    assert int(big[0].item()) == -7  # nothing written before the view
+    got = shifted.cpu().numpy()
+    rows = np.arange(T)
+    _, ora_scores = oracle.indexer(hb, oracle.fill_cache(hb), rows=rows, with_scores=True)
+    lens = hb.positions + 1
+    fails = compare.check_topk(got, ora_scores, lens, k)
+    assert not fails, f"top-k mismatches in {len(fails)} rows, first {fails[0]}"
+    short = lens <= k
+    assert np.array_equal(got[short], res["topk"][short])  # every key in order, then -1
